@@ -1,0 +1,505 @@
+"""Benchmark of the ternary pq2_0 x q8_K hot path on GB300.
+
+One step = one pass of the hot path over one batch of synthetic input:
+quantize the activations to q8_K, then the ternary matmul (the load-time
+repack runs once, before timing, and is reported separately). The headline
+workload is the decode GEMV (32768 x 8192 weights, 1 token), measured in
+Gweights/s; the 4-token and 64-token 17408 x 5120 tiles are measured in the
+same run in GMAC/s.
+
+Timing: inputs resident in HBM; W >= 3 warm-up steps; K timed steps replayed
+from a CUDA graph on one stream, bracketed by a barrier and a device
+synchronize, timed with CUDA events, max over ranks. Weights rotate over
+copies whose total exceeds twice the 129 MB L2, so every step streams its
+weights from HBM. The GEMV's own duration is taken from events around each of
+its launches inside the timed graph. `e2e` repeats the step through the
+Python API with host buffers: pinned host -> device copy of the activations,
+quantize, matmul, device -> pinned host copy of the outputs, every step.
+
+`--impl reference` times the plain C oracle on the host cores instead (a row
+sample of the same workload per step).
+
+Multi-GPU (torchrun): each rank runs its own copy of the workload on its own
+GPU (weak scaling, no collective on the data path); the reported time is the
+maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+PAGES_DECODE_GWEIGHTS = 390.5   # ciot README: t2x4 NEON, 32768 x 8192 matvec, 8 Oryon cores
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+WORKLOADS = {
+    "decode": "decode GEMV 32768x8192 pq2_0 x q8_K, ntok=1",
+    "small_batch": "small-batch 17408x5120 pq2_0 x q8_K, ntok=4",
+    "prefill": "prefill tile 17408x5120 pq2_0 x q8_K, ntok=64 (1% outliers x10)",
+}
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="decode", choices=list(WORKLOADS))
+    p.add_argument("--no-extra", action="store_true", help="skip the 4- and 64-token tiles")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def dist_init(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if os.environ.get("TQ_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value of x over all ranks (timing only, not the data path)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- peaks and clocks
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples every 100 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workloads
+
+def algorithmic_bytes(rows, cols, ntok):
+    """What one matmul must move: packed weights, q8_K activations, f32 outputs."""
+    w = rows * cols // 128 * 34
+    x = ntok * cols // 256 * 292
+    y = ntok * rows * 4
+    return w + x + y
+
+
+def quantize_bytes(ntok, cols):
+    return ntok * cols * 4 + ntok * cols // 256 * 292
+
+
+class Workload:
+    def __init__(self, name, device):
+        import torch
+        import bit_matvec_gb300 as tq
+        wpq, x, cfg = synth.workload(name)
+        self.name, self.cfg = name, cfg
+        self.rows, self.cols, self.ntok = cfg["rows"], cfg["cols"], cfg["ntok"]
+        W = torch.from_numpy(wpq).to(device)
+        wtq = tq.repacked_empty(self.rows, self.cols, device)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        tq.tq_repack(W, wtq, self.rows, self.cols)
+        torch.cuda.synchronize()
+        self.repack_s = time.perf_counter() - t0
+        del W
+        nbytes = wtq.numel()
+        self.copies = max(2, -(-2 * L2_BYTES // nbytes) + 1)
+        self.W = [wtq] + [wtq.clone() for _ in range(self.copies - 1)]
+        self.x_host = x
+        self.X = torch.from_numpy(x).to(device)
+        self.Xq = tq.q8K_empty(self.ntok, self.cols, device)
+        self.Y = torch.empty((self.ntok, self.rows), dtype=torch.float32, device=device)
+        self.device = device
+
+    def step(self, i, stream=None):
+        import bit_matvec_gb300 as tq
+        tq.tq_quantize_q8K(self.X, self.Xq, self.ntok, self.cols, stream)
+        tq.tq_matmul(self.W[i % self.copies], self.Xq, self.Y, self.rows, self.cols, self.ntok,
+                     stream)
+
+    def weights(self):
+        return self.rows * self.cols
+
+    def macs(self):
+        return self.rows * self.cols * self.ntok
+
+
+def time_graph(wl: Workload, steps: int, warmup: int, world: int):
+    """Device time of `steps` steps, and the matmul kernel's mean duration.
+
+    One CUDA graph holds `copies` steps (one per weight copy) with events around
+    each matmul; it is replayed ceil(steps / copies) times, and the first
+    `steps` steps are the ones counted (the graph unit is small next to K).
+    """
+    import torch
+    stream = torch.cuda.Stream(device=wl.device)
+    stream.wait_stream(torch.cuda.current_stream(wl.device))
+    n = wl.copies
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    import bit_matvec_gb300 as tq
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, 3)):                 # un-captured warm-up (kernel attributes)
+            wl.step(i, stream)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                tq.tq_quantize_q8K(wl.X, wl.Xq, wl.ntok, wl.cols, stream)
+                ev[i][0].record(stream)
+                tq.tq_matmul(wl.W[i], wl.Xq, wl.Y, wl.rows, wl.cols, wl.ntok, stream)
+                ev[i][1].record(stream)
+        reps = -(-steps // n)
+        for _ in range(max(1, warmup // n)):            # graph warm-up replays
+            g.replay()
+        stream.synchronize()
+        barrier(world)
+        torch.cuda.synchronize(wl.device)
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(reps):
+            g.replay()
+        end.record(stream)
+        stream.synchronize()
+        # matmul durations: the events inside the graph hold the last replay's times
+        kern_ms = [a.elapsed_time(b) for a, b in ev]
+        barrier(world)
+    total_ms = start.elapsed_time(end)
+    done_steps = reps * n
+    return total_ms / done_steps, statistics.mean(kern_ms), done_steps
+
+
+def time_e2e(wl: Workload, steps: int, warmup: int):
+    """Through the Python API with host buffers: H2D of X, quantize, matmul, D2H of Y."""
+    import torch
+    import bit_matvec_gb300 as tq
+    x_pin = torch.from_numpy(wl.x_host).pin_memory()
+    y_pin = torch.empty((wl.ntok, wl.rows), dtype=torch.float32).pin_memory()
+    X = torch.empty_like(wl.X)
+    stream = torch.cuda.current_stream(wl.device)
+
+    def one(i):
+        X.copy_(x_pin, non_blocking=True)
+        tq.tq_quantize_q8K(X, wl.Xq, wl.ntok, wl.cols, stream)
+        tq.tq_matmul(wl.W[i % wl.copies], wl.Xq, wl.Y, wl.rows, wl.cols, wl.ntok, stream)
+        y_pin.copy_(wl.Y, non_blocking=True)
+
+    for i in range(max(warmup, 3)):
+        one(i)
+    torch.cuda.synchronize(wl.device)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        one(i)
+    torch.cuda.synchronize(wl.device)
+    dt = time.perf_counter() - t0
+    return dt / steps, x_pin.numel() * 4, y_pin.numel() * 4
+
+
+# ---------------------------------------------------------------- oracle timing
+
+def oracle_rate(name: str, budget_s: float, rows_per_call: int | None = None):
+    """The C oracle (single-threaded) on a row sample of the workload.
+
+    Returns (units per second, unit, sample description, cores)."""
+    import oracle
+    cfg = synth.CONFIGS[name]
+    rows, cols, ntok = cfg["rows"], cfg["cols"], cfg["ntok"]
+    s = synth.seeds(cfg["index"])
+    x = synth.activations(ntok, cols, s["acts"], s["outliers"] if cfg["outliers"] else None)
+    if rows_per_call is None:
+        rows_per_call = max(1, min(rows, (1 << 22) // (cols * ntok)))
+    wsub = synth.pq2_0_weights(rows_per_call, cols, cfg["index"])
+    oracle.build()
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        xq = oracle.quantize_q8K(x)
+        oracle.matmul(wsub, xq, rows_per_call, cols)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    work = n * rows_per_call * cols * (ntok if ntok > 1 else 1)
+    unit = "Gweights/s" if ntok == 1 else "GMAC/s"
+    sample = (f"{n} calls x {rows_per_call} of {rows} rows, {cols} cols, ntok={ntok} "
+              f"(quantize + matmul each), {dt:.1f} s")
+    return work / dt / 1e9, unit, sample, 1, dt / n, rows_per_call
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the oracle on the host cores, --steps/--warmup of row samples."""
+    if rank != 0:
+        return
+    name = args.workload
+    cfg = synth.CONFIGS[name]
+    # calibrate a per-step row sample so that warm-up + steps take about a minute
+    _, _, _, _, per_call, rpc = oracle_rate(name, 1.0)
+    per_row = per_call / rpc
+    total = max(1, args.steps + args.warmup)
+    rows_step = int(max(1, min(cfg["rows"], 60.0 / total / per_row)))
+    import oracle
+    s = synth.seeds(cfg["index"])
+    x = synth.activations(cfg["ntok"], cfg["cols"], s["acts"],
+                          s["outliers"] if cfg["outliers"] else None)
+    wsub = synth.pq2_0_weights(rows_step, cfg["cols"], cfg["index"])
+    for _ in range(max(args.warmup, 0)):
+        oracle.matmul(wsub, oracle.quantize_q8K(x), rows_step, cfg["cols"])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.matmul(wsub, oracle.quantize_q8K(x), rows_step, cfg["cols"])
+    dt = time.perf_counter() - t0
+    ntok = cfg["ntok"]
+    per_step = rows_step * cfg["cols"] * ntok
+    value = per_step * args.steps / dt / 1e9
+    unit = "Gweights/s" if ntok == 1 else "GMAC/s"
+    sample = (f"each step: quantize + matmul of {rows_step} of {cfg['rows']} rows x "
+              f"{cfg['cols']} cols, ntok={ntok}")
+    line = {
+        "impl": "reference",
+        "metric": f"ternary matvec {unit} ({WORKLOADS[name]})",
+        "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int32 sums, f64 accumulation", "data": "synthetic (seeded splitmix64)",
+        "config": {"workload": WORKLOADS[name], "rows": cfg["rows"], "cols": cfg["cols"],
+                   "ntok": ntok, "sample_rows": rows_step},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- profile evidence
+
+def kernel_source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "bit_matvec_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(summary_name, files, launch_bytes_key="dram_bytes_per_launch"):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (same source hash); else None."""
+    path = os.path.join(ROOT, "profiles", summary_name)
+    try:
+        with open(path) as f:
+            kv = dict(ln.split(":", 1) for ln in f if ":" in ln and not ln.startswith("#"))
+    except OSError:
+        return None
+    kv = {k.strip(): v.strip() for k, v in kv.items()}
+    if kv.get("source_sha") != kernel_source_sha(files):
+        return None
+    try:
+        return float(kv[launch_bytes_key])
+    except (KeyError, ValueError):
+        return None
+
+
+GEMV_FILES = ("tq_gemv.cu", "tq_internal.cuh")
+TC_FILES = ("tq_gemm_tc.cu", "tq_internal.cuh")
+
+
+def measure(name, args, rank, world, device, peaks, peak_kind, steps):
+    wl = Workload(name, device)
+    step_ms, kern_ms, done = time_graph(wl, steps, args.warmup, world)
+    step_ms = max_over_ranks(step_ms, world, device)
+    abytes = algorithmic_bytes(wl.rows, wl.cols, wl.ntok)
+    res = {"workload": WORKLOADS[name], "rows": wl.rows, "cols": wl.cols, "ntok": wl.ntok,
+           "ms_per_step": step_ms, "steps": done, "weight_copies": wl.copies,
+           "repack_ms": wl.repack_s * 1e3}
+    if wl.ntok == 1:
+        res["gweights_per_s"] = world * wl.weights() / (step_ms * 1e-3) / 1e9
+    res["gmac_per_s"] = world * wl.macs() / (step_ms * 1e-3) / 1e9
+    res["hbm_gbs_step"] = (abytes + quantize_bytes(wl.ntok, wl.cols)) / (step_ms * 1e-3) / 1e9
+    if wl.ntok <= 8:
+        achieved = abytes / (kern_ms * 1e-3) / 1e9
+        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        traffic = profile_traffic(f"gemv_{name}_ncu.txt", GEMV_FILES)
+        res["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                           "frac": achieved / peak, "traffic": traffic,
+                           "kernel": "gemv_kernel", "kernel_ms": kern_ms,
+                           "algorithmic_bytes": abytes, "peak_source": peak_kind}
+    else:
+        flops = 2.0 * wl.macs()
+        achieved = flops / (kern_ms * 1e-3) / 1e12
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        traffic = profile_traffic(f"gemm_tc_{name}_ncu.txt", TC_FILES)
+        res["roofline"] = {"bound": "tensor", "achieved": achieved, "peak": peak,
+                           "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                           "kernel": "gemm_tc_kernel (tcgen05 kind::f16, exact)",
+                           "kernel_ms": kern_ms, "algorithmic_flops": flops,
+                           "peak_source": f"{peak_kind} bf16 dense (f16 runs at the bf16 rate)"}
+    return wl, res
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_init(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    from bit_matvec_gb300 import build as tq_build
+    tq_build.build()
+    peaks, peak_kind = measured_peaks()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    wl, main_res = measure(args.workload, args, rank, world, device, peaks, peak_kind, args.steps)
+    clocks.stop()
+
+    extra = {}
+    if not args.no_extra:
+        for name in ("small_batch", "prefill"):
+            if name != args.workload:
+                _, r = measure(name, args, rank, world, device, peaks, peak_kind,
+                               max(64, args.steps // 10))
+                extra[name] = r
+
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(100, min(args.steps, 5000))
+        s_per_step, h2d, d2h = time_e2e(wl, e2e_steps, args.warmup)
+        s_per_step = max_over_ranks(s_per_step, world, device)
+        units = wl.weights() if wl.ntok == 1 else wl.macs()
+        e2e = {"value": world * units / s_per_step / 1e9,
+               "unit": "Gweights/s" if wl.ntok == 1 else "GMAC/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "ms_per_step": s_per_step * 1e3}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        v, unit, sample, cores, _, _ = oracle_rate(args.workload, 10.0)
+        cpu = {"value": v, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        unit = "Gweights/s" if wl.ntok == 1 else "GMAC/s"
+        value = main_res["gweights_per_s"] if wl.ntok == 1 else main_res["gmac_per_s"]
+        line = {
+            "metric": f"ternary matvec {unit} & HBM GB/s ({WORKLOADS[args.workload]})",
+            "value": value, "unit": unit, "n_gpus": world, "steps": main_res["steps"],
+            "warmup": args.warmup, "ms_per_step": main_res["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": (value / PAGES_DECODE_GWEIGHTS
+                            if args.workload == "decode" else None),
+            "dtype": "int8" if wl.ntok <= 8 else "f16 (exact integer sums)",
+            "data": "synthetic (seeded splitmix64; no model weights)",
+            "config": {"workload": WORKLOADS[args.workload], "rows": wl.rows, "cols": wl.cols,
+                       "ntok": wl.ntok,
+                       "l2": f"{wl.copies} rotating weight copies "
+                             f"({wl.copies * wl.W[0].numel() / 1e6:.0f} MB > 2x 129 MB L2)",
+                       "timing": "CUDA graph of quantize+matmul steps, CUDA events"},
+            "hbm_gbs": main_res["hbm_gbs_step"],
+            "roofline": main_res["roofline"],
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 2 * main_res["steps"],
+            "clocks": clocks.summary(),
+            "repack_ms": main_res["repack_ms"],
+            "also": extra,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

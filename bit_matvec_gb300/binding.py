@@ -1,0 +1,188 @@
+"""ctypes binding of libtq.so: the C ABI of include/tq.h under the same names.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI. Tensors must be CUDA tensors of the current device
+(or of the device given by the first tensor argument, which is made current
+for the call); sizes are passed through unchanged, and the library's status
+codes become TQError. There is no CPU fallback: if libtq.so is missing the
+first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libtq.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "tq.h")
+
+TQ_OK = 0
+TQ_ERR_SHAPE = -1
+TQ_ERR_NULL = -2
+TQ_ERR_ALIGN = -3
+TQ_ERR_CUDA = -4
+TQ_ERR_TIMEOUT = -5
+TQ_ERR_ALIAS = -6
+
+QK_K = 256
+GROUP = 128
+PQ2_0_BYTES = 34
+Q8K_BYTES = 292
+TILE_ROWS = 32
+TILE_BYTES = 1088
+
+_lock = threading.Lock()
+_lib = None
+
+
+class TQError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        lib = _load()
+        msg = lib.tq_strerror(code).decode()
+        if code == TQ_ERR_CUDA:
+            msg += f" (cudaError {lib.tq_last_cuda_error()})"
+        super().__init__(f"{where}: {msg} [{code}]")
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/tq.h declares."""
+    with open(HEADER) as f:
+        src = f.read()
+    return re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(tq_\w+)\s*\(", src, flags=re.M)
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build the CUDA library first "
+                "(python -m bit_matvec_gb300.build, or __graft_entry__.build())")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        sig = {
+            "tq_quantize_q8K": ([P, P, I64, I64, P], I),
+            "tq_repacked_bytes": ([I64, I64], I64),
+            "tq_repack": ([P, P, I64, I64, P], I),
+            "tq_unrepack": ([P, P, I64, I64, P], I),
+            "tq_matmul": ([P, P, P, I64, I64, I64, P], I),
+            "tq_matmul_groupsums": ([P, P, P, I64, I64, I64, P], I),
+            "tq_strerror": ([I], ctypes.c_char_p),
+            "tq_last_cuda_error": ([], I),
+            "tq_device_status": ([], I),
+            "tq_version": ([], ctypes.c_char_p),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+    return _lib
+
+
+def library() -> ctypes.CDLL:
+    """The loaded libtq.so (raises if it has not been built)."""
+    return _load()
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _call(name, device, *args):
+    lib = _load()
+    if device.index is None or device.index == torch.cuda.current_device():
+        rc = getattr(lib, name)(*args)
+    else:
+        with torch.cuda.device(device):
+            rc = getattr(lib, name)(*args)
+    if rc != TQ_OK:
+        raise TQError(rc, name)
+
+
+# ---------------------------------------------------------------- allocation helpers
+
+def q8K_nbytes(ntok: int, cols: int) -> int:
+    return ntok * (cols // QK_K) * Q8K_BYTES
+
+
+def q8K_empty(ntok: int, cols: int, device="cuda") -> torch.Tensor:
+    """uint8 buffer for ntok x cols/256 q8_K blocks."""
+    return torch.empty(q8K_nbytes(ntok, cols), dtype=torch.uint8, device=device)
+
+
+def tq_repacked_bytes(rows: int, cols: int) -> int:
+    n = _load().tq_repacked_bytes(rows, cols)
+    if n < 0:
+        raise TQError(TQ_ERR_SHAPE, "tq_repacked_bytes")
+    return int(n)
+
+
+def repacked_empty(rows: int, cols: int, device="cuda") -> torch.Tensor:
+    return torch.empty(tq_repacked_bytes(rows, cols), dtype=torch.uint8, device=device)
+
+
+# ---------------------------------------------------------------- the C ABI
+
+def tq_quantize_q8K(X: torch.Tensor, Xq: torch.Tensor, ntok: int, cols: int, stream=None):
+    _call("tq_quantize_q8K", X.device, _ptr(X), _ptr(Xq), ntok, cols, _stream(stream, X.device))
+
+
+def tq_repack(Wpq2: torch.Tensor, Wtq: torch.Tensor, rows: int, cols: int, stream=None):
+    _call("tq_repack", Wpq2.device, _ptr(Wpq2), _ptr(Wtq), rows, cols,
+          _stream(stream, Wpq2.device))
+
+
+def tq_unrepack(Wtq: torch.Tensor, Wpq2: torch.Tensor, rows: int, cols: int, stream=None):
+    _call("tq_unrepack", Wtq.device, _ptr(Wtq), _ptr(Wpq2), rows, cols,
+          _stream(stream, Wtq.device))
+
+
+def tq_matmul(Wtq: torch.Tensor, Xq: torch.Tensor, Y: torch.Tensor, rows: int, cols: int,
+              ntok: int, stream=None):
+    _call("tq_matmul", Wtq.device, _ptr(Wtq), _ptr(Xq), _ptr(Y), rows, cols, ntok,
+          _stream(stream, Wtq.device))
+
+
+def tq_matmul_groupsums(Wtq: torch.Tensor, Xq: torch.Tensor, S: torch.Tensor, rows: int,
+                        cols: int, ntok: int, stream=None):
+    _call("tq_matmul_groupsums", Wtq.device, _ptr(Wtq), _ptr(Xq), _ptr(S), rows, cols, ntok,
+          _stream(stream, Wtq.device))
+
+
+def tq_strerror(code: int) -> str:
+    return _load().tq_strerror(code).decode()
+
+
+def tq_last_cuda_error() -> int:
+    return int(_load().tq_last_cuda_error())
+
+
+def tq_device_status(device=None) -> int:
+    """Read and clear the device status word (synchronizes the device)."""
+    lib = _load()
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        return int(lib.tq_device_status())
+
+
+def tq_version() -> str:
+    return _load().tq_version().decode()

@@ -1,0 +1,200 @@
+// tq_api.cu -- the C ABI declared in include/tq.h: argument checks, routing by
+// token count, error reporting. Kernels live in the other files of csrc/.
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "tq_internal.cuh"
+
+namespace tq {
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+// Device-side status word: kernels that bound a wait set it when they give up.
+__device__ int g_device_status = kDevOk;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_status_ptr[kMaxDevices] = {};
+std::map<std::pair<int, const void*>, int> g_smem_optin;
+
+int fail_cuda(cudaError_t e) {
+  g_last_cuda_error = (int)e;
+  return TQ_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+bool aligned4(const void* p) { return ((uintptr_t)p & 3u) == 0; }
+
+bool overlap(const void* a, int64_t na, const void* b, int64_t nb) {
+  const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return na > 0 && nb > 0 && x < y + (uintptr_t)nb && y < x + (uintptr_t)na;
+}
+
+cudaError_t device_status_ptr(int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_status);
+    if (e != cudaSuccess) return e;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return cudaSuccess;
+}
+
+int64_t q8K_bytes(int64_t ntok, int64_t cols) { return ntok * (cols / kQK) * kQ8KBytes; }
+
+int matmul_impl(const void* Wtq, const void* Xq, float* Y, int32_t* S, int64_t rows,
+                int64_t cols, int64_t ntok, void* stream) {
+  if (rows < 0 || cols < 0 || ntok < 0 || cols % kQK != 0) return TQ_ERR_SHAPE;
+  if (rows == 0 || ntok == 0) return TQ_OK;
+  void* out = Y ? (void*)Y : (void*)S;
+  if (!out) return TQ_ERR_NULL;
+  const int64_t out_bytes = Y ? ntok * rows * 4 : ntok * rows * (cols / kGroup) * 4;
+  if (!aligned4(out)) return TQ_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cols == 0) {
+    if (Y) {
+      cudaError_t e = cudaMemsetAsync(Y, 0, (size_t)out_bytes, s);
+      if (e != cudaSuccess) return fail_cuda(e);
+    }
+    return TQ_OK;
+  }
+  if (!Wtq || !Xq) return TQ_ERR_NULL;
+  if (!aligned16(Wtq) || !aligned16(Xq)) return TQ_ERR_ALIGN;
+  if (overlap(out, out_bytes, Wtq, tq_repacked_bytes(rows, cols)) ||
+      overlap(out, out_bytes, Xq, q8K_bytes(ntok, cols)))
+    return TQ_ERR_ALIAS;
+
+  const uint8_t* W = static_cast<const uint8_t*>(Wtq);
+  const uint8_t* X = static_cast<const uint8_t*>(Xq);
+  if (ntok <= gemv_max_tokens()) {
+    cudaError_t e = launch_gemv(W, X, Y, S, rows, cols, (int)ntok, s);
+    if (e == cudaSuccess) return TQ_OK;
+    if (e != cudaErrorNotSupported) return fail_cuda(e);
+    // activations too large for the GEMV's shared memory: tensor-core path
+  }
+  int* status = nullptr;
+  cudaError_t e = device_status_ptr(&status);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = launch_gemm_tc(W, X, Y, S, rows, cols, ntok, status, s);
+  return e == cudaSuccess ? TQ_OK : fail_cuda(e);
+}
+
+}  // namespace
+
+cudaError_t ensure_dynamic_smem(const void* kernel, int bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto key = std::make_pair(dev, kernel);
+  auto it = g_smem_optin.find(key);
+  if (it != g_smem_optin.end() && it->second >= bytes) return cudaSuccess;
+  int optin = 0;
+  e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  if (bytes > optin) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  if (e != cudaSuccess) return e;
+  g_smem_optin[key] = optin;
+  return cudaSuccess;
+}
+
+}  // namespace tq
+
+using namespace tq;
+
+extern "C" {
+
+int tq_quantize_q8K(const float* X, void* Xq, int64_t ntok, int64_t cols, void* stream) {
+  if (ntok < 0 || cols < 0 || cols % kQK != 0) return TQ_ERR_SHAPE;
+  if (ntok == 0 || cols == 0) return TQ_OK;
+  if (!X || !Xq) return TQ_ERR_NULL;
+  if (!aligned16(X) || !aligned16(Xq)) return TQ_ERR_ALIGN;
+  if (overlap(X, ntok * cols * 4, Xq, q8K_bytes(ntok, cols))) return TQ_ERR_ALIAS;
+  cudaError_t e = launch_quantize_q8K(X, static_cast<uint8_t*>(Xq), ntok * (cols / kQK),
+                                      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TQ_OK : fail_cuda(e);
+}
+
+int64_t tq_repacked_bytes(int64_t rows, int64_t cols) {
+  if (rows < 0 || cols < 0 || cols % kGroup != 0) return -1;
+  return (rows + kTileRows - 1) / kTileRows * (cols / kGroup) * kTileBytes;
+}
+
+int tq_repack(const void* Wpq2, void* Wtq, int64_t rows, int64_t cols, void* stream) {
+  if (rows < 0 || cols < 0 || cols % kGroup != 0) return TQ_ERR_SHAPE;
+  if (rows == 0 || cols == 0) return TQ_OK;
+  if (!Wpq2 || !Wtq) return TQ_ERR_NULL;
+  if (!aligned16(Wpq2) || !aligned16(Wtq)) return TQ_ERR_ALIGN;
+  if (overlap(Wpq2, rows * (cols / kGroup) * kPq2Bytes, Wtq, tq_repacked_bytes(rows, cols)))
+    return TQ_ERR_ALIAS;
+  cudaError_t e = launch_repack(static_cast<const uint8_t*>(Wpq2), static_cast<uint8_t*>(Wtq),
+                                rows, cols, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TQ_OK : fail_cuda(e);
+}
+
+int tq_unrepack(const void* Wtq, void* Wpq2, int64_t rows, int64_t cols, void* stream) {
+  if (rows < 0 || cols < 0 || cols % kGroup != 0) return TQ_ERR_SHAPE;
+  if (rows == 0 || cols == 0) return TQ_OK;
+  if (!Wpq2 || !Wtq) return TQ_ERR_NULL;
+  if (!aligned16(Wpq2) || !aligned16(Wtq)) return TQ_ERR_ALIGN;
+  if (overlap(Wpq2, rows * (cols / kGroup) * kPq2Bytes, Wtq, tq_repacked_bytes(rows, cols)))
+    return TQ_ERR_ALIAS;
+  cudaError_t e = launch_unrepack(static_cast<const uint8_t*>(Wtq), static_cast<uint8_t*>(Wpq2),
+                                  rows, cols, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TQ_OK : fail_cuda(e);
+}
+
+int tq_matmul(const void* Wtq, const void* Xq, float* Y, int64_t rows, int64_t cols,
+              int64_t ntok, void* stream) {
+  return matmul_impl(Wtq, Xq, Y, nullptr, rows, cols, ntok, stream);
+}
+
+int tq_matmul_groupsums(const void* Wtq, const void* Xq, int32_t* S, int64_t rows,
+                        int64_t cols, int64_t ntok, void* stream) {
+  return matmul_impl(Wtq, Xq, nullptr, S, rows, cols, ntok, stream);
+}
+
+const char* tq_strerror(int code) {
+  switch (code) {
+    case TQ_OK: return "ok";
+    case TQ_ERR_SHAPE: return "bad shape (cols must be a multiple of 256, sizes >= 0)";
+    case TQ_ERR_NULL: return "null pointer";
+    case TQ_ERR_ALIGN: return "misaligned buffer";
+    case TQ_ERR_CUDA: return "CUDA error (see tq_last_cuda_error)";
+    case TQ_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
+    case TQ_ERR_ALIAS: return "output buffer overlaps an input";
+    default: return "unknown error";
+  }
+}
+
+int tq_last_cuda_error(void) { return g_last_cuda_error; }
+
+int tq_device_status(void) {
+  int* p = nullptr;
+  cudaError_t e = device_status_ptr(&p);
+  if (e != cudaSuccess) return fail_cuda(e);
+  int v = 0;
+  e = cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (v != kDevOk) {
+    const int zero = kDevOk;
+    e = cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  return v == kDevTimeout ? TQ_ERR_TIMEOUT : TQ_OK;
+}
+
+const char* tq_version(void) { return "0.1.0"; }
+
+}  // extern "C"

@@ -1,0 +1,110 @@
+// tq_repack.cu -- load-time permutation of pq2_0 weights into the tq layout,
+// and its inverse.
+//
+// The ternary post ("the layout") repacks once at model load so that
+// unpacking costs one AND per vector; this is the GPU version of that step,
+// with a GPU-chosen order (layout defined in include/tq.h).
+//
+// One warp per tile (32 rows x 128 weights); lane l handles row l. A 32-bit
+// word of pq2_0 codes covers 16 consecutive weights: byte s holds weights
+// 4s..4s+3 at bits 0, 2, 4, 6. The tq word of the same 16 weights holds in
+// byte j the weights j, 4+j, 8+j, 12+j at bits 0, 2, 4, 6. Viewing the word as
+// a 4x4 matrix of 2-bit fields (row = byte), one layout is the transpose of
+// the other, done with two delta swaps (off-diagonal 2x2 blocks, then within
+// each block). A transpose is its own inverse, so unrepack uses the same swap.
+#include "tq_internal.cuh"
+
+namespace tq {
+namespace {
+
+constexpr int kWarpsPerCta = 8;
+
+__device__ __forceinline__ uint32_t transpose_2bit_4x4(uint32_t x) {
+  uint32_t t = (x ^ (x >> 12)) & 0x0000F0F0u;  // fields (s<2, j>=2) <-> (s+2, j-2)
+  x ^= t ^ (t << 12);
+  t = (x ^ (x >> 6)) & 0x00CC00CCu;            // fields (s even, j odd) <-> (s+1, j-1)
+  x ^= t ^ (t << 6);
+  return x;
+}
+
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+repack_kernel(const uint8_t* __restrict__ Wpq2, uint8_t* __restrict__ Wtq, int64_t rows,
+              int64_t ngroups, int64_t ntiles) {
+  const int lane = threadIdx.x & 31;
+  const int64_t tile = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  if (tile >= ntiles) return;
+  const int64_t rb = tile / ngroups, g = tile - rb * ngroups;
+  const int64_t r = rb * kTileRows + lane;
+  uint8_t* out = Wtq + tile * kTileBytes;
+
+  uint32_t w[8];
+  uint16_t scale = 0;
+  if (r < rows) {
+    // pq2_0 blocks are 34 bytes, so only 2-byte alignment is guaranteed.
+    const uint16_t* blk = reinterpret_cast<const uint16_t*>(Wpq2 + (r * ngroups + g) * kPq2Bytes);
+    scale = blk[0];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      w[i] = transpose_2bit_4x4((uint32_t)blk[1 + 2 * i] | ((uint32_t)blk[2 + 2 * i] << 16));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = 0x55555555u;  // padding rows: code 1, w = 0
+  }
+  // words 0..3 cover weights 0..63 (h = 0), words 4..7 weights 64..127 (h = 1)
+  *reinterpret_cast<uint4*>(out + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  *reinterpret_cast<uint4*>(out + 512 + lane * 16) = make_uint4(w[4], w[5], w[6], w[7]);
+  reinterpret_cast<uint16_t*>(out + kTileCodeBytes)[lane] = scale;
+}
+
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+unrepack_kernel(const uint8_t* __restrict__ Wtq, uint8_t* __restrict__ Wpq2, int64_t rows,
+                int64_t ngroups, int64_t ntiles) {
+  const int lane = threadIdx.x & 31;
+  const int64_t tile = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  if (tile >= ntiles) return;
+  const int64_t rb = tile / ngroups, g = tile - rb * ngroups;
+  const int64_t r = rb * kTileRows + lane;
+  if (r >= rows) return;
+  const uint8_t* in = Wtq + tile * kTileBytes;
+  const uint4 lo = *reinterpret_cast<const uint4*>(in + lane * 16);
+  const uint4 hi = *reinterpret_cast<const uint4*>(in + 512 + lane * 16);
+  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  uint16_t* blk = reinterpret_cast<uint16_t*>(Wpq2 + (r * ngroups + g) * kPq2Bytes);
+  blk[0] = reinterpret_cast<const uint16_t*>(in + kTileCodeBytes)[lane];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t p = transpose_2bit_4x4(w[i]);
+    blk[1 + 2 * i] = (uint16_t)(p & 0xFFFFu);
+    blk[2 + 2 * i] = (uint16_t)(p >> 16);
+  }
+}
+
+int64_t tile_count(int64_t rows, int64_t cols) {
+  return (rows + kTileRows - 1) / kTileRows * (cols / kGroup);
+}
+
+}  // namespace
+
+cudaError_t launch_repack(const uint8_t* Wpq2, uint8_t* Wtq, int64_t rows, int64_t cols,
+                          cudaStream_t s) {
+  const int64_t ntiles = tile_count(rows, cols);
+  if (ntiles <= 0) return cudaSuccess;
+  const int64_t grid = (ntiles + kWarpsPerCta - 1) / kWarpsPerCta;
+  if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  repack_kernel<<<(unsigned)grid, kWarpsPerCta * 32, 0, s>>>(Wpq2, Wtq, rows, cols / kGroup,
+                                                             ntiles);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unrepack(const uint8_t* Wtq, uint8_t* Wpq2, int64_t rows, int64_t cols,
+                            cudaStream_t s) {
+  const int64_t ntiles = tile_count(rows, cols);
+  if (ntiles <= 0) return cudaSuccess;
+  const int64_t grid = (ntiles + kWarpsPerCta - 1) / kWarpsPerCta;
+  if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  unrepack_kernel<<<(unsigned)grid, kWarpsPerCta * 32, 0, s>>>(Wtq, Wpq2, rows, cols / kGroup,
+                                                               ntiles);
+  return cudaGetLastError();
+}
+
+}  // namespace tq

@@ -1,0 +1,176 @@
+/*
+ * tq.h -- C ABI of the ternary-weight x int8-activation matrix product
+ * (pq2_0 weights, q8_K activations) on NVIDIA GB300 (sm_103a).
+ *
+ * The method (web pages "how i made a 27b ternary model 3.8x faster on a
+ * laptop cpu by reordering its bits" and the ciot README):
+ *   - weights are ternary, w in {-1, 0, +1}, stored as u = w + 1 in 2 bits
+ *     with one fp16 scale d_w per 128 weights of a row (format pq2_0,
+ *     2.125 bits per weight);
+ *   - activations are quantized on the fly to q8_K: blocks of 256 int8
+ *     values q with one f32 scale d_x and 16 partial sums (bsums);
+ *   - y[t][r] = sum over 128-weight groups g of
+ *       d_w[r][g] * d_x[t][g/2] * isum[t][r][g],
+ *     isum[t][r][g] = sum_{k in g} (u - 1) * q, an exact integer;
+ *   - the weights are repacked once at load time into an order that makes
+ *     unpacking cheap (post, section "the layout"; README "the repack runs
+ *     once at model load").
+ *
+ * Conventions shared by every call:
+ *   - all buffer pointers are DEVICE pointers (cudaMalloc, torch, or managed
+ *     memory) of the current CUDA device, owned by the caller; the library
+ *     allocates no memory and never synchronizes the device;
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream); work is enqueued on it and the call returns at once;
+ *   - sizes are int64_t; a call with any size equal to 0 (no rows, no tokens)
+ *     enqueues nothing and returns TQ_OK, except as stated below;
+ *   - every call returns TQ_OK (0) or a negative TQ_ERR_* code; an error is
+ *     returned before anything is enqueued, except TQ_ERR_CUDA, which reports
+ *     a failed launch (tq_last_cuda_error() gives the cudaError_t);
+ *   - buffers marked "16-byte aligned" must start on a 16-byte boundary
+ *     (TQ_ERR_ALIGN otherwise); input and output buffers must not overlap.
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TQ_OK            0
+#define TQ_ERR_SHAPE    -1  /* cols % 256 != 0, or a negative size */
+#define TQ_ERR_NULL     -2  /* a required pointer is NULL */
+#define TQ_ERR_ALIGN    -3  /* a buffer breaks its alignment rule */
+#define TQ_ERR_CUDA     -4  /* a CUDA launch or runtime call failed */
+#define TQ_ERR_TIMEOUT  -5  /* a kernel gave up a bounded wait (tq_device_status) */
+#define TQ_ERR_ALIAS    -6  /* an output buffer overlaps an input buffer */
+
+#define TQ_QK_K 256          /* activations per q8_K block */
+#define TQ_GROUP 128         /* weights per pq2_0 scale */
+#define TQ_PQ2_0_BYTES 34    /* bytes per pq2_0 block (fp16 scale + 32 code bytes) */
+#define TQ_Q8K_BYTES 292     /* bytes per q8_K block */
+#define TQ_TILE_ROWS 32      /* rows per tile of the repacked layout */
+#define TQ_TILE_BYTES 1088   /* bytes per tile: 32 rows x 128 weights */
+
+/*
+ * q8_K block (ciot README: "256 int8 values, a float scale and 16 partial
+ * sums per block"). Packed, 292 bytes, no padding; blocks of one token are
+ * contiguous and tokens follow each other: block b of token t is element
+ * t * (cols/256) + b of the array.
+ */
+typedef struct {
+    float d;             /* scale: x ~= d * q */
+    int8_t qs[256];      /* q in [-127, 127] */
+    int16_t bsums[16];   /* bsums[i] = qs[16i] + ... + qs[16i+15] */
+} tq_block_q8K;
+
+/*
+ * pq2_0 block (post, "what's running": 2 bits per weight as u = w + 1, one
+ * fp16 scale per 128 weights; README: 2.125 bits per weight). The byte order
+ * inside the block is this library's reading, the pages leave it open:
+ * bytes 0..1 hold the fp16 scale (little-endian), bytes 2..33 the codes, and
+ * weight k (0..127) of the block is in code byte k >> 2 at bits
+ * 2*(k & 3) .. 2*(k & 3)+1. A weight matrix [rows][cols] is rows * cols/128
+ * blocks, row-major: block (r, g) starts at byte (r * cols/128 + g) * 34.
+ *
+ * Repacked layout ("tq"), produced by tq_repack: the same bits in a GPU
+ * order. Rows are taken in tiles of 32 (the last tile padded with code 1,
+ * i.e. w = 0, and scale 0). Tile (row block rb, group g) is 1088 bytes at
+ * offset (rb * cols/128 + g) * 1088: 1024 code bytes, then the 32 fp16
+ * scales of its rows (row l at byte 1024 + 2l). The code of weight k of the
+ * group, row l of the tile, is in byte h*512 + l*16 + wd*4 + j at bits 2s,
+ * where h = k/64, wd = (k%64)/16, s = (k%16)/4, j = k%4. Hence:
+ *   - each 32-bit word holds 16 consecutive weights of one row, and
+ *     word & (0x03030303 << 2s) is 4 consecutive weights times 4^s, one per
+ *     byte, lined up with 4 consecutive int8 activations (one AND per
+ *     dp4a operand: the post's "trick with 4 and 16", on 32-bit lanes);
+ *   - a warp reading 16 bytes per lane reads 512 contiguous bytes: 64
+ *     weights of each of 32 rows.
+ */
+
+/*
+ * tq_quantize_q8K -- quantize activations to q8_K (ciot README: activations
+ * are quantized on the fly to q8_K). For each block of 256 values:
+ * amax = max |x|; if amax == 0 the block is all zero (d = 0); otherwise
+ * d = amax / 127 and q = round-to-nearest-even(x * (127 / amax)) clamped to
+ * [-127, 127] (one IEEE division for 127/amax, one for d); bsums[i] is the
+ * sum of qs[16i .. 16i+15]. Inputs must be finite, with every nonzero
+ * block's amax at least 2^-126 (smaller values are out of contract).
+ *   X   [ntok][cols] f32, row-major, 16-byte aligned.
+ *   Xq  [ntok][cols/256] tq_block_q8K, 16-byte aligned, written.
+ * Errors: TQ_ERR_SHAPE if cols % 256 != 0 or a size is negative.
+ */
+int tq_quantize_q8K(const float *X, void *Xq, int64_t ntok, int64_t cols, void *stream);
+
+/* Bytes of the repacked weights: ceil(rows/32) * (cols/128) * 1088, which is
+ * rows * cols/128 * 34 (the pq2_0 size) when rows % 32 == 0; -1 if
+ * cols % 128 != 0 or a size is negative. */
+int64_t tq_repacked_bytes(int64_t rows, int64_t cols);
+
+/*
+ * tq_repack -- load-time repack of pq2_0 weights into the tq layout (post,
+ * "the layout": "it runs once when the model loads"). A pure permutation of
+ * bits: every code, including the unused value 3, is moved as is.
+ * Out-of-place (the pages repack in place; on the GPU the copy avoids
+ * hazards between thread blocks).
+ *   Wpq2 [rows][cols/128] pq2_0 blocks, 16-byte aligned.
+ *   Wtq  tq_repacked_bytes(rows, cols) bytes, 16-byte aligned, written.
+ * Errors: TQ_ERR_SHAPE if cols % 128 != 0; TQ_ERR_ALIAS if the buffers overlap.
+ */
+int tq_repack(const void *Wpq2, void *Wtq, int64_t rows, int64_t cols, void *stream);
+
+/* tq_unrepack -- the exact inverse of tq_repack (padding rows are dropped). */
+int tq_unrepack(const void *Wtq, void *Wpq2, int64_t rows, int64_t cols, void *stream);
+
+/*
+ * tq_matmul -- Y = the ternary x q8_K product (definition at the top).
+ * Each group sum is exact in int32 (post, "the trick with 4 and 16": the
+ * largest scaled intermediate is 520,192); the scale products and the sum
+ * over groups are f32, accumulated in an order the library chooses, within
+ * 1e-5 of sum_g |d_w d_x isum| of the exact value.
+ * Routing by ntok (post, "the leftovers": never one weight pass per leftover
+ * token): ntok <= 8 runs a bandwidth-bound GEMV that reads the weights once
+ * for all tokens; larger ntok runs a tcgen05 tensor-core kernel with the
+ * token dimension zero-padded to its tile, storing only the real outputs.
+ *   Wtq [tq layout] repacked weights, 16-byte aligned.
+ *   Xq  [ntok][cols/256] q8_K blocks, 16-byte aligned.
+ *   Y   [ntok][rows] f32, 4-byte aligned, overwritten (not accumulated).
+ * With cols == 0 and rows, ntok > 0, Y is set to zero.
+ * Errors: TQ_ERR_SHAPE if cols % 256 != 0; TQ_ERR_ALIAS if Y overlaps an input.
+ */
+int tq_matmul(const void *Wtq, const void *Xq, float *Y, int64_t rows, int64_t cols,
+              int64_t ntok, void *stream);
+
+/*
+ * tq_matmul_groupsums -- parity/debug form of tq_matmul: runs the same
+ * kernels (chosen by ntok the same way) but stores the exact integer group
+ * sums instead of Y.
+ *   S [ntok][rows][cols/128] int32, 4-byte aligned: S[t][r][g] = isum[t][r][g].
+ */
+int tq_matmul_groupsums(const void *Wtq, const void *Xq, int32_t *S, int64_t rows,
+                        int64_t cols, int64_t ntok, void *stream);
+
+/* Human-readable name of a TQ_* code. */
+const char *tq_strerror(int code);
+
+/* cudaError_t of the last TQ_ERR_CUDA returned on this host thread (0 if none). */
+int tq_last_cuda_error(void);
+
+/*
+ * tq_device_status -- read and clear the device-side status word of the
+ * current device. Kernels that wait on a barrier bound the wait; one that
+ * gives up sets this word and returns early (its outputs are then
+ * undefined). Returns TQ_OK, TQ_ERR_TIMEOUT, or TQ_ERR_CUDA. This call
+ * synchronizes the device (it copies the word to the host).
+ */
+int tq_device_status(void);
+
+/* Library version as "major.minor.patch". */
+const char *tq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TQ_H */

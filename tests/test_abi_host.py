@@ -1,0 +1,133 @@
+"""Host-side checks of the C ABI: the library loads, exports every function the
+header declares, and rejects bad arguments before touching a GPU.
+
+Fake device addresses are safe here: every rejected call returns before any
+CUDA runtime call, and the accepted no-op calls (a zero size) enqueue nothing.
+"""
+import ctypes
+
+import pytest
+
+import oracle
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_matvec_gb300 import build
+    build.build()
+    import bit_matvec_gb300 as tq
+    return tq.library()
+
+
+def test_exports_every_header_function(lib):
+    import bit_matvec_gb300 as tq
+    names = tq.header_functions()
+    for required in ("tq_quantize_q8K", "tq_repacked_bytes", "tq_repack", "tq_unrepack",
+                     "tq_matmul", "tq_matmul_groupsums", "tq_strerror"):
+        assert required in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_strerror(lib):
+    import bit_matvec_gb300 as tq
+    assert tq.tq_version().count(".") == 2
+    seen = set()
+    for code in (tq.TQ_OK, tq.TQ_ERR_SHAPE, tq.TQ_ERR_NULL, tq.TQ_ERR_ALIGN, tq.TQ_ERR_CUDA,
+                 tq.TQ_ERR_TIMEOUT, tq.TQ_ERR_ALIAS):
+        s = tq.tq_strerror(code)
+        assert s and s != "unknown error"
+        seen.add(s)
+    assert len(seen) == 7
+    assert tq.tq_strerror(12345) == "unknown error"
+
+
+@pytest.mark.parametrize("rows,cols", [(32, 256), (100, 512), (1, 128), (32768, 8192),
+                                       (17408, 5120), (5120, 17408), (0, 256), (33, 0)])
+def test_repacked_bytes_matches_oracle(lib, rows, cols):
+    assert lib.tq_repacked_bytes(rows, cols) == oracle.repacked_bytes(rows, cols)
+    if rows % 32 == 0:
+        assert lib.tq_repacked_bytes(rows, cols) == rows * cols // 128 * 34
+
+
+def test_repacked_bytes_rejects(lib):
+    assert lib.tq_repacked_bytes(32, 100) == -1
+    assert lib.tq_repacked_bytes(-1, 256) == -1
+
+
+A = 0x7F0000000000     # fake, 16-byte aligned device addresses
+B = 0x7F1000000000
+C = 0x7F2000000000
+P = ctypes.c_void_p
+
+
+def test_shape_errors(lib):
+    import bit_matvec_gb300 as tq
+    S = tq.TQ_ERR_SHAPE
+    assert lib.tq_matmul(P(A), P(B), P(C), 32, 300, 1, None) == S       # cols % 256
+    assert lib.tq_matmul(P(A), P(B), P(C), 32, 128, 1, None) == S
+    assert lib.tq_matmul(P(A), P(B), P(C), -1, 256, 1, None) == S
+    assert lib.tq_matmul(P(A), P(B), P(C), 32, 256, -2, None) == S
+    assert lib.tq_matmul_groupsums(P(A), P(B), P(C), 32, 384, 1, None) == S
+    assert lib.tq_quantize_q8K(P(A), P(B), 1, 100, None) == S
+    assert lib.tq_quantize_q8K(P(A), P(B), -1, 256, None) == S
+    assert lib.tq_repack(P(A), P(B), 32, 100, None) == S
+    assert lib.tq_unrepack(P(A), P(B), -3, 256, None) == S
+
+
+def test_empty_calls_are_noops(lib):
+    import bit_matvec_gb300 as tq
+    # no tokens or no rows: nothing to do, even with NULL buffers
+    assert lib.tq_matmul(None, None, None, 32, 256, 0, None) == tq.TQ_OK
+    assert lib.tq_matmul(None, None, None, 0, 256, 4, None) == tq.TQ_OK
+    assert lib.tq_matmul_groupsums(None, None, None, 0, 512, 9, None) == tq.TQ_OK
+    assert lib.tq_quantize_q8K(None, None, 0, 256, None) == tq.TQ_OK
+    assert lib.tq_quantize_q8K(None, None, 3, 0, None) == tq.TQ_OK
+    assert lib.tq_repack(None, None, 0, 256, None) == tq.TQ_OK
+    assert lib.tq_unrepack(None, None, 32, 0, None) == tq.TQ_OK
+
+
+def test_null_errors(lib):
+    import bit_matvec_gb300 as tq
+    N = tq.TQ_ERR_NULL
+    assert lib.tq_matmul(None, P(B), P(C), 32, 256, 1, None) == N
+    assert lib.tq_matmul(P(A), None, P(C), 32, 256, 1, None) == N
+    assert lib.tq_matmul(P(A), P(B), None, 32, 256, 1, None) == N
+    assert lib.tq_matmul(P(A), P(B), None, 32, 0, 1, None) == N          # Y needed to zero it
+    assert lib.tq_matmul_groupsums(P(A), P(B), None, 32, 256, 1, None) == N
+    assert lib.tq_quantize_q8K(None, P(B), 1, 256, None) == N
+    assert lib.tq_quantize_q8K(P(A), None, 1, 256, None) == N
+    assert lib.tq_repack(None, P(B), 32, 256, None) == N
+    assert lib.tq_unrepack(P(A), None, 32, 256, None) == N
+
+
+def test_alignment_errors(lib):
+    import bit_matvec_gb300 as tq
+    E = tq.TQ_ERR_ALIGN
+    assert lib.tq_matmul(P(A + 8), P(B), P(C), 32, 256, 1, None) == E     # W needs 16
+    assert lib.tq_matmul(P(A), P(B + 4), P(C), 32, 256, 1, None) == E     # Xq needs 16
+    assert lib.tq_matmul(P(A), P(B), P(C + 2), 32, 256, 1, None) == E     # Y needs 4
+    assert lib.tq_matmul_groupsums(P(A), P(B), P(C + 1), 32, 256, 1, None) == E
+    assert lib.tq_quantize_q8K(P(A + 4), P(B), 1, 256, None) == E
+    assert lib.tq_quantize_q8K(P(A), P(B + 12), 1, 256, None) == E
+    assert lib.tq_repack(P(A + 2), P(B), 32, 256, None) == E
+    assert lib.tq_unrepack(P(A), P(B + 8), 32, 256, None) == E
+
+
+def test_alias_errors(lib):
+    import bit_matvec_gb300 as tq
+    E = tq.TQ_ERR_ALIAS
+    wbytes = lib.tq_repacked_bytes(64, 512)
+    assert lib.tq_matmul(P(A), P(B), P(A + wbytes - 16), 64, 512, 1, None) == E
+    assert lib.tq_matmul(P(A), P(B), P(B + 16), 64, 512, 1, None) == E
+    assert lib.tq_quantize_q8K(P(A), P(A + 16), 1, 256, None) == E
+    assert lib.tq_repack(P(A), P(A), 32, 256, None) == E                      # in place
+    assert lib.tq_unrepack(P(A), P(A + 1088 - 16), 32, 256, None) == E
+
+
+def test_binding_rejects_cpu_tensors(lib):
+    import torch
+    import bit_matvec_gb300 as tq
+    x = torch.zeros(256)
+    with pytest.raises(ValueError):
+        tq.tq_quantize_q8K(x, torch.zeros(292, dtype=torch.uint8), 1, 256)

@@ -1,0 +1,209 @@
+"""GPU parity against the CPU oracle, through the C ABI.
+
+Bit-exact: q8_K bytes (scales, int8 values, partial sums), repacked bytes,
+and every int32 group sum. Within 1e-5 of sum_g |d_w d_x isum| per output:
+the f32 results. Sizes span several tiles with ragged tails; the GEMV path
+is ntok <= 8, the tensor-core path ntok >= 9.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from conftest import read_golden
+from gpu_util import (DEV, assert_close, ensure_built, gpu_groupsums, gpu_matmul, gpu_quantize,
+                      gpu_repack, q8K_from_dev, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ensure_built()
+
+
+def _weights(rows, cols, seed_index):
+    return synth.pq2_0_weights(rows, cols, seed_index)
+
+
+def _acts(ntok, cols, seed_index, outliers=True):
+    s = synth.seeds(seed_index)
+    return synth.activations(ntok, cols, s["acts"], s["outliers"] if outliers else None)
+
+
+def _q8K_equal(a, b):
+    assert np.array_equal(a["d"].view(np.uint32), b["d"].view(np.uint32))
+    assert np.array_equal(a["qs"], b["qs"])
+    assert np.array_equal(a["bsums"], b["bsums"])
+
+
+# ---------------------------------------------------------------- quantize
+
+@pytest.mark.parametrize("ntok,cols", [(1, 256), (3, 1024), (7, 2304), (64, 5120), (5, 17408)])
+def test_quantize_bit_exact(ntok, cols):
+    x = _acts(ntok, cols, 10 + ntok)
+    got = q8K_from_dev(gpu_quantize(x), ntok, cols)
+    _q8K_equal(got, oracle.quantize_q8K(x))
+
+
+def test_quantize_special_blocks():
+    rows = []
+    for name in ("q8K_scale_one.txt", "q8K_scale_two.txt"):
+        x = np.zeros(256, dtype=np.float32)
+        for tok in read_golden(name):
+            if tok[0] not in ("d", "bsums"):
+                x[int(tok[0])] = np.float32(tok[1])
+        rows.append(x)
+    rows.append(np.zeros(256, dtype=np.float32))                       # all zero
+    one = np.zeros(256, dtype=np.float32); one[77] = -3.25; rows.append(one)
+    rows.append(np.full(256, 1e30, dtype=np.float32))                  # extreme magnitude
+    rows.append(np.full(256, -7.0, dtype=np.float32))                  # constant
+    ints = np.random.default_rng(3).integers(-127, 128, 256).astype(np.float32)
+    ints[5] = 127; rows.append(ints)                                   # exact integers
+    tiny = np.linspace(-1, 1, 256, dtype=np.float32) * np.float32(1e-30); rows.append(tiny)
+    x = np.stack(rows).reshape(1, -1)
+    got = q8K_from_dev(gpu_quantize(x), 1, x.shape[1])
+    want = oracle.quantize_q8K(x)
+    _q8K_equal(got, want)
+    assert got["d"][0, 0] == 1.0 and got["d"][0, 1] == 2.0
+
+
+# ---------------------------------------------------------------- repack
+
+@pytest.mark.parametrize("rows,cols", [(32, 128), (100, 256), (1, 384), (300, 1024), (64, 5120)])
+def test_repack_bit_exact_and_roundtrip(rows, cols):
+    import bit_matvec_gb300 as tq
+    rng = np.random.default_rng(rows + cols)
+    b = rng.integers(0, 256, size=rows * cols // 128 * 34, dtype=np.uint8)   # code 3 included
+    Wtq = gpu_repack(b, rows, cols)
+    assert np.array_equal(Wtq.cpu().numpy(), oracle.repack(b, rows, cols))
+    back = torch.empty(b.size, dtype=torch.uint8, device=DEV)
+    tq.tq_unrepack(Wtq, back, rows, cols)
+    assert np.array_equal(back.cpu().numpy(), b)
+
+
+# ---------------------------------------------------------------- group sums and matmul
+
+SHAPES = [(32, 256), (100, 512), (300, 768), (128, 1024)]
+GEMV_TOKENS = [1, 2, 3, 4, 5, 7, 8]          # one weight pass for all tokens
+TC_TOKENS = [9, 15, 16, 17, 63, 64, 65, 130]  # tensor cores, token tile zero-padded
+
+
+def _check_product(rows, cols, ntok):
+    wpq = _weights(rows, cols, 20 + rows % 7)
+    x = _acts(ntok, cols, 30 + ntok)
+    Wtq = gpu_repack(wpq, rows, cols)
+    Xq = gpu_quantize(x)
+    xq = oracle.quantize_q8K(x)
+    S = gpu_groupsums(Wtq, Xq, rows, cols, ntok)
+    assert np.array_equal(S, oracle.groupsums(wpq, xq, rows, cols))
+    y_ref, abs_sum = oracle.matmul(wpq, xq, rows, cols)
+    assert_close(gpu_matmul(Wtq, Xq, rows, cols, ntok), y_ref, abs_sum)
+
+
+@pytest.mark.parametrize("rows,cols", SHAPES)
+@pytest.mark.parametrize("ntok", GEMV_TOKENS)
+def test_gemv_groupsums_exact_matmul_close(rows, cols, ntok):
+    _check_product(rows, cols, ntok)
+
+
+@pytest.mark.parametrize("rows,cols", SHAPES)
+@pytest.mark.parametrize("ntok", TC_TOKENS)
+def test_tc_groupsums_exact_matmul_close(rows, cols, ntok):
+    _check_product(rows, cols, ntok)
+
+
+@pytest.mark.parametrize("ntok", [1, 4, 8, 9, 16, 64, 65], ids=lambda t: f"{'tc' if t > 8 else 'gemv'}{t}")
+def test_exact_integer_mode(ntok):
+    """d_w = 1 and d_x = 1 (integer activations with absmax 127 in every block):
+    the output is the exact integer product, on both paths."""
+    rows, cols = 96, 1024
+    rng = np.random.default_rng(ntok)
+    w = rng.integers(-1, 2, size=(rows, cols))
+    wpq = synth.pack_pq2_0((w + 1).astype(np.uint8), np.ones((rows, cols // 128), np.float16))
+    x = rng.integers(-127, 128, size=(ntok, cols)).astype(np.float32)
+    x[:, ::256] = 127.0
+    Wtq = gpu_repack(wpq, rows, cols)
+    Xq = gpu_quantize(x)
+    y = gpu_matmul(Wtq, Xq, rows, cols, ntok)
+    assert np.array_equal(y.astype(np.int64), x.astype(np.int64) @ w.T)
+    assert np.array_equal(y, (x.astype(np.int64) @ w.T).astype(np.float32))
+
+
+@pytest.mark.parametrize("ntok", [1, 8, 64], ids=lambda t: f"{'tc' if t > 8 else 'gemv'}{t}")
+def test_extremes(ntok):
+    """All u = 2 (w = +1) or all u = 0 against q = +-127: the largest group sums."""
+    rows, cols = 64, 512
+    for code in (0, 2):
+        wpq = synth.pack_pq2_0(np.full((rows, cols), code, np.uint8),
+                               np.ones((rows, cols // 128), np.float16))
+        x = np.where(np.arange(cols) % 2 == 0, 127.0, -127.0).astype(np.float32)
+        x = np.tile(x, (ntok, 1))
+        x[ntok // 2:] = 127.0
+        Wtq, Xq = gpu_repack(wpq, rows, cols), gpu_quantize(x)
+        S = gpu_groupsums(Wtq, Xq, rows, cols, ntok)
+        assert np.array_equal(S, oracle.groupsums(wpq, oracle.quantize_q8K(x), rows, cols))
+        assert np.abs(S).max() == 16256
+
+
+def test_empty_and_degenerate():
+    import bit_matvec_gb300 as tq
+    rows, cols = 64, 512
+    Wtq = gpu_repack(_weights(rows, cols, 1), rows, cols)
+    Xq = gpu_quantize(_acts(2, cols, 1))
+    Y = torch.full((2, rows), 5.0, device=DEV)
+    tq.tq_matmul(Wtq, Xq, Y, rows, cols, 0)          # no tokens: Y untouched
+    tq.tq_matmul(Wtq, Xq, Y, 0, cols, 2)             # no rows
+    assert torch.all(Y == 5.0)
+    tq.tq_matmul(Wtq, Xq, Y, rows, 0, 2)             # empty inner dimension: zeros
+    assert torch.all(Y == 0.0)
+    with pytest.raises(tq.TQError):
+        tq.tq_matmul(Wtq, Xq, Y, rows, 300, 2)
+
+
+def test_deterministic_and_stream():
+    rows, cols, ntok = 200, 2048, 5
+    wpq, x = _weights(rows, cols, 2), _acts(ntok, cols, 2)
+    Wtq, Xq = gpu_repack(wpq, rows, cols), gpu_quantize(x)
+    s = torch.cuda.Stream()
+    import bit_matvec_gb300 as tq
+    ys = []
+    for _ in range(2):
+        Y = torch.empty((ntok, rows), device=DEV)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            tq.tq_matmul(Wtq, Xq, Y, rows, cols, ntok, stream=s)
+        s.synchronize()
+        ys.append(Y.cpu().numpy())
+    assert np.array_equal(ys[0].view(np.uint32), ys[1].view(np.uint32))
+    assert tq.tq_device_status() == tq.TQ_OK
+
+
+# ---------------------------------------------------------------- full-size workloads
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "small_batch", "prefill"])
+def test_workload_sampled_rows(name):
+    """Full-size workloads in the same launch configuration the benchmark times;
+    the oracle recomputes a sample of rows (first, last, and spread)."""
+    wpq, x, cfg = synth.workload(name)
+    rows, cols, ntok = cfg["rows"], cfg["cols"], cfg["ntok"]
+    Wtq, Xq = gpu_repack(wpq, rows, cols), gpu_quantize(x)
+    xq = oracle.quantize_q8K(x)
+    _q8K_equal(q8K_from_dev(Xq, ntok, cols), xq)
+    y = gpu_matmul(Wtq, Xq, rows, cols, ntok)
+    S = gpu_groupsums(Wtq, Xq, rows, cols, ntok)
+    rng = np.random.default_rng(rows)
+    sample = np.unique(np.concatenate([[0, 1, 31, 32, rows - 1],
+                                       rng.integers(0, rows, 60)]))
+    wsub = oracle.pq2_0_rows(wpq, cols, sample)
+    y_ref, abs_sum = oracle.matmul(wsub, xq, len(sample), cols)
+    assert_close(y[:, sample], y_ref, abs_sum)
+    assert np.array_equal(S[:, sample, :], oracle.groupsums(wsub, xq, len(sample), cols))
+    # the repacked tiles of the sampled rows hold the same bits as pq2_0
+    if rows * cols <= 32768 * 8192:
+        wtq = Wtq.cpu().numpy()
+        assert np.array_equal(wtq[:oracle.repacked_bytes(64, cols)],
+                              oracle.repack(wpq[:64 * cols // 128 * 34], 64, cols))
