@@ -211,49 +211,78 @@ class Workload:
 
 
 def time_graph(wl: Workload, steps: int, warmup: int, world: int):
-    """Device time of `steps` steps, and the matmul kernel's mean duration.
+    """Device time per step, and the matmul kernel's average launch duration.
 
-    One CUDA graph holds `copies` steps (one per weight copy) with events around
-    each matmul; it is replayed ceil(steps / copies) times, and the first
-    `steps` steps are the ones counted (the graph unit is small next to K).
+    Graph A holds `copies` steps (quantize + matmul, one per weight copy) and is
+    replayed ceil(steps / copies) times between two events: the step time, with
+    consecutive kernels overlapping as they do in a real decode (programmatic
+    dependent launch). Graph M holds `copies` matmul launches only and is
+    replayed as often: the timed region's length over its launches is the
+    kernel's average launch duration. Graph B (steps with events around each
+    matmul, which serialise the kernels) gives the isolated per-launch time too.
     """
     import torch
+    import bit_matvec_gb300 as tq
     stream = torch.cuda.Stream(device=wl.device)
     stream.wait_stream(torch.cuda.current_stream(wl.device))
     n = wl.copies
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(n)]
-    import bit_matvec_gb300 as tq
+
+    def timing_event():
+        try:   # recorded inside a graph as an external event node, readable after replay
+            return torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            return torch.cuda.Event(enable_timing=True)
+
+    ev = [(timing_event(), timing_event()) for _ in range(n)]
+
+    def timed(graph, reps):
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        end.record(stream)
+        stream.synchronize()
+        return start.elapsed_time(end)
+
     with torch.cuda.stream(stream):
         for i in range(max(warmup, 3)):                 # un-captured warm-up (kernel attributes)
             wl.step(i, stream)
         stream.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
+        ga = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ga, stream=stream):
+            for i in range(n):
+                wl.step(i, stream)
+        gm = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gm, stream=stream):
+            for i in range(n):
+                tq.tq_matmul(wl.W[i], wl.Xq, wl.Y, wl.rows, wl.cols, wl.ntok, stream)
+        gb = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gb, stream=stream):
             for i in range(n):
                 tq.tq_quantize_q8K(wl.X, wl.Xq, wl.ntok, wl.cols, stream)
                 ev[i][0].record(stream)
                 tq.tq_matmul(wl.W[i], wl.Xq, wl.Y, wl.rows, wl.cols, wl.ntok, stream)
                 ev[i][1].record(stream)
         reps = -(-steps // n)
-        for _ in range(max(1, warmup // n)):            # graph warm-up replays
-            g.replay()
+        for g in (ga, gm, gb):                          # graph warm-up replays
+            for _ in range(max(1, warmup // n)):
+                g.replay()
         stream.synchronize()
         barrier(world)
         torch.cuda.synchronize(wl.device)
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
-        start.record(stream)
-        for _ in range(reps):
-            g.replay()
-        end.record(stream)
+        total_ms = timed(ga, reps)
+        kern_ms = timed(gm, reps) / (reps * n)
+        gb.replay()
         stream.synchronize()
-        # matmul durations: the events inside the graph hold the last replay's times
-        kern_ms = [a.elapsed_time(b) for a, b in ev]
+        try:
+            serial_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        except RuntimeError:
+            serial_ms = None
         barrier(world)
-    total_ms = start.elapsed_time(end)
     done_steps = reps * n
-    return total_ms / done_steps, statistics.mean(kern_ms), done_steps
+    how = "timed graph of back-to-back matmul launches (events around the region)"
+    return total_ms / done_steps, kern_ms, done_steps, how, serial_ms
 
 
 def time_e2e(wl: Workload, steps: int, warmup: int):
@@ -392,7 +421,7 @@ TC_FILES = ("tq_gemm_tc.cu", "tq_internal.cuh")
 
 def measure(name, args, rank, world, device, peaks, peak_kind, steps):
     wl = Workload(name, device)
-    step_ms, kern_ms, done = time_graph(wl, steps, args.warmup, world)
+    step_ms, kern_ms, done, kern_how, serial_ms = time_graph(wl, steps, args.warmup, world)
     step_ms = max_over_ranks(step_ms, world, device)
     abytes = algorithmic_bytes(wl.rows, wl.cols, wl.ntok)
     res = {"workload": WORKLOADS[name], "rows": wl.rows, "cols": wl.cols, "ntok": wl.ntok,
@@ -408,7 +437,8 @@ def measure(name, args, rank, world, device, peaks, peak_kind, steps):
         traffic = profile_traffic(f"gemv_{name}_ncu.txt", GEMV_FILES)
         res["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                            "frac": achieved / peak, "traffic": traffic,
-                           "kernel": "gemv_kernel", "kernel_ms": kern_ms,
+                           "kernel": "gemv_kernel", "kernel_ms": kern_ms, "kernel_timing": kern_how,
+                           "kernel_ms_serialised": serial_ms,
                            "algorithmic_bytes": abytes, "peak_source": peak_kind}
     else:
         flops = 2.0 * wl.macs()
@@ -418,7 +448,8 @@ def measure(name, args, rank, world, device, peaks, peak_kind, steps):
         res["roofline"] = {"bound": "tensor", "achieved": achieved, "peak": peak,
                            "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                            "kernel": "gemm_tc_kernel (tcgen05 kind::f16, exact)",
-                           "kernel_ms": kern_ms, "algorithmic_flops": flops,
+                           "kernel_ms": kern_ms, "kernel_timing": kern_how,
+                           "kernel_ms_serialised": serial_ms, "algorithmic_flops": flops,
                            "peak_source": f"{peak_kind} bf16 dense (f16 runs at the bf16 rate)"}
     return wl, res
 

@@ -3,6 +3,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <unordered_map>
 #include <utility>
 
 #include "tq_internal.cuh"
@@ -19,6 +20,24 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int* g_status_ptr[kMaxDevices] = {};
 std::map<std::pair<int, const void*>, int> g_smem_optin;
+
+// Last kernel this library enqueued on each stream. The GEMV may read weights
+// before the preceding kernel finishes only when that kernel is the quantizer,
+// which never writes weights.
+enum LastOp { kOpOther = 0, kOpQuantize = 1 };
+std::mutex g_stream_mu;
+std::unordered_map<cudaStream_t, int> g_last_op;
+
+void note_op(cudaStream_t s, int op) {
+  std::lock_guard<std::mutex> lk(g_stream_mu);
+  g_last_op[s] = op;
+}
+
+bool last_op_is_quantize(cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_stream_mu);
+  auto it = g_last_op.find(s);
+  return it != g_last_op.end() && it->second == kOpQuantize;
+}
 
 int fail_cuda(cudaError_t e) {
   g_last_cuda_error = (int)e;
@@ -62,6 +81,7 @@ int matmul_impl(const void* Wtq, const void* Xq, float* Y, int32_t* S, int64_t r
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cols == 0) {
     if (Y) {
+      note_op(s, kOpOther);
       cudaError_t e = cudaMemsetAsync(Y, 0, (size_t)out_bytes, s);
       if (e != cudaSuccess) return fail_cuda(e);
     }
@@ -75,15 +95,17 @@ int matmul_impl(const void* Wtq, const void* Xq, float* Y, int32_t* S, int64_t r
 
   const uint8_t* W = static_cast<const uint8_t*>(Wtq);
   const uint8_t* X = static_cast<const uint8_t*>(Xq);
+  int* status = nullptr;
+  cudaError_t e = device_status_ptr(&status);
+  if (e != cudaSuccess) return fail_cuda(e);
+  const bool after_quantize = last_op_is_quantize(s);
+  note_op(s, kOpOther);
   if (ntok <= gemv_max_tokens()) {
-    cudaError_t e = launch_gemv(W, X, Y, S, rows, cols, (int)ntok, s);
+    e = launch_gemv(W, X, Y, S, rows, cols, (int)ntok, status, after_quantize, s);
     if (e == cudaSuccess) return TQ_OK;
     if (e != cudaErrorNotSupported) return fail_cuda(e);
     // activations too large for the GEMV's shared memory: tensor-core path
   }
-  int* status = nullptr;
-  cudaError_t e = device_status_ptr(&status);
-  if (e != cudaSuccess) return fail_cuda(e);
   e = launch_gemm_tc(W, X, Y, S, rows, cols, ntok, status, s);
   return e == cudaSuccess ? TQ_OK : fail_cuda(e);
 }
@@ -121,8 +143,9 @@ int tq_quantize_q8K(const float* X, void* Xq, int64_t ntok, int64_t cols, void* 
   if (!X || !Xq) return TQ_ERR_NULL;
   if (!aligned16(X) || !aligned16(Xq)) return TQ_ERR_ALIGN;
   if (overlap(X, ntok * cols * 4, Xq, q8K_bytes(ntok, cols))) return TQ_ERR_ALIAS;
-  cudaError_t e = launch_quantize_q8K(X, static_cast<uint8_t*>(Xq), ntok * (cols / kQK),
-                                      static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_quantize_q8K(X, static_cast<uint8_t*>(Xq), ntok * (cols / kQK), s);
+  note_op(s, e == cudaSuccess ? kOpQuantize : kOpOther);
   return e == cudaSuccess ? TQ_OK : fail_cuda(e);
 }
 
@@ -138,6 +161,7 @@ int tq_repack(const void* Wpq2, void* Wtq, int64_t rows, int64_t cols, void* str
   if (!aligned16(Wpq2) || !aligned16(Wtq)) return TQ_ERR_ALIGN;
   if (overlap(Wpq2, rows * (cols / kGroup) * kPq2Bytes, Wtq, tq_repacked_bytes(rows, cols)))
     return TQ_ERR_ALIAS;
+  note_op(static_cast<cudaStream_t>(stream), kOpOther);
   cudaError_t e = launch_repack(static_cast<const uint8_t*>(Wpq2), static_cast<uint8_t*>(Wtq),
                                 rows, cols, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? TQ_OK : fail_cuda(e);
@@ -150,6 +174,7 @@ int tq_unrepack(const void* Wtq, void* Wpq2, int64_t rows, int64_t cols, void* s
   if (!aligned16(Wpq2) || !aligned16(Wtq)) return TQ_ERR_ALIGN;
   if (overlap(Wpq2, rows * (cols / kGroup) * kPq2Bytes, Wtq, tq_repacked_bytes(rows, cols)))
     return TQ_ERR_ALIAS;
+  note_op(static_cast<cudaStream_t>(stream), kOpOther);
   cudaError_t e = launch_unrepack(static_cast<const uint8_t*>(Wtq), static_cast<uint8_t*>(Wpq2),
                                   rows, cols, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? TQ_OK : fail_cuda(e);

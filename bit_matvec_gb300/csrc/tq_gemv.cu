@@ -4,12 +4,18 @@
 // Decode reads every weight once per token batch, so the bus is the limit
 // (ternary post, "did it reach the wall?" and "prefill wants a different
 // shape"). The kernel streams the repacked weights once for all tokens:
-//   - a warp owns a 32-row tile column; lane l is row l of the tile, so one
-//     16-byte load per lane reads 512 contiguous bytes (64 weights of each of
-//     32 rows) and no lane ever needs a cross-lane reduction of dot products;
+//   - each CTA owns a contiguous range of 32-row tile columns; its weights are
+//     one contiguous byte range, streamed through a ring of shared-memory
+//     stages with 1-D TMA bulk copies (cp.async.bulk, 16 or more tiles of
+//     1088 bytes per copy), each completed on a "full" mbarrier; the last of
+//     the 16 warps to release a slot refills it, so no warp waits for another;
+//   - the 16 warps each take tiles of a stage: the same 32 rows, different
+//     128-weight groups. Lane l is row l, so no lane ever needs a
+//     cross-lane reduction of dot products; the 16 partial sums of a row are
+//     added in shared memory once per tile column, in a fixed order
+//     (deterministic output);
 //   - the activations of all tokens sit in shared memory; every lane of a warp
-//     reads the same 16 bytes at once (a broadcast), so activation traffic is
-//     1/32 of a per-lane scheme;
+//     reads the same 16 bytes at once (a broadcast);
 //   - unpacking a 32-bit weight word (16 weights) is one AND per dp4a operand:
 //     word & (0x03030303 << 2s) is 4 consecutive weights times 4^s, and slot s
 //     accumulates in its own register (post, "the trick with 4 and 16"); the
@@ -18,50 +24,78 @@
 //     minus the sum of the group's activations from the q8_K partial sums turns
 //     u back into w (dot(w,y) = dot(u,y) - sum(y)), and one f32 FMA applies
 //     d_w * d_x;
-//   - warps of a CTA split the groups of a tile column; partial results are
-//     summed in shared memory in a fixed order (deterministic output).
+//   - launched as a programmatic dependent: when the previous kernel is the
+//     quantizer, the first weight stages are requested before waiting for it.
+#include <algorithm>
+
 #include "tq_internal.cuh"
 
 namespace tq {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
+// Compile-time tuning: warps per CTA (one token / more tokens), tiles each
+// warp takes from a stage, the deepest ring, the most CTAs on one SM, and
+// whether the grid should split the tile columns evenly.
+#ifndef TQ_GEMV_WARPS_T1
+#define TQ_GEMV_WARPS_T1 16
+#endif
+#ifndef TQ_GEMV_WARPS
+#define TQ_GEMV_WARPS 16
+#endif
+#ifndef TQ_GEMV_TILES_PER_WARP
+#define TQ_GEMV_TILES_PER_WARP 2
+#endif
+#ifndef TQ_GEMV_MAX_STAGES
+#define TQ_GEMV_MAX_STAGES 2
+#endif
+#ifndef TQ_GEMV_CTAS_PER_SM
+#define TQ_GEMV_CTAS_PER_SM 2
+#endif
+#ifndef TQ_GEMV_EVEN_GRID
+#define TQ_GEMV_EVEN_GRID 1
+#endif
+
 constexpr int kMaxTok = 8;
-// Groups per batch of weight loads kept in flight: deep for 1 token (bound
-// by the weight stream), shallower when the dot products dominate.
+constexpr int kTilesPerWarp = TQ_GEMV_TILES_PER_WARP;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Per token count: warps (each owns tiles of every stage), stage size, and
+// how many CTAs the register budget is planned for.
 template <int T>
-__host__ __device__ constexpr int batch_for() { return T == 1 ? 4 : 2; }
+struct Cfg {
+  static constexpr int kWarps = T == 1 ? TQ_GEMV_WARPS_T1 : TQ_GEMV_WARPS;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kStageTiles = kWarps * kTilesPerWarp;
+  static constexpr int kStageBytes = kStageTiles * kTileBytes;
+  static constexpr int kMinCtas = (T == 1 && kThreads <= 512) ? 2 : 1;
+};
 
 struct GemvArgs {
   const uint8_t* Wtq;
   const uint8_t* Xq;
   float* Y;
   int32_t* S;
+  int* status;
   int rows;
-  int ngroups;   // cols / 128
-  int nblk;      // cols / 256
-  int nrb;       // row tiles
-  int ksplit;    // warps per row tile
+  int ngroups;        // cols / 128
+  int nblk;           // cols / 256
+  int nrb;            // 32-row tile columns
+  int stages;         // ring depth
+  int early_weights;  // 1: the previous kernel does not write Wtq; prefetch before waiting
 };
 
 struct GroupCodes {
   uint4 lo, hi;     // weights 0..63 and 64..127 of this lane's row
-  uint16_t scale;   // fp16 bits of d_w
+  uint32_t scale;   // fp16 bits of d_w (low half)
 };
 
-__device__ __forceinline__ void load_group(const uint8_t* tile, int lane, GroupCodes& c) {
-  c.lo = ldg_stream_v4(tile + lane * 16);
-  c.hi = ldg_stream_v4(tile + 512 + lane * 16);
-  c.scale = ldg_u16(tile + kTileCodeBytes + lane * 2);
-}
 
 template <int T, bool kGroupSums>
 __device__ __forceinline__ void group_dot(const GroupCodes& c, int g, const int8_t* sq,
                                           const int* sgsum, const float* sdx, const GemvArgs& a,
                                           int row, float (&y)[T]) {
   const uint32_t wv[8] = {c.lo.x, c.lo.y, c.lo.z, c.lo.w, c.hi.x, c.hi.y, c.hi.z, c.hi.w};
-  const float dw = __half2float(__ushort_as_half(c.scale));
+  const float dw = __half2float(__ushort_as_half((unsigned short)c.scale));
   const int cols = a.ngroups * kGroup;
 #pragma unroll
   for (int t = 0; t < T; ++t) {
@@ -85,37 +119,94 @@ __device__ __forceinline__ void group_dot(const GroupCodes& c, int g, const int8
   }
 }
 
+// Shared memory: [ring][full bars][red-full bars][red-empty bars][slot counters]
+// [q8 values][group sums][scales][partial sums]
+struct SmemPlan {
+  int64_t ring, bars, counters, sq, sgsum, sdx, red, total;
+};
+
+template <int T>
+__host__ __device__ inline SmemPlan plan_smem(int stages, int64_t cols) {
+  SmemPlan p;
+  const int64_t g = cols / kGroup, b = cols / kQK;
+  p.ring = 0;
+  p.bars = (int64_t)stages * Cfg<T>::kStageBytes;        // full[S], redfull[2], redempty[2]
+  p.counters = p.bars + (stages + 4) * 8;                  // int[S]
+  p.sq = (p.counters + stages * 4 + 15) / 16 * 16;
+  p.sgsum = p.sq + T * cols;
+  p.sdx = p.sgsum + T * g * 4;
+  p.red = p.sdx + T * b * 4;
+  p.total = p.red + (int64_t)2 * Cfg<T>::kWarps * T * 32 * 4;
+  return p;
+}
+
 template <int T, bool kGroupSums>
-__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
+__global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kernel(const GemvArgs a) {
+  constexpr int kConsumers = Cfg<T>::kWarps;
+  constexpr int kStageTiles = Cfg<T>::kStageTiles;
+  constexpr int kStageBytes = Cfg<T>::kStageBytes;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int S = a.stages;
   const int cols = a.ngroups * kGroup;
-  int8_t* sq = reinterpret_cast<int8_t*>(smem);                 // [T][cols]
-  int* sgsum = reinterpret_cast<int*>(smem + T * cols);          // [T][ngroups]
-  float* sdx = reinterpret_cast<float*>(sgsum + T * a.ngroups);  // [T][nblk]
-  float* sred = sdx + T * a.nblk;                                // [kWarps][T][32]
+  const SmemPlan pl = plan_smem<T>(S, cols);
+  uint8_t* ring = smem + pl.ring;                                 // [S][stage]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + pl.bars);  // [S]
+  uint64_t* redfull = full + S;                                   // [2]
+  uint64_t* redempty = redfull + 2;                               // [2]
+  int* released = reinterpret_cast<int*>(smem + pl.counters);    // [S]
+  int8_t* sq = reinterpret_cast<int8_t*>(smem + pl.sq);           // [T][cols]
+  int* sgsum = reinterpret_cast<int*>(smem + pl.sgsum);           // [T][ngroups]
+  float* sdx = reinterpret_cast<float*>(smem + pl.sdx);           // [T][nblk]
+  float* red = reinterpret_cast<float*>(smem + pl.red);           // [2][kConsumers][T][32]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tiles_per_cta = kWarps / a.ksplit;
-  const int rb = blockIdx.x * tiles_per_cta + warp / a.ksplit;
-  const int part = warp % a.ksplit;
-  const int g0 = (int)((int64_t)a.ngroups * part / a.ksplit);
-  const int g1 = (int)((int64_t)a.ngroups * (part + 1) / a.ksplit);
-  const bool active = rb < a.nrb;
-  const int row = rb * kTileRows + lane;
-  const uint8_t* tiles = a.Wtq + (int64_t)rb * a.ngroups * kTileBytes;
+  // this CTA's tile columns, and the bulk copies (stages) that cover them
+  const int rb0 = (int)((int64_t)blockIdx.x * a.nrb / gridDim.x);
+  const int rb1 = (int)((int64_t)(blockIdx.x + 1) * a.nrb / gridDim.x);
+  const int per_rb = (a.ngroups + kStageTiles - 1) / kStageTiles;
+  const int nstage = (rb1 - rb0) * per_rb;
+  const uint64_t policy = l2_evict_first_policy();
 
-  constexpr int kBatch = batch_for<T>();
-  // First batch of weights goes out before the activations are staged.
-  GroupCodes cur[kBatch];
-  if (active) {
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u)
-      if (g0 + u < g1) load_group(tiles + (int64_t)(g0 + u) * kTileBytes, lane, cur[u]);
+  // Stage j of this CTA covers tile column rb0 + j / per_rb, groups from
+  // (j % per_rb) * kStageTiles; it lands in ring slot j % S. Counters below
+  // advance these incrementally (no division in the loop).
+  auto issue = [&](int slot, int rb, int st) {
+    const int gs = st * kStageTiles;
+    const uint32_t bytes = (uint32_t)(min(kStageTiles, a.ngroups - gs) * kTileBytes);
+    const uint32_t bar = smem_u32(full + slot);
+    mbarrier_arrive_expect_tx(bar, bytes);
+    bulk_copy_g2s(smem_u32(ring + (size_t)slot * kStageBytes),
+                  a.Wtq + ((int64_t)rb * a.ngroups + gs) * kTileBytes, bytes, bar, policy);
+  };
+  auto issue_first = [&]() {
+    int rb = rb0, st = 0;
+    for (int j = 0; j < min(S, nstage); ++j) {
+      issue(j, rb, st);
+      if (++st == per_rb) { st = 0; ++rb; }
+    }
+  };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbarrier_init(smem_u32(full + i), 1);
+      released[i] = 0;
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbarrier_init(smem_u32(redfull + i), kConsumers);
+      mbarrier_init(smem_u32(redempty + i), T);
+    }
+    mbarrier_init_fence();
+    // When the previous kernel in the stream is the quantizer (it does not
+    // write weights) the first stages go out before waiting for it.
+    if (a.early_weights) issue_first();
   }
+  pdl_launch_dependents();
+  pdl_wait_primary();   // the q8_K activations are written by the previous kernel
+  if (threadIdx.x == 0 && !a.early_weights) issue_first();
 
   // Stage q8_K activations: qs as a dense int8 [T][cols] array, the sum of each
   // 128-value half-block (8 partial sums), and the block scales.
-  for (int tb = warp; tb < T * a.nblk; tb += kWarps) {
+  for (int tb = warp; tb < T * a.nblk; tb += kConsumers) {
     const int t = tb / a.nblk, b = tb - t * a.nblk;
     const uint8_t* blk = a.Xq + (int64_t)tb * kQ8KBytes;
     const uint32_t* qs = reinterpret_cast<const uint32_t*>(blk + kQ8KQsOffset);
@@ -131,108 +222,164 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
   }
   __syncthreads();
 
-  float y[T];
+  bool failed = false;
+  int j = 0, slot = 0;
+  uint32_t phase = 0;
+  for (int rb = rb0, i = 0; rb < rb1; ++rb, ++i) {
+    const int row = rb * kTileRows + lane;
+    float y[T];
 #pragma unroll
-  for (int t = 0; t < T; ++t) y[t] = 0.0f;
-
-  if (active) {
-    for (int gb = g0; gb < g1; gb += kBatch) {
-      GroupCodes nxt[kBatch];
+    for (int t = 0; t < T; ++t) y[t] = 0.0f;
+    for (int st = 0; st < per_rb; ++st, ++j) {
+      const int gs = st * kStageTiles;
+      const int nt = min(kStageTiles, a.ngroups - gs);
+      if (!failed && !mbarrier_wait_bounded(smem_u32(full + slot), phase, kWaitLimitNs))
+        failed = true;
+      // this warp's tiles of the stage: warp, warp + 16, ... (spread for short stages)
+      GroupCodes c[kTilesPerWarp];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u)
-        if (gb + kBatch + u < g1)
-          load_group(tiles + (int64_t)(gb + kBatch + u) * kTileBytes, lane, nxt[u]);
+      for (int u = 0; u < kTilesPerWarp; ++u) {
+        const int tl = warp + u * kConsumers;
+        if (!failed && tl < nt) {
+          const uint8_t* tile = ring + (size_t)slot * kStageBytes + tl * kTileBytes;
+          c[u].lo = *reinterpret_cast<const uint4*>(tile + lane * 16);
+          c[u].hi = *reinterpret_cast<const uint4*>(tile + 512 + lane * 16);
+          c[u].scale = *reinterpret_cast<const uint16_t*>(tile + kTileCodeBytes + lane * 2);
+        }
+      }
+      __syncwarp();   // the whole warp has read its tile: release the slot
+      if (lane == 0) {
+        // the last of the 16 warps to release a slot refills it (nobody waits)
+        __threadfence_block();
+        if (atomicAdd(released + slot, 1) == kConsumers - 1) {
+          released[slot] = 0;
+          if (!failed && j + S < nstage) {
+            int st2 = st + S, rb2 = rb;
+            while (st2 >= per_rb) { st2 -= per_rb; ++rb2; }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(slot, rb2, st2);
+          }
+        }
+      }
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u)
-        if (gb + u < g1) group_dot<T, kGroupSums>(cur[u], gb + u, sq, sgsum, sdx, a, row, y);
+      for (int u = 0; u < kTilesPerWarp; ++u) {
+        const int tl = warp + u * kConsumers;
+        if (!failed && tl < nt) group_dot<T, kGroupSums>(c[u], gs + tl, sq, sgsum, sdx, a, row, y);
+      }
+      if (++slot == S) { slot = 0; phase ^= 1u; }
+    }
+    if (!kGroupSums) {
+      // The 16 partial sums of each row meet in shared memory; warp
+      // (i*T + t) % 16 adds those of token t in warp order (deterministic) and
+      // stores them. Buffers alternate between tile columns; mbarriers order
+      // the writers and the reducers, so no warp waits for all the others.
+      const int p = i & 1;
+      float* r = red + p * (kConsumers * T * 32);
+      if (i >= 2 && !failed &&
+          !mbarrier_wait_bounded(smem_u32(redempty + p), (uint32_t)(((i >> 1) - 1) & 1),
+                                 kWaitLimitNs))
+        failed = true;
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) cur[u] = nxt[u];
+      for (int t = 0; t < T; ++t) r[(warp * T + t) * 32 + lane] = y[t];
+      __syncwarp();
+      if (lane == 0) mbarrier_arrive(smem_u32(redfull + p));
+      const int t = (warp - i * T) & (kConsumers - 1);
+      if (t < T) {
+        if (!failed && !mbarrier_wait_bounded(smem_u32(redfull + p), (uint32_t)((i >> 1) & 1),
+                                              kWaitLimitNs))
+          failed = true;
+        float s = 0.0f;
+#pragma unroll
+        for (int k = 0; k < kConsumers; ++k) s += r[(k * T + t) * 32 + lane];
+        if (!failed && row < a.rows) a.Y[(int64_t)t * a.rows + row] = s;
+        __syncwarp();
+        if (lane == 0) mbarrier_arrive(smem_u32(redempty + p));
+      }
     }
   }
-  if (kGroupSums) return;
-
-  if (a.ksplit > 1) {
-#pragma unroll
-    for (int t = 0; t < T; ++t) sred[(warp * T + t) * 32 + lane] = y[t];
-    __syncthreads();
-    if (part != 0) return;
-#pragma unroll
-    for (int t = 0; t < T; ++t) {
-      float s = y[t];
-      for (int k = 1; k < a.ksplit; ++k) s += sred[((warp + k) * T + t) * 32 + lane];
-      y[t] = s;
+  if (failed && lane == 0) atomicExch(a.status, kDevTimeout);
+  // Copies can still be in flight only after a failed wait: then let the last
+  // stage of each slot land before the CTA's shared memory is released.
+  if (__syncthreads_or(failed) && threadIdx.x == 0) {
+    for (int sl = 0; sl < S && sl < nstage; ++sl) {
+      const int last = sl + (nstage - 1 - sl) / S * S;
+      mbarrier_wait_bounded(smem_u32(full + sl), (uint32_t)((last / S) & 1), kWaitLimitNs);
     }
-  }
-  if (active && row < a.rows) {
-#pragma unroll
-    for (int t = 0; t < T; ++t) a.Y[(int64_t)t * a.rows + row] = y[t];
   }
 }
 
 template <int T, bool G>
-const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(&gemv_kernel<T, G>);
+cudaError_t launch_t(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
+  static_assert(T >= 1 && T <= kMaxTok, "token count");
+  auto kernel = gemv_kernel<T, G>;
+  GemvArgs a = a0;
+  int dev = 0, optin = 0, nsm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+          cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  // deepest ring that fits
+  int stages = TQ_GEMV_MAX_STAGES;
+  while (stages > 2 && plan_smem<T>(stages, cols).total > optin) --stages;
+  const int64_t smem = plan_smem<T>(stages, cols).total;
+  if (smem > optin) return cudaErrorNotSupported;
+  a.stages = stages;
+  e = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), (int)smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, Cfg<T>::kThreads, (size_t)smem);
+  if (e != cudaSuccess) return e;
+  per_sm = max(1, min(per_sm, TQ_GEMV_CTAS_PER_SM));
+  int grid = (int)std::min<int64_t>(a.nrb, (int64_t)nsm * per_sm);
+#if TQ_GEMV_EVEN_GRID
+  // Prefer a grid that splits the tile columns evenly (every CTA the same
+  // work), if one exists within the top quarter of the resident capacity.
+  for (int g = grid; g >= grid - grid / 4 && g >= 1; --g)
+    if (a.nrb % g == 0) { grid = g; break; }
+#endif
+  return launch_pdl(kernel, dim3(grid), dim3(Cfg<T>::kThreads), (size_t)smem, s, a);
 }
 
 template <int T>
-cudaError_t launch_t(const GemvArgs& a, dim3 grid, int smem, bool gsum, cudaStream_t s) {
-  const void* fn = gsum ? kernel_ptr<T, true>() : kernel_ptr<T, false>();
-  cudaError_t e = ensure_dynamic_smem(fn, smem);
-  if (e != cudaSuccess) return e;
-  if (gsum)
-    gemv_kernel<T, true><<<grid, kThreads, smem, s>>>(a);
-  else
-    gemv_kernel<T, false><<<grid, kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_tok(const GemvArgs& a, int64_t cols, bool gsum, cudaStream_t s) {
+  return gsum ? launch_t<T, true>(a, cols, s) : launch_t<T, false>(a, cols, s);
 }
 
 }  // namespace
 
 int gemv_max_tokens() { return kMaxTok; }
 
-int64_t gemv_smem_bytes(int64_t cols, int ntok) {
-  const int64_t g = cols / kGroup, b = cols / kQK;
-  return ntok * cols + ntok * g * 4 + ntok * b * 4 + (int64_t)kWarps * ntok * 32 * 4;
-}
 
 cudaError_t launch_gemv(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t* S,
-                        int64_t rows, int64_t cols, int ntok, cudaStream_t s) {
+                        int64_t rows, int64_t cols, int ntok, int* dev_status, bool early_weights,
+                        cudaStream_t s) {
   if (ntok < 1 || ntok > kMaxTok) return cudaErrorNotSupported;
-  const int64_t smem = gemv_smem_bytes(cols, ntok);
-  int dev = 0, optin = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  if (e != cudaSuccess) return e;
-  if (smem > optin || rows > 0x7fffffff / 2) return cudaErrorNotSupported;
-
+  if (rows > 0x7fffffff / 2 || cols / kGroup > 0x7fffffff / kTileBytes)
+    return cudaErrorNotSupported;
   GemvArgs a;
   a.Wtq = Wtq;
   a.Xq = Xq;
   a.Y = Y;
   a.S = S;
+  a.status = dev_status;
   a.rows = (int)rows;
   a.ngroups = (int)(cols / kGroup);
   a.nblk = (int)(cols / kQK);
   a.nrb = (int)((rows + kTileRows - 1) / kTileRows);
-  // Split the groups of a tile column over more warps until ~2048 warps are
-  // busy, keeping at least two groups per warp.
-  int ksplit = 1;
-  while (ksplit < kWarps && (int64_t)a.nrb * ksplit < 2048 && a.ngroups / (ksplit * 2) >= 2)
-    ksplit *= 2;
-  a.ksplit = ksplit;
-  const int tiles_per_cta = kWarps / ksplit;
-  const dim3 grid((unsigned)((a.nrb + tiles_per_cta - 1) / tiles_per_cta));
+  a.stages = 2;
+  a.early_weights = early_weights ? 1 : 0;
   const bool gsum = S != nullptr;
   switch (ntok) {
-    case 1: return launch_t<1>(a, grid, (int)smem, gsum, s);
-    case 2: return launch_t<2>(a, grid, (int)smem, gsum, s);
-    case 3: return launch_t<3>(a, grid, (int)smem, gsum, s);
-    case 4: return launch_t<4>(a, grid, (int)smem, gsum, s);
-    case 5: return launch_t<5>(a, grid, (int)smem, gsum, s);
-    case 6: return launch_t<6>(a, grid, (int)smem, gsum, s);
-    case 7: return launch_t<7>(a, grid, (int)smem, gsum, s);
-    default: return launch_t<8>(a, grid, (int)smem, gsum, s);
+    case 1: return launch_tok<1>(a, cols, gsum, s);
+    case 2: return launch_tok<2>(a, cols, gsum, s);
+    case 3: return launch_tok<3>(a, cols, gsum, s);
+    case 4: return launch_tok<4>(a, cols, gsum, s);
+    case 5: return launch_tok<5>(a, cols, gsum, s);
+    case 6: return launch_tok<6>(a, cols, gsum, s);
+    case 7: return launch_tok<7>(a, cols, gsum, s);
+    default: return launch_tok<8>(a, cols, gsum, s);
   }
 }
 

@@ -52,6 +52,99 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
   return d;
 }
 
+// ---------------------------------------------------------------- mbarrier / bulk copy
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbarrier_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbarrier_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// One bounded poll: the thread may sleep in hardware up to `hint_ns` for the
+// phase to complete (it wakes as soon as it does), so waiting costs no issue
+// slots.
+__device__ __forceinline__ bool mbarrier_try_wait(uint32_t bar, uint32_t parity,
+                                                  uint32_t hint_ns = 20000u) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of an mbarrier, giving up after `limit_ns` of global
+// time (checked every 16 polls, with a cap of 2^28 polls). Returns false on
+// giving up; the caller records the failure and stops using the barrier.
+__device__ __forceinline__ bool mbarrier_wait_bounded(uint32_t bar, uint32_t parity,
+                                                      uint64_t limit_ns) {
+  if (mbarrier_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0; it < (1u << 28); ++it) {
+    if (mbarrier_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 15u && global_timer_ns() - t0 > limit_ns) return false;
+  }
+  return false;
+}
+
+// Arm an mbarrier for `bytes` of incoming bulk-copy data (one arrival).
+__device__ __forceinline__ void mbarrier_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+// L2 policy for data read once per launch: evict it first.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// 1-D bulk copy global -> shared (TMA), completion counted on an mbarrier.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// Plain arrival on an mbarrier (release semantics at CTA scope).
+__device__ __forceinline__ void mbarrier_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Named barrier for a subset of the CTA's warps (ids 1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue, and wait until the previous kernel's results are visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- launchers
 // Each returns a cudaError_t from the launch (cudaSuccess if nothing ran).
 
@@ -61,11 +154,32 @@ cudaError_t launch_repack(const uint8_t* Wpq2, uint8_t* Wtq, int64_t rows, int64
 cudaError_t launch_unrepack(const uint8_t* Wtq, uint8_t* Wpq2, int64_t rows, int64_t cols,
                             cudaStream_t s);
 
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel in the stream finishes; it must call pdl_wait_primary()
+// before reading that kernel's output.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // GEMV for 1..8 tokens. Returns cudaErrorNotSupported (without launching)
 // when the activations of all tokens do not fit in shared memory.
+// early_weights: the kernel enqueued just before on the stream does not write
+// Wtq, so weight reads may start before waiting for it.
 cudaError_t launch_gemv(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t* S,
-                        int64_t rows, int64_t cols, int ntok, cudaStream_t s);
-int64_t gemv_smem_bytes(int64_t cols, int ntok);
+                        int64_t rows, int64_t cols, int ntok, int* dev_status, bool early_weights,
+                        cudaStream_t s);
 int gemv_max_tokens();
 
 // Tensor-core path for any ntok >= 1 (used for ntok > gemv_max_tokens()).

@@ -24,6 +24,10 @@ __device__ __forceinline__ uint32_t pack4_s8(int a, int b, int c, int d) {
 
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
 quantize_q8K_kernel(const float* __restrict__ X, uint8_t* __restrict__ Xq, int64_t nblocks) {
+  // Launched as a programmatic dependent: start early, but touch no memory
+  // before the previous kernel in the stream has finished.
+  pdl_launch_dependents();
+  pdl_wait_primary();
   const int lane = threadIdx.x & 31;
   const int64_t blk = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   if (blk >= nblocks) return;  // whole warp leaves together
@@ -73,8 +77,8 @@ cudaError_t launch_quantize_q8K(const float* X, uint8_t* Xq, int64_t nblocks, cu
   if (nblocks <= 0) return cudaSuccess;
   const int64_t grid = (nblocks + kWarpsPerCta - 1) / kWarpsPerCta;
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  quantize_q8K_kernel<<<(unsigned)grid, kWarpsPerCta * 32, 0, s>>>(X, Xq, nblocks);
-  return cudaGetLastError();
+  return launch_pdl(quantize_q8K_kernel, dim3((unsigned)grid), dim3(kWarpsPerCta * 32), 0, s, X,
+                    Xq, nblocks);
 }
 
 }  // namespace tq

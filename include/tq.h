@@ -138,6 +138,13 @@ int tq_unrepack(const void *Wtq, void *Wpq2, int64_t rows, int64_t cols, void *s
  *   Xq  [ntok][cols/256] q8_K blocks, 16-byte aligned.
  *   Y   [ntok][rows] f32, 4-byte aligned, overwritten (not accumulated).
  * With cols == 0 and rows, ntok > 0, Y is set to zero.
+ * Overlap: the kernels are launched as programmatic dependents, so they may
+ * start while the kernel enqueued before them on the stream is finishing; they
+ * wait for it before reading Xq. When the previous call this library received
+ * for the stream was tq_quantize_q8K, the GEMV also starts reading Wtq before
+ * that wait, since the quantizer never writes weights; so do not write Wtq
+ * with a kernel of your own between tq_quantize_q8K and tq_matmul on one
+ * stream (copies and events are fine).
  * Errors: TQ_ERR_SHAPE if cols % 256 != 0; TQ_ERR_ALIAS if Y overlaps an input.
  */
 int tq_matmul(const void *Wtq, const void *Xq, float *Y, int64_t rows, int64_t cols,
