@@ -1,5 +1,5 @@
 // tq_gemm_tc.cu -- ternary x q8_K product for many tokens on the 5th-generation
-// tensor cores (tcgen05.mma, accumulators in tensor memory).
+// tensor cores (tcgen05.mma, operands and accumulators in tensor memory).
 //
 // With many tokens a loaded weight is reused by all of them and instruction
 // count, not the bus, bounds the work (ternary post, "prefill wants a
@@ -11,87 +11,64 @@
 // tensor rate is a small fraction of its f16 rate, so f16 is the faster exact
 // route.)
 //
-// Per CTA: M = 128 weight rows (four 32-row tiles) x N = 64 tokens (zero
-// padded; post, "the leftovers": pad, run one pass, store only the real
-// outputs). For each 128-weight group g:
-//   1. each thread unpacks its row's 128 codes straight to f16 w = u - 1 and
-//      writes them to shared memory in the UMMA K-major no-swizzle layout;
-//      threads also convert the group's int8 activations of all 64 tokens;
-//   2. one thread issues 8 MMAs (K = 16 each) into a TMEM accumulator and
-//      commits them to an mbarrier;
-//   3. every thread reads its row of the accumulator (exact group sums) with
-//      tcgen05.ld and applies d_w[r][g] * d_x[t][g/2] in f32.
+// One CTA computes 128 weight rows x 64 tokens (tokens zero-padded; ternary
+// post, "the leftovers": pad, run one pass, store only the real outputs).
+// Each 128-weight group g flows through a 3-stage ring:
+//   - 8 converter warps load the group's codes (16 bytes per row-half per
+//     thread) and unpack them straight to f16 w = u - 1: (code & mask) | 0x6400
+//     is 1024 + u*4^s, one HFMA2 by 4^-s takes off the 1024 and the 1. The
+//     result goes into tensor memory with tcgen05.st as the MMA's A operand
+//     (lane = row), so A never touches shared memory. They also convert the
+//     group's int8 activations of the 64 tokens to f16 into shared memory in
+//     the UMMA K-major layout (the B operand). Loads for group g+1 are in
+//     flight while group g is converted.
+//   - one thread issues 8 MMAs (M=128, N=64, K=16) into the stage's TMEM
+//     accumulator and commits them to an mbarrier.
+//   - 8 epilogue warps read the accumulator (exact group sums) with
+//     tcgen05.ld and apply d_w[r][g] * d_x[t][g/2] in f32.
 // Each group's sum stays separate because the weight scale changes from
-// group to group.
+// group to group; the ring lets conversion, MMA and epilogue of consecutive
+// groups overlap.
 #include "tq_internal.cuh"
 
 namespace tq {
 namespace {
 
-constexpr int kM = 128;       // rows per CTA = UMMA M
-constexpr int kN = 64;        // tokens per CTA = UMMA N
-constexpr int kThreads = 128;
+constexpr int kM = 128;          // weight rows per CTA (UMMA M)
+constexpr int kN = 64;           // tokens per CTA (UMMA N)
+constexpr int kStages = 3;
+constexpr int kConvWarps = 8;    // converters: warp w -> rows 32*(w%4).., k half w/4
+constexpr int kEpiWarps = 8;     // epilogue: warp w -> rows 32*(w%4).., tokens 32*(w/4)..
+constexpr int kMmaWarp = kConvWarps + kEpiWarps;
+constexpr int kThreads = (kMmaWarp + 1) * 32;
 constexpr int kTilesPerCta = kM / kTileRows;
-constexpr uint32_t kTmemCols = 64;  // one f32 accumulator of 128 lanes x 64 columns
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCol = 0;      // stage s accumulator: columns s*64 ..
+constexpr uint32_t kACol = 192;      // stage s A operand: columns 192 + s*64 ..
 
-// UMMA canonical K-major layout without swizzle: a core matrix is 8 rows x 16
-// bytes stored as 128 contiguous bytes; LBO = distance between core matrices
-// along K, SBO = distance between 8-row groups. A group (128 f16 along K) is
-// 16 core matrices per 8-row group.
+// UMMA canonical K-major layout without swizzle for B: a core matrix is 8
+// tokens x 16 bytes stored as 128 contiguous bytes; LBO = distance between
+// core matrices along K, SBO = distance between 8-token groups.
 constexpr uint32_t kLBO = 128;
 constexpr uint32_t kSBO = 16 * 128;
-constexpr int kABytes = kM * kGroup * 2;   // 32 KB
-constexpr int kBBytes = kN * kGroup * 2;   // 16 KB
-constexpr int kSmemBytes = kABytes + kBBytes + kN * 4 + 16;
+constexpr int kBBytes = kN * kGroup * 2;   // 16 KB per stage
+constexpr int kSmemUsed = kStages * kBBytes + kStages * (kM + kN) * 4 + 3 * kStages * 8 + 16;
+// Request enough shared memory that only one CTA fits on an SM: each CTA
+// allocates all 512 tensor-memory columns.
+constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
 
 // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B f16
 // (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
 // M >> 4 at bits 24-28.
 constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kN >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s; an MMA group takes microseconds
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // Shared-memory matrix descriptor: start >> 4 (bits 0-13), LBO >> 4 (16-29),
 // SBO >> 4 (32-45), the constant 0b001 at bits 46-48, no swizzle (61-63 = 0).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(kLBO >> 4) << 16) |
          ((uint64_t)(kSBO >> 4) << 32) | (1ull << 46);
-}
-
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait: gives up after kWaitLimitNs of global time (or 2^30 polls).
-__device__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer();
-  for (uint32_t it = 0; it < (1u << 30); ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 255u && globaltimer() - t0 > kWaitLimitNs) return false;
-  }
-  return false;
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -101,13 +78,14 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16.
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -116,19 +94,34 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                ::"r"(bar) : "memory");
 }
 
-// 16 consecutive f32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
+// 32 consecutive 32-bit columns of this thread's TMEM lane -> registers.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// registers -> 32 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+        "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
+        "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]),
+        "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+        "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
 }
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
@@ -168,155 +161,210 @@ struct TcArgs {
   int nrb;
 };
 
+// What one converter thread loads for one group.
+struct ConvIn {
+  uint4 codes;      // 64 weights of its row (half of the group)
+  uint32_t scale;   // fp16 bits of d_w (used by the k-half-0 threads)
+  uint32_t q[8];    // 32 int8 activations of its token
+  float dx;         // q8_K scale of its token's block (k-quarter-0 threads)
+};
+
 template <bool kGroupSums>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + kABytes;
-  float* sdx = reinterpret_cast<float*>(smem + kABytes + kBBytes);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sdx + kN);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
+  uint8_t* sB = smem;                                                          // [S][16 KB]
+  float* sdw = reinterpret_cast<float*>(smem + kStages * kBBytes);             // [S][128]
+  float* sdx = sdw + kStages * kM;                                             // [S][64]
+  uint64_t* conv_full = reinterpret_cast<uint64_t*>(sdx + kStages * kN);       // [S]
+  uint64_t* mma_done = conv_full + kStages;                                    // [S]
+  uint64_t* stage_free = mma_done + kStages;                                   // [S]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stage_free + kStages);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t bar_a = smem_addr(bar);
+  const int G = a.ngroups;
 
-  if (warp == 0) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                 ::"r"(smem_addr(tmem_slot)), "r"(kTmemCols) : "memory");
+                 ::"r"(smem_u32(tmem_slot)), "r"(kTmemCols) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 0) {
-    mbar_init(bar_a, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int s = 0; s < kStages; ++s) {
+      mbarrier_init(smem_u32(conv_full + s), kConvWarps * 32);
+      mbarrier_init(smem_u32(mma_done + s), 1);
+      mbarrier_init(smem_u32(stage_free + s), kEpiWarps * 32);
+    }
+    mbarrier_init_fence();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
-  // this thread's weight row and its activation duty
-  const int64_t rb = (int64_t)blockIdx.x * kTilesPerCta + warp;
-  const int64_t row = rb * kTileRows + lane;
-  const uint8_t* tiles = a.Wtq + rb * a.ngroups * kTileBytes;
-  const bool row_tile_ok = rb < a.nrb;
-  const int n_local = tid & (kN - 1);          // token converted by this thread
-  const int k_half = tid >> 6;                 // which 64 activations of the group
-  const int64_t tok = (int64_t)blockIdx.y * kN + n_local;
-  const bool tok_ok = tok < a.ntok;
-  const uint32_t a_row_off = (uint32_t)((tid >> 3) * kSBO + (tid & 7) * 16);
-  const uint32_t b_row_off = (uint32_t)((n_local >> 3) * kSBO + (n_local & 7) * 16);
-
-  float y[kN];
-#pragma unroll
-  for (int n = 0; n < kN; ++n) y[n] = 0.0f;
   bool failed = false;
 
-  for (int g = 0; g < a.ngroups; ++g) {
-    // ---- 1a. weights of this row -> f16 w in A (row tid, K-major)
-    uint32_t wv[8];
-    uint16_t sbits = 0;
-    if (row_tile_ok) {
-      const uint8_t* tile = tiles + (int64_t)g * kTileBytes;
-      const uint4 lo = ldg_stream_v4(tile + lane * 16);
-      const uint4 hi = ldg_stream_v4(tile + 512 + lane * 16);
-      sbits = ldg_u16(tile + kTileCodeBytes + lane * 2);
-      wv[0] = lo.x; wv[1] = lo.y; wv[2] = lo.z; wv[3] = lo.w;
-      wv[4] = hi.x; wv[5] = hi.y; wv[6] = hi.z; wv[7] = hi.w;
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) wv[i] = 0x55555555u;  // w = 0
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      // word i: weights 16i + 4s + j sit in byte j at bits 2s
-      const uint32_t x01 = __byte_perm(wv[i], 0, 0x4140);  // bytes 0,1 -> low byte of each half
-      const uint32_t x23 = __byte_perm(wv[i], 0, 0x4342);  // bytes 2,3
-      const uint4 c0 = make_uint4(codes_to_w<0>(x01), codes_to_w<0>(x23), codes_to_w<1>(x01),
-                                  codes_to_w<1>(x23));       // k = 16i .. 16i+7
-      const uint4 c1 = make_uint4(codes_to_w<2>(x01), codes_to_w<2>(x23), codes_to_w<3>(x01),
-                                  codes_to_w<3>(x23));       // k = 16i+8 .. 16i+15
-      *reinterpret_cast<uint4*>(sA + a_row_off + (2 * i) * kLBO) = c0;
-      *reinterpret_cast<uint4*>(sA + a_row_off + (2 * i + 1) * kLBO) = c1;
-    }
+  if (warp < kConvWarps) {
+    // ---------------- converters
+    const int q4 = warp & 3, khalf = warp >> 2;          // row quarter, k half of A
+    const int64_t rb = (int64_t)blockIdx.x * kTilesPerCta + q4;
+    const bool row_ok = rb < a.nrb;
+    const uint8_t* tiles = a.Wtq + rb * G * kTileBytes + khalf * 512 + lane * 16;
+    const int ct = warp * 32 + lane;                      // 0..255
+    const int n = ct & (kN - 1), kq = ct >> 6;            // token, k quarter of B
+    const int64_t tok = (int64_t)blockIdx.y * kN + n;
+    const bool tok_ok = tok < a.ntok;
+    const uint8_t* xrow = a.Xq + tok * a.nblk * kQ8KBytes;
+    const uint32_t b_off = (uint32_t)((n >> 3) * kSBO + (n & 7) * 16);
+    const uint32_t a_lane = (uint32_t)(q4 * 32) << 16;
 
-    // ---- 1b. activations: token n_local, k = 64*k_half .. +63 -> f16 in B
-    {
-      uint32_t q[16];
+    auto load = [&](int g, ConvIn& in) {
+      if (row_ok) {
+        const uint8_t* t = tiles + (int64_t)g * kTileBytes;
+        in.codes = ldg_stream_v4(t);
+        in.scale = khalf == 0 ? ldg_u16(t - khalf * 512 - lane * 16 + kTileCodeBytes + lane * 2) : 0u;
+      } else {
+        in.codes = make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);  // w = 0
+        in.scale = 0u;
+      }
       if (tok_ok) {
-        const uint8_t* blk = a.Xq + (tok * a.nblk + (g >> 1)) * kQ8KBytes;
+        const uint8_t* blk = xrow + (int64_t)(g >> 1) * kQ8KBytes;
         const uint32_t* src =
-            reinterpret_cast<const uint32_t*>(blk + kQ8KQsOffset + (g & 1) * 128 + k_half * 64);
+            reinterpret_cast<const uint32_t*>(blk + kQ8KQsOffset + (g & 1) * 128 + kq * 32);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) q[i] = __ldg(src + i);
-        if (k_half == 0) sdx[n_local] = __ldg(reinterpret_cast<const float*>(blk));
+        for (int i = 0; i < 8; ++i) in.q[i] = __ldg(src + i);
+        in.dx = kq == 0 ? __ldg(reinterpret_cast<const float*>(blk)) : 0.0f;
       } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) q[i] = 0u;
-        if (k_half == 0) sdx[n_local] = 0.0f;
+        for (int i = 0; i < 8; ++i) in.q[i] = 0u;
+        in.dx = 0.0f;
       }
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {  // 8 activations per core-matrix row
-        uint4 h;
-        s8x4_to_h2x2(q[2 * c], h.x, h.y);
-        s8x4_to_h2x2(q[2 * c + 1], h.z, h.w);
-        *reinterpret_cast<uint4*>(sB + b_row_off + (k_half * 8 + c) * kLBO) = h;
-      }
-    }
-    // generic-proxy smem writes -> visible to the tensor core (async proxy)
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncthreads();
+    };
 
-    // ---- 2. one thread issues the group's 8 MMAs (K = 16 each)
-    if (tid == 0) {
+    ConvIn cur, nxt;
+    load(0, cur);
+    int s = 0;
+    uint32_t ph = 0;
+    for (int g = 0; g < G; ++g) {
+      if (g + 1 < G) load(g + 1, nxt);
+      // stage s is free once the epilogue has drained group g - 3
+      if (g >= kStages && !failed &&
+          !mbarrier_wait_bounded(smem_u32(stage_free + s), ph ^ 1u, kWaitLimitNs))
+        failed = true;
+      failed = __any_sync(0xffffffffu, failed);   // tcgen05.st below is warp-wide
       tc_fence_after();
-      const uint32_t a0 = smem_addr(sA), b0 = smem_addr(sB);
+      if (!failed) {
+        // A: 64 weights of this row -> 32 f16 pairs in TMEM (columns = k pairs)
+        uint32_t wa[32];
+        const uint32_t wv[4] = {cur.codes.x, cur.codes.y, cur.codes.z, cur.codes.w};
 #pragma unroll
-      for (int kk = 0; kk < kGroup / 16; ++kk)
-        mma_f16(tmem, smem_desc(a0 + kk * 2 * kLBO), smem_desc(b0 + kk * 2 * kLBO), kIdesc,
-                kk > 0 ? 1u : 0u);
-      mma_commit(bar_a);
+        for (int i = 0; i < 4; ++i) {
+          // word i: weights 16i + 4s + j in byte j at bits 2s (k local to this half)
+          const uint32_t x01 = __byte_perm(wv[i], 0, 0x4140);
+          const uint32_t x23 = __byte_perm(wv[i], 0, 0x4342);
+          wa[8 * i + 0] = codes_to_w<0>(x01);
+          wa[8 * i + 1] = codes_to_w<0>(x23);
+          wa[8 * i + 2] = codes_to_w<1>(x01);
+          wa[8 * i + 3] = codes_to_w<1>(x23);
+          wa[8 * i + 4] = codes_to_w<2>(x01);
+          wa[8 * i + 5] = codes_to_w<2>(x23);
+          wa[8 * i + 6] = codes_to_w<3>(x01);
+          wa[8 * i + 7] = codes_to_w<3>(x23);
+        }
+        tmem_st32(tmem + a_lane + kACol + (uint32_t)s * 64 + (uint32_t)khalf * 32, wa);
+        // B: 32 activations of token n -> 4 core-matrix rows (8 k each)
+        uint8_t* b = sB + s * kBBytes + b_off;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4 h;
+          s8x4_to_h2x2(cur.q[2 * c], h.x, h.y);
+          s8x4_to_h2x2(cur.q[2 * c + 1], h.z, h.w);
+          *reinterpret_cast<uint4*>(b + (kq * 4 + c) * kLBO) = h;
+        }
+        if (khalf == 0) sdw[s * kM + q4 * 32 + lane] = __half2float(__ushort_as_half((unsigned short)cur.scale));
+        if (kq == 0) sdx[s * kN + n] = cur.dx;
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      mbarrier_arrive(smem_u32(conv_full + s));
+      cur = nxt;
+      if (++s == kStages) { s = 0; ph ^= 1u; }
     }
-
-    // ---- 3. wait for the accumulator, then scale and accumulate in f32
-    const bool ok = mbar_wait_bounded(bar_a, (uint32_t)(g & 1));
-    if (__syncthreads_or(!ok)) {
-      failed = true;
-      break;
-    }
-    tc_fence_after();
-    const float dw = __half2float(__ushort_as_half(sbits));
+  } else if (warp < kMmaWarp) {
+    // ---------------- epilogue
+    const int ew = warp - kConvWarps;
+    const int q4 = ew & 3, nhalf = ew >> 2;               // row quarter, token half
+    const int64_t row = ((int64_t)blockIdx.x * kTilesPerCta + q4) * kTileRows + lane;
+    const int n0 = nhalf * 32;
+    const uint32_t acc_lane = (uint32_t)(q4 * 32) << 16;
+    float y[32];
 #pragma unroll
-    for (int c = 0; c < kN / 16; ++c) {
-      float acc[16];
-      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c * 16, acc);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int n = c * 16 + j;
+    for (int j = 0; j < 32; ++j) y[j] = 0.0f;
+    int s = 0;
+    uint32_t ph = 0;
+    for (int g = 0; g < G; ++g) {
+      if (!failed && !mbarrier_wait_bounded(smem_u32(mma_done + s), ph, kWaitLimitNs)) failed = true;
+      failed = __any_sync(0xffffffffu, failed);   // tcgen05.ld below is warp-wide
+      tc_fence_after();
+      if (!failed) {
+        uint32_t acc[32];
+        tmem_ld32(tmem + acc_lane + kAccCol + (uint32_t)s * 64 + (uint32_t)n0, acc);
         if (kGroupSums) {
-          const int64_t t = (int64_t)blockIdx.y * kN + n;
-          if (row_tile_ok && row < a.rows && t < a.ntok)
-            a.S[(t * a.rows + row) * a.ngroups + g] = __float2int_rn(acc[j]);
+          if (row < a.rows) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int64_t t = (int64_t)blockIdx.y * kN + n0 + j;
+              if (t < a.ntok) a.S[(t * a.rows + row) * G + g] = __float2int_rn(__uint_as_float(acc[j]));
+            }
+          }
         } else {
-          y[n] = fmaf(dw * sdx[n], acc[j], y[n]);
+          const float dw = sdw[s * kM + q4 * 32 + lane];
+          const float4* dx4 = reinterpret_cast<const float4*>(sdx + s * kN + n0);
+#pragma unroll
+          for (int j4 = 0; j4 < 8; ++j4) {
+            const float4 d = dx4[j4];
+            y[4 * j4 + 0] = fmaf(dw * d.x, __uint_as_float(acc[4 * j4 + 0]), y[4 * j4 + 0]);
+            y[4 * j4 + 1] = fmaf(dw * d.y, __uint_as_float(acc[4 * j4 + 1]), y[4 * j4 + 1]);
+            y[4 * j4 + 2] = fmaf(dw * d.z, __uint_as_float(acc[4 * j4 + 2]), y[4 * j4 + 2]);
+            y[4 * j4 + 3] = fmaf(dw * d.w, __uint_as_float(acc[4 * j4 + 3]), y[4 * j4 + 3]);
+          }
         }
       }
+      tc_fence_before();
+      mbarrier_arrive(smem_u32(stage_free + s));
+      if (++s == kStages) { s = 0; ph ^= 1u; }
     }
-    tc_fence_before();
-    __syncthreads();  // all TMEM reads and sA/sB/sdx reads done before the next group
-  }
-
-  if (failed && tid == 0) atomicExch(a.status, kDevTimeout);
-  if (!failed && !kGroupSums && row_tile_ok && row < a.rows) {
+    if (!kGroupSums && !failed && row < a.rows) {
 #pragma unroll
-    for (int n = 0; n < kN; ++n) {
-      const int64_t t = (int64_t)blockIdx.y * kN + n;
-      if (t < a.ntok) a.Y[t * a.rows + row] = y[n];
+      for (int j = 0; j < 32; ++j) {
+        const int64_t t = (int64_t)blockIdx.y * kN + n0 + j;
+        if (t < a.ntok) a.Y[t * a.rows + row] = y[j];
+      }
+    }
+  } else if (lane == 0) {
+    // ---------------- MMA issuer
+    const uint32_t b0 = smem_u32(sB);
+    int s = 0;
+    uint32_t ph = 0;
+    for (int g = 0; g < G; ++g) {
+      if (!failed && !mbarrier_wait_bounded(smem_u32(conv_full + s), ph, kWaitLimitNs)) failed = true;
+      tc_fence_after();
+      if (!failed) {
+        const uint32_t d = tmem + kAccCol + (uint32_t)s * 64;
+        const uint32_t at = tmem + kACol + (uint32_t)s * 64;
+#pragma unroll
+        for (int kk = 0; kk < kGroup / 16; ++kk)
+          mma_f16_tmem_a(d, at + 8 * kk, smem_desc(b0 + s * kBBytes + kk * 2 * kLBO), kIdesc,
+                         kk > 0 ? 1u : 0u);
+      }
+      mma_commit(smem_u32(mma_done + s));   // also on failure: keeps the epilogue's phases moving
+      if (++s == kStages) { s = 0; ph ^= 1u; }
     }
   }
 
+  if (failed) atomicExch(a.status, kDevTimeout);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols) : "memory");
