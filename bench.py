@@ -62,6 +62,8 @@ def parse_args():
     p.add_argument("--no-extra", action="store_true", help="skip the 4- and 64-token tiles")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    p.add_argument("--tensor-rates", action="store_true",
+                   help="only measure library int8 / bf16 / f16 GEMM rates (operand-type choice)")
     return p.parse_args()
 
 
@@ -195,13 +197,14 @@ class Workload:
         self.X = torch.from_numpy(x).to(device)
         self.Xq = tq.q8K_empty(self.ntok, self.cols, device)
         self.Y = torch.empty((self.ntok, self.rows), dtype=torch.float32, device=device)
+        self.ws = tq.workspace_empty(self.rows, self.cols, self.ntok, device)
         self.device = device
 
     def step(self, i, stream=None):
         import bit_matvec_gb300 as tq
         tq.tq_quantize_q8K(self.X, self.Xq, self.ntok, self.cols, stream)
-        tq.tq_matmul(self.W[i % self.copies], self.Xq, self.Y, self.rows, self.cols, self.ntok,
-                     stream)
+        tq.tq_matmul_ws(self.W[i % self.copies], self.Xq, self.Y, self.rows, self.cols, self.ntok,
+                        self.ws, stream)
 
     def weights(self):
         return self.rows * self.cols
@@ -256,13 +259,13 @@ def time_graph(wl: Workload, steps: int, warmup: int, world: int):
         gm = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gm, stream=stream):
             for i in range(n):
-                tq.tq_matmul(wl.W[i], wl.Xq, wl.Y, wl.rows, wl.cols, wl.ntok, stream)
+                tq.tq_matmul_ws(wl.W[i], wl.Xq, wl.Y, wl.rows, wl.cols, wl.ntok, wl.ws, stream)
         gb = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gb, stream=stream):
             for i in range(n):
                 tq.tq_quantize_q8K(wl.X, wl.Xq, wl.ntok, wl.cols, stream)
                 ev[i][0].record(stream)
-                tq.tq_matmul(wl.W[i], wl.Xq, wl.Y, wl.rows, wl.cols, wl.ntok, stream)
+                tq.tq_matmul_ws(wl.W[i], wl.Xq, wl.Y, wl.rows, wl.cols, wl.ntok, wl.ws, stream)
                 ev[i][1].record(stream)
         reps = -(-steps // n)
         for g in (ga, gm, gb):                          # graph warm-up replays
@@ -297,7 +300,7 @@ def time_e2e(wl: Workload, steps: int, warmup: int):
     def one(i):
         X.copy_(x_pin, non_blocking=True)
         tq.tq_quantize_q8K(X, wl.Xq, wl.ntok, wl.cols, stream)
-        tq.tq_matmul(wl.W[i % wl.copies], wl.Xq, wl.Y, wl.rows, wl.cols, wl.ntok, stream)
+        tq.tq_matmul_ws(wl.W[i % wl.copies], wl.Xq, wl.Y, wl.rows, wl.cols, wl.ntok, wl.ws, stream)
         y_pin.copy_(wl.Y, non_blocking=True)
 
     for i in range(max(warmup, 3)):
@@ -454,8 +457,46 @@ def measure(name, args, rank, world, device, peaks, peak_kind, steps):
     return wl, res
 
 
+def tensor_rates():
+    """Dense tensor-core rate by operand type through the vendor GEMMs (int8 via
+    torch._int_mm, bf16 and f16 via matmul), square n x n x n, 3 warm-up and 20
+    timed launches with CUDA events. Decides which MMA kind the tensor-core
+    path uses; prints one JSON line per size."""
+    import torch
+    torch.backends.cuda.matmul.allow_tf32 = False
+    dev = torch.device("cuda", 0)
+
+    def rate(fn, flops, reps=20):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return flops / (a.elapsed_time(b) / reps / 1e3) / 1e12
+
+    g = torch.Generator(device=dev).manual_seed(1)
+    for n in (4096, 8192, 16384):
+        a8 = torch.randint(-127, 127, (n, n), dtype=torch.int8, device=dev, generator=g)
+        b8 = torch.randint(-127, 127, (n, n), dtype=torch.int8, device=dev,
+                           generator=g).t().contiguous().t()
+        ab = torch.randn(n, n, dtype=torch.bfloat16, device=dev, generator=g)
+        bb = torch.randn(n, n, dtype=torch.bfloat16, device=dev, generator=g)
+        ah, bh = ab.half(), bb.half()
+        print(json.dumps({"n": n,
+                          "int8_tops": round(rate(lambda: torch._int_mm(a8, b8), 2 * n ** 3), 1),
+                          "bf16_tflops": round(rate(lambda: ab @ bb, 2 * n ** 3), 1),
+                          "f16_tflops": round(rate(lambda: ah @ bh, 2 * n ** 3), 1)}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.tensor_rates:
+        tensor_rates()
+        return
     rank, world, local = dist_init(args.gpus)
     if args.impl == "reference":
         run_reference(args, rank, world)

@@ -27,6 +27,7 @@ TQ_ERR_ALIGN = -3
 TQ_ERR_CUDA = -4
 TQ_ERR_TIMEOUT = -5
 TQ_ERR_ALIAS = -6
+TQ_ERR_WORKSPACE = -7
 
 QK_K = 256
 GROUP = 128
@@ -74,6 +75,9 @@ def _load():
             "tq_unrepack": ([P, P, I64, I64, P], I),
             "tq_matmul": ([P, P, P, I64, I64, I64, P], I),
             "tq_matmul_groupsums": ([P, P, P, I64, I64, I64, P], I),
+            "tq_matmul_workspace_bytes": ([I64, I64, I64], I64),
+            "tq_matmul_ws": ([P, P, P, I64, I64, I64, P, I64, P], I),
+            "tq_matmul_groupsums_ws": ([P, P, P, I64, I64, I64, P, I64, P], I),
             "tq_strerror": ([I], ctypes.c_char_p),
             "tq_last_cuda_error": ([], I),
             "tq_device_status": ([], I),
@@ -167,6 +171,31 @@ def tq_matmul_groupsums(Wtq: torch.Tensor, Xq: torch.Tensor, S: torch.Tensor, ro
                         cols: int, ntok: int, stream=None):
     _call("tq_matmul_groupsums", Wtq.device, _ptr(Wtq), _ptr(Xq), _ptr(S), rows, cols, ntok,
           _stream(stream, Wtq.device))
+
+
+def tq_matmul_workspace_bytes(rows: int, cols: int, ntok: int) -> int:
+    n = _load().tq_matmul_workspace_bytes(rows, cols, ntok)
+    if n < 0:
+        raise TQError(TQ_ERR_SHAPE, "tq_matmul_workspace_bytes")
+    return int(n)
+
+
+def workspace_empty(rows: int, cols: int, ntok: int, device="cuda") -> torch.Tensor:
+    """uint8 buffer for tq_matmul_ws (at least one byte, so it has an address)."""
+    return torch.empty(max(1, tq_matmul_workspace_bytes(rows, cols, ntok)), dtype=torch.uint8,
+                       device=device)
+
+
+def tq_matmul_ws(Wtq: torch.Tensor, Xq: torch.Tensor, Y: torch.Tensor, rows: int, cols: int,
+                 ntok: int, workspace: torch.Tensor, stream=None):
+    _call("tq_matmul_ws", Wtq.device, _ptr(Wtq), _ptr(Xq), _ptr(Y), rows, cols, ntok,
+          _ptr(workspace), workspace.numel(), _stream(stream, Wtq.device))
+
+
+def tq_matmul_groupsums_ws(Wtq: torch.Tensor, Xq: torch.Tensor, S: torch.Tensor, rows: int,
+                           cols: int, ntok: int, workspace: torch.Tensor, stream=None):
+    _call("tq_matmul_groupsums_ws", Wtq.device, _ptr(Wtq), _ptr(Xq), _ptr(S), rows, cols, ntok,
+          _ptr(workspace), workspace.numel(), _stream(stream, Wtq.device))
 
 
 def tq_strerror(code: int) -> str:

@@ -70,8 +70,14 @@ cudaError_t device_status_ptr(int** out) {
 
 int64_t q8K_bytes(int64_t ntok, int64_t cols) { return ntok * (cols / kQK) * kQ8KBytes; }
 
+int64_t workspace_bytes(int64_t rows, int64_t cols, int64_t ntok) {
+  if (rows <= 0 || cols <= 0 || ntok <= gemv_max_tokens()) return 0;
+  return tc_workspace_bytes(cols, ntok);
+}
+
 int matmul_impl(const void* Wtq, const void* Xq, float* Y, int32_t* S, int64_t rows,
-                int64_t cols, int64_t ntok, void* stream) {
+                int64_t cols, int64_t ntok, void* ws, int64_t ws_bytes, bool use_ws,
+                void* stream) {
   if (rows < 0 || cols < 0 || ntok < 0 || cols % kQK != 0) return TQ_ERR_SHAPE;
   if (rows == 0 || ntok == 0) return TQ_OK;
   void* out = Y ? (void*)Y : (void*)S;
@@ -92,6 +98,15 @@ int matmul_impl(const void* Wtq, const void* Xq, float* Y, int32_t* S, int64_t r
   if (overlap(out, out_bytes, Wtq, tq_repacked_bytes(rows, cols)) ||
       overlap(out, out_bytes, Xq, q8K_bytes(ntok, cols)))
     return TQ_ERR_ALIAS;
+  const int64_t need = use_ws ? workspace_bytes(rows, cols, ntok) : 0;
+  if (need > 0) {
+    if (!ws) return TQ_ERR_NULL;
+    if (!aligned16(ws)) return TQ_ERR_ALIGN;
+    if (ws_bytes < need) return TQ_ERR_WORKSPACE;
+    if (overlap(ws, need, out, out_bytes) || overlap(ws, need, Wtq, tq_repacked_bytes(rows, cols)) ||
+        overlap(ws, need, Xq, q8K_bytes(ntok, cols)))
+      return TQ_ERR_ALIAS;
+  }
 
   const uint8_t* W = static_cast<const uint8_t*>(Wtq);
   const uint8_t* X = static_cast<const uint8_t*>(Xq);
@@ -106,7 +121,10 @@ int matmul_impl(const void* Wtq, const void* Xq, float* Y, int32_t* S, int64_t r
     if (e != cudaErrorNotSupported) return fail_cuda(e);
     // activations too large for the GEMV's shared memory: tensor-core path
   }
-  e = launch_gemm_tc(W, X, Y, S, rows, cols, ntok, status, s);
+  if (need > 0)
+    e = launch_gemm_tc_ws(W, X, Y, S, rows, cols, ntok, static_cast<uint8_t*>(ws), status, s);
+  else
+    e = launch_gemm_tc(W, X, Y, S, rows, cols, ntok, status, s);
   return e == cudaSuccess ? TQ_OK : fail_cuda(e);
 }
 
@@ -182,12 +200,30 @@ int tq_unrepack(const void* Wtq, void* Wpq2, int64_t rows, int64_t cols, void* s
 
 int tq_matmul(const void* Wtq, const void* Xq, float* Y, int64_t rows, int64_t cols,
               int64_t ntok, void* stream) {
-  return matmul_impl(Wtq, Xq, Y, nullptr, rows, cols, ntok, stream);
+  return matmul_impl(Wtq, Xq, Y, nullptr, rows, cols, ntok, nullptr, 0, false, stream);
 }
 
 int tq_matmul_groupsums(const void* Wtq, const void* Xq, int32_t* S, int64_t rows,
                         int64_t cols, int64_t ntok, void* stream) {
-  return matmul_impl(Wtq, Xq, nullptr, S, rows, cols, ntok, stream);
+  return matmul_impl(Wtq, Xq, nullptr, S, rows, cols, ntok, nullptr, 0, false, stream);
+}
+
+int64_t tq_matmul_workspace_bytes(int64_t rows, int64_t cols, int64_t ntok) {
+  if (rows < 0 || cols < 0 || ntok < 0 || cols % kQK != 0) return -1;
+  return workspace_bytes(rows, cols, ntok);
+}
+
+int tq_matmul_ws(const void* Wtq, const void* Xq, float* Y, int64_t rows, int64_t cols,
+                 int64_t ntok, void* workspace, int64_t workspace_bytes, void* stream) {
+  return matmul_impl(Wtq, Xq, Y, nullptr, rows, cols, ntok, workspace, workspace_bytes, true,
+                     stream);
+}
+
+int tq_matmul_groupsums_ws(const void* Wtq, const void* Xq, int32_t* S, int64_t rows,
+                           int64_t cols, int64_t ntok, void* workspace, int64_t workspace_bytes,
+                           void* stream) {
+  return matmul_impl(Wtq, Xq, nullptr, S, rows, cols, ntok, workspace, workspace_bytes, true,
+                     stream);
 }
 
 const char* tq_strerror(int code) {
@@ -199,6 +235,7 @@ const char* tq_strerror(int code) {
     case TQ_ERR_CUDA: return "CUDA error (see tq_last_cuda_error)";
     case TQ_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
     case TQ_ERR_ALIAS: return "output buffer overlaps an input";
+    case TQ_ERR_WORKSPACE: return "workspace smaller than tq_matmul_workspace_bytes";
     default: return "unknown error";
   }
 }

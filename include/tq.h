@@ -46,6 +46,7 @@ extern "C" {
 #define TQ_ERR_CUDA     -4  /* a CUDA launch or runtime call failed */
 #define TQ_ERR_TIMEOUT  -5  /* a kernel gave up a bounded wait (tq_device_status) */
 #define TQ_ERR_ALIAS    -6  /* an output buffer overlaps an input buffer */
+#define TQ_ERR_WORKSPACE -7 /* workspace smaller than tq_matmul_workspace_bytes */
 
 #define TQ_QK_K 256          /* activations per q8_K block */
 #define TQ_GROUP 128         /* weights per pq2_0 scale */
@@ -158,6 +159,39 @@ int tq_matmul(const void *Wtq, const void *Xq, float *Y, int64_t rows, int64_t c
  */
 int tq_matmul_groupsums(const void *Wtq, const void *Xq, int32_t *S, int64_t rows,
                         int64_t cols, int64_t ntok, void *stream);
+
+/*
+ * tq_matmul_workspace_bytes -- scratch needed by tq_matmul_ws for this shape:
+ * 0 when ntok <= 8 (the GEMV needs none); otherwise
+ * ceil(ntok/64) * (cols/128) * 16384 + ceil(ntok/64) * (cols/256) * 256 bytes.
+ * -1 for a bad shape.
+ */
+int64_t tq_matmul_workspace_bytes(int64_t rows, int64_t cols, int64_t ntok);
+
+/*
+ * tq_matmul_ws -- tq_matmul with a caller-provided workspace, the faster form
+ * for ntok >= 9: a pre-pass converts the q8_K activations once into the
+ * tensor cores' f16 operand layout in the workspace (instead of every
+ * 128-row tile of the weights converting them again), then the tensor-core
+ * kernel reads them with one bulk copy per 128-weight group. Same results
+ * and tolerance as tq_matmul; for ntok <= 8 it is tq_matmul.
+ *   workspace  device buffer of at least tq_matmul_workspace_bytes(rows, cols,
+ *              ntok) bytes, 16-byte aligned, owned by the caller; its contents
+ *              are overwritten and meaningless after the call; it must not
+ *              overlap Wtq, Xq or Y. Calls that share a workspace must be
+ *              ordered (the same stream, or synchronized streams).
+ * Errors: as tq_matmul; TQ_ERR_NULL if the workspace is needed and NULL;
+ * TQ_ERR_WORKSPACE if it is smaller than needed; TQ_ERR_ALIGN if it is
+ * misaligned; TQ_ERR_ALIAS if it overlaps another buffer.
+ */
+int tq_matmul_ws(const void *Wtq, const void *Xq, float *Y, int64_t rows, int64_t cols,
+                 int64_t ntok, void *workspace, int64_t workspace_bytes, void *stream);
+
+/* tq_matmul_groupsums_ws -- tq_matmul_groupsums through the kernels of
+ * tq_matmul_ws (parity/debug): S[t][r][g] = isum[t][r][g]. */
+int tq_matmul_groupsums_ws(const void *Wtq, const void *Xq, int32_t *S, int64_t rows,
+                           int64_t cols, int64_t ntok, void *workspace,
+                           int64_t workspace_bytes, void *stream);
 
 /* Human-readable name of a TQ_* code. */
 const char *tq_strerror(int code);

@@ -64,3 +64,21 @@ def assert_close(y_gpu, y_ref, abs_sum, rel=1e-5):
     assert bad.size == 0, (f"{len(bad)} outputs out of tolerance, first at {tuple(bad[0])}: "
                            f"gpu {y_gpu[tuple(bad[0])]} ref {y_ref[tuple(bad[0])]} "
                            f"bound {bound[tuple(bad[0])]}")
+
+
+def gpu_matmul_ws(Wtq, Xq, rows, cols, ntok) -> np.ndarray:
+    import bit_matvec_gb300 as tq
+    Y = torch.full((ntok, rows), float("nan"), dtype=torch.float32, device=DEV)
+    ws = tq.workspace_empty(rows, cols, ntok, DEV)
+    ws.fill_(0xAB)   # stale contents must not matter
+    tq.tq_matmul_ws(Wtq, Xq, Y, rows, cols, ntok, ws)
+    return Y.cpu().numpy()
+
+
+def gpu_groupsums_ws(Wtq, Xq, rows, cols, ntok) -> np.ndarray:
+    import bit_matvec_gb300 as tq
+    S = torch.full((ntok, rows, cols // 128), -(2 ** 31), dtype=torch.int32, device=DEV)
+    ws = tq.workspace_empty(rows, cols, ntok, DEV)
+    ws.fill_(0xCD)
+    tq.tq_matmul_groupsums_ws(Wtq, Xq, S, rows, cols, ntok, ws)
+    return S.cpu().numpy()

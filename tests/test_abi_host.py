@@ -23,7 +23,8 @@ def test_exports_every_header_function(lib):
     import bit_matvec_gb300 as tq
     names = tq.header_functions()
     for required in ("tq_quantize_q8K", "tq_repacked_bytes", "tq_repack", "tq_unrepack",
-                     "tq_matmul", "tq_matmul_groupsums", "tq_strerror"):
+                     "tq_matmul", "tq_matmul_groupsums", "tq_strerror", "tq_matmul_ws",
+                     "tq_matmul_workspace_bytes", "tq_matmul_groupsums_ws"):
         assert required in names
     for n in names:
         assert hasattr(lib, n), n
@@ -34,11 +35,11 @@ def test_version_and_strerror(lib):
     assert tq.tq_version().count(".") == 2
     seen = set()
     for code in (tq.TQ_OK, tq.TQ_ERR_SHAPE, tq.TQ_ERR_NULL, tq.TQ_ERR_ALIGN, tq.TQ_ERR_CUDA,
-                 tq.TQ_ERR_TIMEOUT, tq.TQ_ERR_ALIAS):
+                 tq.TQ_ERR_TIMEOUT, tq.TQ_ERR_ALIAS, tq.TQ_ERR_WORKSPACE):
         s = tq.tq_strerror(code)
         assert s and s != "unknown error"
         seen.add(s)
-    assert len(seen) == 7
+    assert len(seen) == 8
     assert tq.tq_strerror(12345) == "unknown error"
 
 
@@ -131,3 +132,30 @@ def test_binding_rejects_cpu_tensors(lib):
     x = torch.zeros(256)
     with pytest.raises(ValueError):
         tq.tq_quantize_q8K(x, torch.zeros(292, dtype=torch.uint8), 1, 256)
+
+
+def test_workspace_bytes(lib):
+    # none for the GEMV route; B tiles + block scales per 64-token tile otherwise
+    assert lib.tq_matmul_workspace_bytes(32768, 8192, 1) == 0
+    assert lib.tq_matmul_workspace_bytes(17408, 5120, 8) == 0
+    assert lib.tq_matmul_workspace_bytes(17408, 5120, 64) == 40 * 16384 + 20 * 256
+    assert lib.tq_matmul_workspace_bytes(100, 512, 65) == 2 * (4 * 16384 + 2 * 256)
+    assert lib.tq_matmul_workspace_bytes(0, 512, 65) == 0
+    assert lib.tq_matmul_workspace_bytes(32, 300, 9) == -1
+    assert lib.tq_matmul_workspace_bytes(-1, 512, 9) == -1
+
+
+def test_workspace_errors(lib):
+    import bit_matvec_gb300 as tq
+    D = 0x7F3000000000
+    need = lib.tq_matmul_workspace_bytes(64, 512, 16)
+    ws = lib.tq_matmul_ws
+    assert ws(P(A), P(B), P(C), 64, 512, 16, None, need, None) == tq.TQ_ERR_NULL
+    assert ws(P(A), P(B), P(C), 64, 512, 16, P(D + 8), need, None) == tq.TQ_ERR_ALIGN
+    assert ws(P(A), P(B), P(C), 64, 512, 16, P(D), need - 16, None) == tq.TQ_ERR_WORKSPACE
+    assert ws(P(A), P(B), P(C), 64, 512, 16, P(C + 64), need, None) == tq.TQ_ERR_ALIAS
+    assert ws(P(A), P(B), P(C), 64, 512, 16, P(B), need, None) == tq.TQ_ERR_ALIAS
+    assert ws(P(A), P(B), P(C), 64, 300, 16, P(D), need, None) == tq.TQ_ERR_SHAPE
+    assert ws(None, None, None, 64, 512, 0, None, 0, None) == tq.TQ_OK
+    gs = lib.tq_matmul_groupsums_ws
+    assert gs(P(A), P(B), P(C), 64, 512, 16, P(D), need - 1, None) == tq.TQ_ERR_WORKSPACE

@@ -12,8 +12,8 @@ import torch
 import oracle
 import synth
 from conftest import read_golden
-from gpu_util import (DEV, assert_close, ensure_built, gpu_groupsums, gpu_matmul, gpu_quantize,
-                      gpu_repack, q8K_from_dev, to_dev)
+from gpu_util import (DEV, assert_close, ensure_built, gpu_groupsums, gpu_groupsums_ws, gpu_matmul,
+                      gpu_matmul_ws, gpu_quantize, gpu_repack, q8K_from_dev, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -92,16 +92,17 @@ GEMV_TOKENS = [1, 2, 3, 4, 5, 7, 8]          # one weight pass for all tokens
 TC_TOKENS = [9, 15, 16, 17, 63, 64, 65, 130]  # tensor cores, token tile zero-padded
 
 
-def _check_product(rows, cols, ntok):
+def _check_product(rows, cols, ntok, ws=False):
     wpq = _weights(rows, cols, 20 + rows % 7)
     x = _acts(ntok, cols, 30 + ntok)
     Wtq = gpu_repack(wpq, rows, cols)
     Xq = gpu_quantize(x)
     xq = oracle.quantize_q8K(x)
-    S = gpu_groupsums(Wtq, Xq, rows, cols, ntok)
+    gs, mm = (gpu_groupsums_ws, gpu_matmul_ws) if ws else (gpu_groupsums, gpu_matmul)
+    S = gs(Wtq, Xq, rows, cols, ntok)
     assert np.array_equal(S, oracle.groupsums(wpq, xq, rows, cols))
     y_ref, abs_sum = oracle.matmul(wpq, xq, rows, cols)
-    assert_close(gpu_matmul(Wtq, Xq, rows, cols, ntok), y_ref, abs_sum)
+    assert_close(mm(Wtq, Xq, rows, cols, ntok), y_ref, abs_sum)
 
 
 @pytest.mark.parametrize("rows,cols", SHAPES)
@@ -116,6 +117,13 @@ def test_tc_groupsums_exact_matmul_close(rows, cols, ntok):
     _check_product(rows, cols, ntok)
 
 
+@pytest.mark.parametrize("rows,cols", SHAPES)
+@pytest.mark.parametrize("ntok", TC_TOKENS)
+def test_tc_ws_groupsums_exact_matmul_close(rows, cols, ntok):
+    """The workspace form: activations packed once by a pre-pass."""
+    _check_product(rows, cols, ntok, ws=True)
+
+
 @pytest.mark.parametrize("ntok", [1, 4, 8, 9, 16, 64, 65], ids=lambda t: f"{'tc' if t > 8 else 'gemv'}{t}")
 def test_exact_integer_mode(ntok):
     """d_w = 1 and d_x = 1 (integer activations with absmax 127 in every block):
@@ -128,9 +136,10 @@ def test_exact_integer_mode(ntok):
     x[:, ::256] = 127.0
     Wtq = gpu_repack(wpq, rows, cols)
     Xq = gpu_quantize(x)
-    y = gpu_matmul(Wtq, Xq, rows, cols, ntok)
-    assert np.array_equal(y.astype(np.int64), x.astype(np.int64) @ w.T)
-    assert np.array_equal(y, (x.astype(np.int64) @ w.T).astype(np.float32))
+    for mm in (gpu_matmul, gpu_matmul_ws):
+        y = mm(Wtq, Xq, rows, cols, ntok)
+        assert np.array_equal(y.astype(np.int64), x.astype(np.int64) @ w.T)
+        assert np.array_equal(y, (x.astype(np.int64) @ w.T).astype(np.float32))
 
 
 @pytest.mark.parametrize("ntok", [1, 8, 64], ids=lambda t: f"{'tc' if t > 8 else 'gemv'}{t}")
@@ -195,12 +204,16 @@ def test_workload_sampled_rows(name):
     _q8K_equal(q8K_from_dev(Xq, ntok, cols), xq)
     y = gpu_matmul(Wtq, Xq, rows, cols, ntok)
     S = gpu_groupsums(Wtq, Xq, rows, cols, ntok)
+    y_ws = gpu_matmul_ws(Wtq, Xq, rows, cols, ntok)
+    S_ws = gpu_groupsums_ws(Wtq, Xq, rows, cols, ntok)
+    assert np.array_equal(S_ws, S)
     rng = np.random.default_rng(rows)
     sample = np.unique(np.concatenate([[0, 1, 31, 32, rows - 1],
                                        rng.integers(0, rows, 60)]))
     wsub = oracle.pq2_0_rows(wpq, cols, sample)
     y_ref, abs_sum = oracle.matmul(wsub, xq, len(sample), cols)
     assert_close(y[:, sample], y_ref, abs_sum)
+    assert_close(y_ws[:, sample], y_ref, abs_sum)
     assert np.array_equal(S[:, sample, :], oracle.groupsums(wsub, xq, len(sample), cols))
     # the repacked tiles of the sampled rows hold the same bits as pq2_0
     if rows * cols <= 32768 * 8192:
