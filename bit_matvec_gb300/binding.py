@@ -35,6 +35,7 @@ PQ2_0_BYTES = 34
 Q8K_BYTES = 292
 TILE_ROWS = 32
 TILE_BYTES = 1088
+STATIC_WS_BYTES = 8 << 20   # TQ_STATIC_WS_BYTES: fixed workspace of tq_matmul_static_ws
 
 _lock = threading.Lock()
 _lib = None
@@ -78,6 +79,7 @@ def _load():
             "tq_matmul_workspace_bytes": ([I64, I64, I64], I64),
             "tq_matmul_ws": ([P, P, P, I64, I64, I64, P, I64, P], I),
             "tq_matmul_groupsums_ws": ([P, P, P, I64, I64, I64, P, I64, P], I),
+            "tq_matmul_static_ws": ([P, P, P, I64, I64, I64, P], I),
             "tq_strerror": ([I], ctypes.c_char_p),
             "tq_last_cuda_error": ([], I),
             "tq_device_status": ([], I),
@@ -196,6 +198,15 @@ def tq_matmul_groupsums_ws(Wtq: torch.Tensor, Xq: torch.Tensor, S: torch.Tensor,
                            cols: int, ntok: int, workspace: torch.Tensor, stream=None):
     _call("tq_matmul_groupsums_ws", Wtq.device, _ptr(Wtq), _ptr(Xq), _ptr(S), rows, cols, ntok,
           _ptr(workspace), workspace.numel(), _stream(stream, Wtq.device))
+
+
+def tq_matmul_static_ws(Wtq: torch.Tensor, Xq: torch.Tensor, Y: torch.Tensor, rows: int,
+                        cols: int, ntok: int, stream=None):
+    """tq_matmul_ws with the library's fixed STATIC_WS_BYTES device array as
+    its workspace, for callers that cannot allocate device memory. Calls share
+    that array: calls that overlap on the GPU race, so keep them ordered."""
+    _call("tq_matmul_static_ws", Wtq.device, _ptr(Wtq), _ptr(Xq), _ptr(Y), rows, cols, ntok,
+          _stream(stream, Wtq.device))
 
 
 def tq_strerror(code: int) -> str:

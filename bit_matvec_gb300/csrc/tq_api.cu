@@ -130,6 +130,8 @@ int matmul_impl(const void* Wtq, const void* Xq, float* Y, int32_t* S, int64_t r
 
 }  // namespace
 
+void record_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
+
 cudaError_t ensure_dynamic_smem(const void* kernel, int bytes) {
   if (bytes <= 48 * 1024) return cudaSuccess;
   int dev = 0;

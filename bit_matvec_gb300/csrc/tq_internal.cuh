@@ -197,5 +197,7 @@ cudaError_t launch_gemm_tc_ws(const uint8_t* Wtq, const uint8_t* Xq, float* Y, i
 // Opt a kernel in to `bytes` of dynamic shared memory on the current device
 // (cached per device and kernel).
 cudaError_t ensure_dynamic_smem(const void* kernel, int bytes);
+// Record e as this host thread's tq_last_cuda_error.
+void record_cuda_error(cudaError_t e);
 
 }  // namespace tq

@@ -54,6 +54,7 @@ extern "C" {
 #define TQ_Q8K_BYTES 292     /* bytes per q8_K block */
 #define TQ_TILE_ROWS 32      /* rows per tile of the repacked layout */
 #define TQ_TILE_BYTES 1088   /* bytes per tile: 32 rows x 128 weights */
+#define TQ_STATIC_WS_BYTES (8 << 20)  /* fixed workspace of tq_matmul_static_ws: 8 MiB */
 
 /*
  * q8_K block (ciot README: "256 int8 values, a float scale and 16 partial
@@ -192,6 +193,34 @@ int tq_matmul_ws(const void *Wtq, const void *Xq, float *Y, int64_t rows, int64_
 int tq_matmul_groupsums_ws(const void *Wtq, const void *Xq, int32_t *S, int64_t rows,
                            int64_t cols, int64_t ntok, void *workspace,
                            int64_t workspace_bytes, void *stream);
+
+/*
+ * tq_matmul_static_ws -- tq_matmul_ws without a caller workspace: the
+ * workspace is a fixed device array of TQ_STATIC_WS_BYTES inside this
+ * library, so the call allocates nothing. The paper has no counterpart to
+ * this entry point; it exists for callers that cannot allocate device memory
+ * where they run the matmul (a plugin that only receives input and output
+ * pointers from its host application, an engine that allows no allocation
+ * after start-up because cudaMalloc can synchronize the device, code whose
+ * caching allocator must not be bypassed).
+ *   Same arguments, results and errors as tq_matmul_ws, minus the workspace.
+ *   Limit: tq_matmul_workspace_bytes(rows, cols, ntok) <= TQ_STATIC_WS_BYTES,
+ *   else TQ_ERR_WORKSPACE before anything runs (for example cols = 5120
+ *   allows ntok <= 768; ntok <= 8 needs no workspace and has no limit).
+ *   Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current), which may also load the
+ *   library's code for the array onto that device; make that first call
+ *   before any stream capture. TQ_ERR_CUDA if the look-up fails.
+ *   Memory: the array occupies TQ_STATIC_WS_BYTES on every GPU where it has
+ *   been loaded, until the process exits.
+ *   Sharing: every call uses the same array, which keeps the last call's
+ *   contents (nothing in it needs to start at zero: the pre-pass rewrites all
+ *   of it that the matmul reads). Calls whose kernels overlap on the GPU
+ *   (different streams, different host threads) race on it and give wrong
+ *   results; order them on one stream or synchronize between them.
+ */
+int tq_matmul_static_ws(const void *Wtq, const void *Xq, float *Y, int64_t rows, int64_t cols,
+                        int64_t ntok, void *stream);
 
 /* Human-readable name of a TQ_* code. */
 const char *tq_strerror(int code);
