@@ -419,7 +419,7 @@ def profile_traffic(summary_name, files, launch_bytes_key="dram_bytes_per_launch
 
 
 GEMV_FILES = ("tq_gemv.cu", "tq_internal.cuh")
-TC_FILES = ("tq_gemm_tc.cu", "tq_internal.cuh")
+TC_FILES = ("tq_gemm_tc_ws.cu", "tq_tcgen05.cuh", "tq_internal.cuh")
 
 
 def measure(name, args, rank, world, device, peaks, peak_kind, steps):
@@ -447,10 +447,10 @@ def measure(name, args, rank, world, device, peaks, peak_kind, steps):
         flops = 2.0 * wl.macs()
         achieved = flops / (kern_ms * 1e-3) / 1e12
         peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-        traffic = profile_traffic(f"gemm_tc_{name}_ncu.txt", TC_FILES)
+        traffic = profile_traffic(f"gemm_tc_ws_{name}_ncu.txt", TC_FILES)
         res["roofline"] = {"bound": "tensor", "achieved": achieved, "peak": peak,
                            "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
-                           "kernel": "gemm_tc_kernel (tcgen05 kind::f16, exact)",
+                           "kernel": "act_pack + gemm_tc_ws_kernel (tcgen05 kind::f16, exact)",
                            "kernel_ms": kern_ms, "kernel_timing": kern_how,
                            "kernel_ms_serialised": serial_ms, "algorithmic_flops": flops,
                            "peak_source": f"{peak_kind} bf16 dense (f16 runs at the bf16 rate)"}

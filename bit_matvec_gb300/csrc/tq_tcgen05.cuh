@@ -40,6 +40,17 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem], kind::f16.
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                ::"r"(bar) : "memory");
@@ -75,28 +86,74 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
-__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
-__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
-
 // Codes of slot s (bits 2s..2s+1 of two bytes, placed in the low byte of each
 // 16-bit half) -> f16 pair of w = u - 1. OR-ing 0x6400 (1024.0) makes the half
-// 1024 + u * 4^s exactly; one FMA by 4^-s minus (1024 * 4^-s + 1) gives u - 1.
+// 1024 + u * 4^s exactly; one FMA by 4^-s plus -(1024 * 4^-s + 1) gives u - 1.
+// The two constants are written as f16x2 bit patterns so that no conversion
+// runs on the device.
+template <int s> struct WConst;
+template <> struct WConst<0> { static constexpr uint32_t m = 0x3C003C00u, b = 0xE401E401u; };  // 1, -1025
+template <> struct WConst<1> { static constexpr uint32_t m = 0x34003400u, b = 0xDC04DC04u; };  // 1/4, -257
+template <> struct WConst<2> { static constexpr uint32_t m = 0x2C002C00u, b = 0xD410D410u; };  // 1/16, -65
+template <> struct WConst<3> { static constexpr uint32_t m = 0x24002400u, b = 0xCC40CC40u; };  // 1/64, -17
+
 template <int s>
 __device__ __forceinline__ uint32_t codes_to_w(uint32_t x) {
   const uint32_t v = (x & (0x00030003u << (2 * s))) | 0x64006400u;
-  const float sc = 1.0f / (float)(1 << (2 * s));
-  const __half2 m = __float2half2_rn(sc);
-  const __half2 b = __float2half2_rn(-(1024.0f * sc + 1.0f));
-  return h2_bits(__hfma2(bits_h2(v), m, b));
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(WConst<s>::m), "r"(WConst<s>::b));
+  return r;
 }
 
 // int8 x4 -> two f16 pairs (exact): bias to u8, place under exponent 0x64
-// (1024 + byte), subtract 1152.
+// (1024 + byte), subtract 1152 (f16x2 bits 0x64806480).
 __device__ __forceinline__ void s8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
   const uint32_t u = w ^ 0x80808080u;
-  const __half2 off = __float2half2_rn(1152.0f);
-  lo = h2_bits(__hsub2(bits_h2(__byte_perm(u, 0x64646464u, 0x5150)), off));
-  hi = h2_bits(__hsub2(bits_h2(__byte_perm(u, 0x64646464u, 0x5352)), off));
+  const uint32_t a = __byte_perm(u, 0x64646464u, 0x5150);
+  const uint32_t b = __byte_perm(u, 0x64646464u, 0x5352);
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane -> registers,
+// without waiting: the caller issues tcgen05.wait::ld before reading r.
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+// Packed pairs of f32 (f32x2 arithmetic, one instruction per pair).
+__device__ __forceinline__ uint64_t f2_pack(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_packf(float lo, float hi) {
+  return f2_pack(__float_as_uint(lo), __float_as_uint(hi));
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+  uint32_t lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+  return make_float2(__uint_as_float(lo), __uint_as_float(hi));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 }  // namespace tc

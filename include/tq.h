@@ -164,7 +164,7 @@ int tq_matmul_groupsums(const void *Wtq, const void *Xq, int32_t *S, int64_t row
 /*
  * tq_matmul_workspace_bytes -- scratch needed by tq_matmul_ws for this shape:
  * 0 when ntok <= 8 (the GEMV needs none); otherwise
- * ceil(ntok/64) * (cols/128) * 16384 + ceil(ntok/64) * (cols/256) * 256 bytes.
+ * ceil(ntok/64) * (cols/128) * 18432 + ceil(ntok/64) * (cols/256) * 256 bytes.
  * -1 for a bad shape.
  */
 int64_t tq_matmul_workspace_bytes(int64_t rows, int64_t cols, int64_t ntok);
@@ -206,7 +206,7 @@ int tq_matmul_groupsums_ws(const void *Wtq, const void *Xq, int32_t *S, int64_t 
  *   Same arguments, results and errors as tq_matmul_ws, minus the workspace.
  *   Limit: tq_matmul_workspace_bytes(rows, cols, ntok) <= TQ_STATIC_WS_BYTES,
  *   else TQ_ERR_WORKSPACE before anything runs (for example cols = 5120
- *   allows ntok <= 768; ntok <= 8 needs no workspace and has no limit).
+ *   allows ntok <= 704; ntok <= 8 needs no workspace and has no limit).
  *   Set-up: the first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current), which may also load the
  *   library's code for the array onto that device; make that first call
