@@ -111,6 +111,14 @@ def test_gemv_groupsums_exact_matmul_close(rows, cols, ntok):
     _check_product(rows, cols, ntok)
 
 
+@pytest.mark.parametrize("rows,cols,ntok", [(64, 8192, 4), (64, 8192, 8), (96, 16384, 6)])
+def test_gemv_wide_rows(rows, cols, ntok):
+    """Long rows: from 4 tokens the tensor-core (mma.sync) variant runs while its
+    f16 activations fit in shared memory (8 x 8192 do not: the dp4a loop takes
+    over); 16384 columns at 6 tokens exercise the largest staged activations."""
+    _check_product(rows, cols, ntok)
+
+
 @pytest.mark.parametrize("rows,cols", SHAPES)
 @pytest.mark.parametrize("ntok", TC_TOKENS)
 def test_tc_groupsums_exact_matmul_close(rows, cols, ntok):
