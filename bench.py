@@ -5,7 +5,8 @@ quantize the activations to q8_K, then the ternary matmul (the load-time
 repack runs once, before timing, and is reported separately). The headline
 workload is the decode GEMV (32768 x 8192 weights, 1 token), measured in
 Gweights/s; the 4-token and 64-token 17408 x 5120 tiles are measured in the
-same run in GMAC/s.
+same run in GMAC/s, and the 64-block decode-step replay (23.82 G weights,
+6.33 GB per step) at 1 and 512 tokens.
 
 Timing: inputs resident in HBM; W >= 3 warm-up steps; K timed steps replayed
 from a CUDA graph on one stream, bracketed by a barrier and a device
@@ -62,6 +63,8 @@ def parse_args():
     p.add_argument("--no-extra", action="store_true", help="skip the 4- and 64-token tiles")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    p.add_argument("--no-replay", action="store_true",
+                   help="skip the 64-block decode-step replay (ntok 1 and 512)")
     p.add_argument("--tensor-rates", action="store_true",
                    help="only measure library int8 / bf16 / f16 GEMM rates (operand-type choice)")
     return p.parse_args()
@@ -211,6 +214,102 @@ class Workload:
 
     def macs(self):
         return self.rows * self.cols * self.ntok
+
+
+class ReplayWorkload:
+    """The decode-step replay: 64 blocks x {Wqkv 15360x5120, Wo 5120x5120,
+    W_gate and W_up 17408x5120, W_down 5120x17408} (23.82 G weights, 6.33 GB in
+    64 x 5 distinct allocations, so every step streams them from HBM; each
+    block's allocations hold copies of one synthetic block). One step = for
+    every block and matrix: quantize that matrix's activations, matmul. The
+    activations of a matrix are one seeded batch shared by the 64 blocks."""
+
+    def __init__(self, ntok, device, blocks=synth.REPLAY_BLOCKS):
+        import torch
+        import bit_matvec_gb300 as tq
+        self.ntok, self.blocks, self.device = ntok, blocks, device
+        self.mats = []
+        need = 0
+        for m in range(len(synth.REPLAY_BLOCK)):
+            wpq, x, rows, cols = synth.replay_matrix(m, ntok)
+            W = torch.from_numpy(wpq).to(device)
+            wtq = tq.repacked_empty(rows, cols, device)
+            tq.tq_repack(W, wtq, rows, cols)
+            torch.cuda.synchronize(device)
+            del W
+            self.mats.append(dict(
+                rows=rows, cols=cols, W=[wtq] + [wtq.clone() for _ in range(blocks - 1)],
+                X=torch.from_numpy(x).to(device), Xq=tq.q8K_empty(ntok, cols, device),
+                Y=torch.empty((ntok, rows), dtype=torch.float32, device=device)))
+            need = max(need, tq.tq_matmul_workspace_bytes(rows, cols, ntok))
+        self.ws = torch.empty(max(1, need), dtype=torch.uint8, device=device)
+
+    def step(self, stream=None):
+        import bit_matvec_gb300 as tq
+        for b in range(self.blocks):
+            for m in self.mats:
+                tq.tq_quantize_q8K(m["X"], m["Xq"], self.ntok, m["cols"], stream)
+                tq.tq_matmul_ws(m["W"][b], m["Xq"], m["Y"], m["rows"], m["cols"], self.ntok,
+                                self.ws, stream)
+
+    def launches(self):
+        return 2 * self.blocks * len(self.mats)
+
+    def weights(self):
+        return self.blocks * sum(m["rows"] * m["cols"] for m in self.mats)
+
+    def weight_bytes(self):
+        return self.blocks * sum(m["W"][0].numel() for m in self.mats)
+
+    def algorithmic_bytes(self):
+        return self.blocks * sum(algorithmic_bytes(m["rows"], m["cols"], self.ntok)
+                                 for m in self.mats)
+
+
+def measure_replay(ntok, steps, warmup, world, device, peaks, peak_kind):
+    """Device time of whole replay steps from one CUDA graph per step."""
+    import torch
+    wl = ReplayWorkload(ntok, device)
+    stream = torch.cuda.Stream(device=device)
+    stream.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(stream):
+        wl.step(stream)                                 # un-captured warm-up (kernel attributes)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            wl.step(stream)
+        for _ in range(max(warmup, 3)):
+            g.replay()
+        stream.synchronize()
+        barrier(world)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(steps):
+            g.replay()
+        end.record(stream)
+        stream.synchronize()
+        ms = max_over_ranks(start.elapsed_time(end) / steps, world, device)
+    res = {"workload": f"decode-step replay, {wl.blocks} blocks x 5 matrices, ntok={ntok}",
+           "ntok": ntok, "ms_per_step": ms, "steps": steps, "launches_per_step": wl.launches(),
+           "weights_per_step": wl.weights(), "weight_bytes_per_step": wl.weight_bytes(),
+           "timing": "CUDA graph of one whole step, CUDA events"}
+    if ntok == 1:
+        res["gweights_per_s"] = world * wl.weights() / (ms * 1e-3) / 1e9
+        achieved = wl.algorithmic_bytes() / (ms * 1e-3) / 1e9
+        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        res["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                           "frac": achieved / peak, "peak_source": peak_kind,
+                           "note": "whole step (quantize + matmul launches) over algorithmic bytes"}
+    else:
+        res["gmac_per_s"] = world * wl.weights() * ntok / (ms * 1e-3) / 1e9
+        achieved = 2.0 * wl.weights() * ntok / (ms * 1e-3) / 1e12
+        peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+        res["roofline"] = {"bound": "tensor", "achieved": achieved, "peak": peak,
+                           "unit": "TFLOP/s", "frac": achieved / peak,
+                           "peak_source": f"{peak_kind} bf16 dense sustained (a long step)"}
+    del wl
+    torch.cuda.empty_cache()
+    return res
 
 
 def time_graph(wl: Workload, steps: int, warmup: int, world: int):
@@ -524,6 +623,10 @@ def main():
                 _, r = measure(name, args, rank, world, device, peaks, peak_kind,
                                max(64, args.steps // 10))
                 extra[name] = r
+    if not args.no_replay:
+        for ntok, rsteps in ((1, 30), (512, 3)):
+            extra[f"replay_ntok{ntok}"] = measure_replay(ntok, rsteps, args.warmup // 100 + 1, world,
+                                                         device, peaks, peak_kind)
 
     e2e = None
     if not args.no_e2e:

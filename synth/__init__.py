@@ -58,6 +58,9 @@ REPLAY_BLOCK = (
     ("w_down", 5120, 17408),
 )
 REPLAY_BLOCKS = 64
+# Stream seeds of replay matrix m start at SEED_BASE + REPLAY_SEED_OFFSET + 4 m,
+# clear of the named workloads' seeds.
+REPLAY_SEED_OFFSET = 0x100
 
 
 def seeds(config_index: int) -> dict:
@@ -175,6 +178,25 @@ def pq2_0_weights(rows: int, cols: int, config_index: int, row0: int = 0) -> np.
     codes = ternary_codes(rows, cols, s["weights"], row0)
     sc = group_scales(rows, cols, s["scales"], row0)
     return pack_pq2_0(codes, sc)
+
+
+def replay_seeds(m: int) -> dict:
+    """Stream seeds of matrix m of the decode-step replay block."""
+    base = SEED_BASE + REPLAY_SEED_OFFSET + 4 * m
+    return dict(weights=base, scales=base + 1, acts=base + 2, outliers=base + 3)
+
+
+def replay_matrix(m: int, ntok: int, row0: int = 0, rows: int | None = None):
+    """(pq2_0 bytes of rows row0.., f32 activations[ntok][cols], rows, cols) of
+    matrix m of one replay block. Every block of the replay holds a copy of
+    these weights in its own allocation."""
+    _, nrows, cols = REPLAY_BLOCK[m]
+    rows = nrows - row0 if rows is None else rows
+    s = replay_seeds(m)
+    codes = ternary_codes(rows, cols, s["weights"], row0)
+    sc = group_scales(rows, cols, s["scales"], row0)
+    x = activations(ntok, cols, s["acts"])
+    return pack_pq2_0(codes, sc), x, nrows, cols
 
 
 def workload(name: str):

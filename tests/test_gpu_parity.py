@@ -228,3 +228,20 @@ def test_workload_sampled_rows(name):
         wtq = Wtq.cpu().numpy()
         assert np.array_equal(wtq[:oracle.repacked_bytes(64, cols)],
                               oracle.repack(wpq[:64 * cols // 128 * 34], 64, cols))
+
+
+@pytest.mark.parametrize("m,ntok", [(0, 1), (1, 1), (2, 1), (3, 1), (4, 1), (0, 512), (4, 512)],
+                         ids=lambda v: str(v))
+def test_replay_matrices_sampled_rows(m, ntok):
+    """The decode-step replay's matrices (including the 17408-column W_down) at
+    1 token (GEMV) and 512 tokens (tensor cores, workspace form), full size, in
+    the benchmark's launch configuration; sampled rows against the oracle."""
+    wpq, x, rows, cols = synth.replay_matrix(m, ntok)
+    Wtq, Xq = gpu_repack(wpq, rows, cols), gpu_quantize(x)
+    xq = oracle.quantize_q8K(x)
+    y_ws = gpu_matmul_ws(Wtq, Xq, rows, cols, ntok)
+    rng = np.random.default_rng(rows + m)
+    sample = np.unique(np.concatenate([[0, 127, 128, rows - 1], rng.integers(0, rows, 12)]))
+    wsub = oracle.pq2_0_rows(wpq, cols, sample)
+    y_ref, abs_sum = oracle.matmul(wsub, xq, len(sample), cols)
+    assert_close(y_ws[:, sample], y_ref, abs_sum)
