@@ -8,12 +8,12 @@
 //     one contiguous byte range, streamed through a ring of shared-memory
 //     stages with 1-D TMA bulk copies (cp.async.bulk, 16 or more tiles of
 //     1088 bytes per copy), each completed on a "full" mbarrier; the last of
-//     the 16 warps to release a slot refills it, so no warp waits for another;
-//   - the 16 warps each take tiles of a stage: the same 32 rows, different
-//     128-weight groups. Lane l is row l, so no lane ever needs a
-//     cross-lane reduction of dot products; the 16 partial sums of a row are
-//     added in shared memory once per tile column, in a fixed order
-//     (deterministic output);
+//     the warps to release a slot refills it, so no warp waits for another;
+//   - the warps (8 for one token, 16 for more) each take tiles of a stage:
+//     the same 32 rows, different 128-weight groups. Lane l is row l, so no
+//     lane ever needs a cross-lane reduction of dot products; the warps'
+//     partial sums of a row are added in shared memory once per tile column,
+//     in a fixed order (deterministic output);
 //   - the activations of all tokens sit in shared memory; every lane of a warp
 //     reads the same 16 bytes at once (a broadcast);
 //   - unpacking a 32-bit weight word (16 weights) is one AND per dp4a operand:
@@ -37,10 +37,13 @@ namespace {
 // warp takes from a stage, the deepest ring, the most CTAs on one SM, and
 // whether the grid should split the tile columns evenly.
 #ifndef TQ_GEMV_WARPS_T1
-#define TQ_GEMV_WARPS_T1 16
+#define TQ_GEMV_WARPS_T1 8
 #endif
 #ifndef TQ_GEMV_WARPS
 #define TQ_GEMV_WARPS 16
+#endif
+#ifndef TQ_GEMV_TILES_PER_WARP_T1
+#define TQ_GEMV_TILES_PER_WARP_T1 4
 #endif
 #ifndef TQ_GEMV_TILES_PER_WARP
 #define TQ_GEMV_TILES_PER_WARP 2
@@ -56,7 +59,6 @@ namespace {
 #endif
 
 constexpr int kMaxTok = 8;
-constexpr int kTilesPerWarp = TQ_GEMV_TILES_PER_WARP;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // Per token count: warps (each owns tiles of every stage), stage size, and
@@ -65,6 +67,7 @@ template <int T>
 struct Cfg {
   static constexpr int kWarps = T == 1 ? TQ_GEMV_WARPS_T1 : TQ_GEMV_WARPS;
   static constexpr int kThreads = kWarps * 32;
+  static constexpr int kTilesPerWarp = T == 1 ? TQ_GEMV_TILES_PER_WARP_T1 : TQ_GEMV_TILES_PER_WARP;
   static constexpr int kStageTiles = kWarps * kTilesPerWarp;
   static constexpr int kStageBytes = kStageTiles * kTileBytes;
   static constexpr int kMinCtas = (T == 1 && kThreads <= 512) ? 2 : 1;
@@ -204,21 +207,27 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
   pdl_wait_primary();   // the q8_K activations are written by the previous kernel
   if (threadIdx.x == 0 && !a.early_weights) issue_first();
 
-  // Stage q8_K activations: qs as a dense int8 [T][cols] array, the sum of each
-  // 128-value half-block (8 partial sums), and the block scales.
-  for (int tb = warp; tb < T * a.nblk; tb += kConsumers) {
-    const int t = tb / a.nblk, b = tb - t * a.nblk;
-    const uint8_t* blk = a.Xq + (int64_t)tb * kQ8KBytes;
-    const uint32_t* qs = reinterpret_cast<const uint32_t*>(blk + kQ8KQsOffset);
-    uint32_t* dst = reinterpret_cast<uint32_t*>(sq + t * cols + b * kQK);
-    dst[lane] = __ldg(qs + lane);
-    dst[lane + 32] = __ldg(qs + lane + 32);
-    int s = lane < 16 ? (int)__ldg(reinterpret_cast<const int16_t*>(blk + kQ8KBsumsOffset) + lane) : 0;
-    s += __shfl_xor_sync(0xffffffffu, s, 1);
-    s += __shfl_xor_sync(0xffffffffu, s, 2);
-    s += __shfl_xor_sync(0xffffffffu, s, 4);
-    if (lane == 0 || lane == 8) sgsum[t * a.ngroups + 2 * b + (lane >> 3)] = s;
-    if (lane == 0) sdx[tb] = __ldg(reinterpret_cast<const float*>(blk));
+  // Stage q8_K activations, every thread issuing independent loads: qs as a
+  // dense int8 [T][cols] array (block tb = t * nblk + b lands at tb * 256), the
+  // sum of each 128-value half-block (8 partial sums), and the block scales.
+  {
+    const int nw = T * a.nblk * (kQK / 4);
+#pragma unroll 4
+    for (int w = threadIdx.x; w < nw; w += Cfg<T>::kThreads) {
+      const int tb = w >> 6, k = w & 63;
+      reinterpret_cast<uint32_t*>(sq + tb * kQK)[k] = __ldg(
+          reinterpret_cast<const uint32_t*>(a.Xq + (int64_t)tb * kQ8KBytes + kQ8KQsOffset) + k);
+    }
+    for (int h = threadIdx.x; h < T * a.nblk * 2; h += Cfg<T>::kThreads) {
+      const int tb = h >> 1, half = h & 1;
+      const uint8_t* blk = a.Xq + (int64_t)tb * kQ8KBytes;
+      const int16_t* bs = reinterpret_cast<const int16_t*>(blk + kQ8KBsumsOffset) + half * 8;
+      int sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sum += __ldg(bs + i);
+      sgsum[h] = sum;   // = sgsum[t * ngroups + 2 * b + half]
+      if (half == 0) sdx[tb] = __ldg(reinterpret_cast<const float*>(blk));
+    }
   }
   __syncthreads();
 
@@ -236,9 +245,9 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
       if (!failed && !mbarrier_wait_bounded(smem_u32(full + slot), phase, kWaitLimitNs))
         failed = true;
       // this warp's tiles of the stage: warp, warp + 16, ... (spread for short stages)
-      GroupCodes c[kTilesPerWarp];
+      GroupCodes c[Cfg<T>::kTilesPerWarp];
 #pragma unroll
-      for (int u = 0; u < kTilesPerWarp; ++u) {
+      for (int u = 0; u < Cfg<T>::kTilesPerWarp; ++u) {
         const int tl = warp + u * kConsumers;
         if (!failed && tl < nt) {
           const uint8_t* tile = ring + (size_t)slot * kStageBytes + tl * kTileBytes;
@@ -249,7 +258,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
       }
       __syncwarp();   // the whole warp has read its tile: release the slot
       if (lane == 0) {
-        // the last of the 16 warps to release a slot refills it (nobody waits)
+        // the last of the warps to release a slot refills it (nobody waits)
         __threadfence_block();
         if (atomicAdd(released + slot, 1) == kConsumers - 1) {
           released[slot] = 0;
@@ -262,15 +271,15 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
         }
       }
 #pragma unroll
-      for (int u = 0; u < kTilesPerWarp; ++u) {
+      for (int u = 0; u < Cfg<T>::kTilesPerWarp; ++u) {
         const int tl = warp + u * kConsumers;
         if (!failed && tl < nt) group_dot<T, kGroupSums>(c[u], gs + tl, sq, sgsum, sdx, a, row, y);
       }
       if (++slot == S) { slot = 0; phase ^= 1u; }
     }
     if (!kGroupSums) {
-      // The 16 partial sums of each row meet in shared memory; warp
-      // (i*T + t) % 16 adds those of token t in warp order (deterministic) and
+      // The warps' partial sums of each row meet in shared memory; warp
+      // (i*T + t) % warps adds those of token t in warp order (deterministic) and
       // stores them. Buffers alternate between tile columns; mbarriers order
       // the writers and the reducers, so no warp waits for all the others.
       const int p = i & 1;
@@ -559,9 +568,9 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1) gemv_mma_kernel(const Gem
         failed = true;
       failed = __any_sync(0xffffffffu, failed);   // mma.sync below is warp-wide
       const uint8_t* stage = ring + (size_t)slot * kStageBytes;
-      MmaCodes mc[kTilesPerWarp];
+      MmaCodes mc[Cfg<T>::kTilesPerWarp];
 #pragma unroll
-      for (int u = 0; u < kTilesPerWarp; ++u) {
+      for (int u = 0; u < Cfg<T>::kTilesPerWarp; ++u) {
         const int tl = warp + u * kConsumers;
         if (!failed && tl < nt) load_mma_codes(stage + tl * kTileBytes, lane, mc[u]);
       }
@@ -579,7 +588,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1) gemv_mma_kernel(const Gem
         }
       }
 #pragma unroll
-      for (int u = 0; u < kTilesPerWarp; ++u) {
+      for (int u = 0; u < Cfg<T>::kTilesPerWarp; ++u) {
         const int tl = warp + u * kConsumers;
         if (!failed && tl < nt)
           group_mma<T, kGroupSums>(mc[u], gs + tl, sb, pl.sb_stride, sgsum, sdx, a, row_base, lane, y);
@@ -587,7 +596,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1) gemv_mma_kernel(const Gem
       if (++slot == S) { slot = 0; phase ^= 1u; }
     }
     if (!kGroupSums) {
-      // The 16 warps' partial sums of this tile column meet in shared memory;
+      // The warps' partial sums of this tile column meet in shared memory;
       // warp (i*8 + e) % 16 adds C position e over the warps in warp order.
       const int p = i & 1;
       float* r = red + p * (kConsumers * 8 * 32);
