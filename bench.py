@@ -14,8 +14,9 @@ synchronize, timed with CUDA events, max over ranks. Weights rotate over
 copies whose total exceeds twice the 129 MB L2, so every step streams its
 weights from HBM. The GEMV's own duration is taken from events around each of
 its launches inside the timed graph. `e2e` repeats the step through the
-Python API with host buffers: pinned host -> device copy of the activations,
-quantize, matmul, device -> pinned host copy of the outputs, every step.
+C ABI with host buffers (tq_matmul_host): pinned host -> device copy of the
+activations, quantize, matmul, device -> pinned host copy of the outputs,
+every step.
 
 `--impl reference` times the plain C oracle on the host cores instead (a row
 sample of the same workload per step).
@@ -388,7 +389,8 @@ def time_graph(wl: Workload, steps: int, warmup: int, world: int):
 
 
 def time_e2e(wl: Workload, steps: int, warmup: int):
-    """Through the Python API with host buffers: H2D of X, quantize, matmul, D2H of Y."""
+    """Through the C ABI with host buffers: one tq_matmul_host call per step
+    (pinned host X -> device, quantize, matmul, device -> pinned host Y)."""
     import torch
     import bit_matvec_gb300 as tq
     x_pin = torch.from_numpy(wl.x_host).pin_memory()
@@ -397,10 +399,8 @@ def time_e2e(wl: Workload, steps: int, warmup: int):
     stream = torch.cuda.current_stream(wl.device)
 
     def one(i):
-        X.copy_(x_pin, non_blocking=True)
-        tq.tq_quantize_q8K(X, wl.Xq, wl.ntok, wl.cols, stream)
-        tq.tq_matmul_ws(wl.W[i % wl.copies], wl.Xq, wl.Y, wl.rows, wl.cols, wl.ntok, wl.ws, stream)
-        y_pin.copy_(wl.Y, non_blocking=True)
+        tq.tq_matmul_host(wl.W[i % wl.copies], x_pin, X, wl.Xq, wl.Y, y_pin, wl.rows, wl.cols,
+                          wl.ntok, wl.ws, stream)
 
     for i in range(max(warmup, 3)):
         one(i)

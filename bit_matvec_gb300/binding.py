@@ -80,6 +80,7 @@ def _load():
             "tq_matmul_ws": ([P, P, P, I64, I64, I64, P, I64, P], I),
             "tq_matmul_groupsums_ws": ([P, P, P, I64, I64, I64, P, I64, P], I),
             "tq_matmul_static_ws": ([P, P, P, I64, I64, I64, P], I),
+            "tq_matmul_host": ([P, P, P, P, P, P, I64, I64, I64, P, I64, P], I),
             "tq_strerror": ([I], ctypes.c_char_p),
             "tq_last_cuda_error": ([], I),
             "tq_device_status": ([], I),
@@ -206,6 +207,25 @@ def tq_matmul_static_ws(Wtq: torch.Tensor, Xq: torch.Tensor, Y: torch.Tensor, ro
     its workspace, for callers that cannot allocate device memory. Calls share
     that array: calls that overlap on the GPU race, so keep them ordered."""
     _call("tq_matmul_static_ws", Wtq.device, _ptr(Wtq), _ptr(Xq), _ptr(Y), rows, cols, ntok,
+          _stream(stream, Wtq.device))
+
+
+def _host_ptr(t: torch.Tensor):
+    if t.is_cuda:
+        raise ValueError("tensor must live in host memory")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def tq_matmul_host(Wtq: torch.Tensor, X_host: torch.Tensor, X: torch.Tensor, Xq: torch.Tensor,
+                   Y: torch.Tensor, Y_host: torch.Tensor, rows: int, cols: int, ntok: int,
+                   workspace: torch.Tensor, stream=None):
+    """Host f32 activations in, host f32 outputs out, in one enqueued step (copy
+    in, quantize, matmul, copy out); X_host and Y_host should be pinned. Returns
+    at once: synchronize the stream before reading Y_host."""
+    _call("tq_matmul_host", Wtq.device, _ptr(Wtq), _host_ptr(X_host), _ptr(X), _ptr(Xq), _ptr(Y),
+          _host_ptr(Y_host), rows, cols, ntok, _ptr(workspace), workspace.numel(),
           _stream(stream, Wtq.device))
 
 

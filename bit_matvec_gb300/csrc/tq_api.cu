@@ -228,6 +228,42 @@ int tq_matmul_groupsums_ws(const void* Wtq, const void* Xq, int32_t* S, int64_t 
                      stream);
 }
 
+int tq_matmul_host(const void* Wtq, const float* X_host, float* X, void* Xq, float* Y,
+                   float* Y_host, int64_t rows, int64_t cols, int64_t ntok, void* workspace,
+                   int64_t workspace_bytes, void* stream) {
+  if (rows < 0 || cols < 0 || ntok < 0 || cols % kQK != 0) return TQ_ERR_SHAPE;
+  if (rows == 0 || ntok == 0) return TQ_OK;
+  // every check of the calls below, before anything is enqueued
+  if (!X_host || !Y_host || !X || !Xq || !Y || !Wtq) return TQ_ERR_NULL;
+  if (!aligned16(X) || !aligned16(Xq) || !aligned16(Wtq) || !aligned4(Y)) return TQ_ERR_ALIGN;
+  const int64_t x_bytes = ntok * cols * 4, y_bytes = ntok * rows * 4;
+  const int64_t xq_bytes = q8K_bytes(ntok, cols), w_bytes = tq_repacked_bytes(rows, cols);
+  if (overlap(X, x_bytes, Xq, xq_bytes) || overlap(Y, y_bytes, Wtq, w_bytes) ||
+      overlap(Y, y_bytes, Xq, xq_bytes) || overlap(Y, y_bytes, X, x_bytes))
+    return TQ_ERR_ALIAS;
+  const int64_t need = tq::workspace_bytes(rows, cols, ntok);
+  if (need > 0) {
+    if (!workspace) return TQ_ERR_NULL;
+    if (!aligned16(workspace)) return TQ_ERR_ALIGN;
+    if (workspace_bytes < need) return TQ_ERR_WORKSPACE;
+    if (overlap(workspace, need, Y, y_bytes) || overlap(workspace, need, Wtq, w_bytes) ||
+        overlap(workspace, need, Xq, xq_bytes))
+      return TQ_ERR_ALIAS;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (x_bytes > 0) {
+    const cudaError_t e = cudaMemcpyAsync(X, X_host, (size_t)x_bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  int rc = tq_quantize_q8K(X, Xq, ntok, cols, stream);
+  if (rc != TQ_OK) return rc;
+  rc = tq_matmul_ws(Wtq, Xq, Y, rows, cols, ntok, workspace, workspace_bytes, stream);
+  if (rc != TQ_OK) return rc;
+  const cudaError_t e = cudaMemcpyAsync(Y_host, Y, (size_t)y_bytes, cudaMemcpyDeviceToHost, s);
+  note_op(s, kOpOther);
+  return e == cudaSuccess ? TQ_OK : fail_cuda(e);
+}
+
 const char* tq_strerror(int code) {
   switch (code) {
     case TQ_OK: return "ok";

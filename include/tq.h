@@ -195,6 +195,28 @@ int tq_matmul_groupsums_ws(const void *Wtq, const void *Xq, int32_t *S, int64_t 
                            int64_t workspace_bytes, void *stream);
 
 /*
+ * tq_matmul_host -- one whole step from host memory to host memory, in one
+ * call: copy X from the host, quantize it (tq_quantize_q8K), multiply
+ * (tq_matmul_ws), copy Y back to the host. Everything is enqueued on `stream`
+ * with cudaMemcpyAsync and kernel launches; the call returns at once, so the
+ * caller synchronizes the stream before reading Y_host.
+ *   X_host [ntok][cols] f32 host memory, pinned (page-locked) for the copy
+ *          to be asynchronous; it must stay unchanged until the copy is done.
+ *   X      [ntok][cols] f32 device staging buffer, 16-byte aligned.
+ *   Xq     [ntok][cols/256] q8_K device buffer, 16-byte aligned.
+ *   Y      [ntok][rows] f32 device buffer, 4-byte aligned.
+ *   Y_host [ntok][rows] f32 host memory, pinned; written when the stream
+ *          reaches the copy.
+ *   Wtq, workspace, workspace_bytes: as tq_matmul_ws.
+ * Errors: those of tq_quantize_q8K and tq_matmul_ws, checked before anything
+ * is enqueued; TQ_ERR_NULL for a NULL host or staging buffer; TQ_ERR_CUDA if
+ * a copy or launch fails (work already enqueued stays enqueued).
+ */
+int tq_matmul_host(const void *Wtq, const float *X_host, float *X, void *Xq, float *Y,
+                   float *Y_host, int64_t rows, int64_t cols, int64_t ntok, void *workspace,
+                   int64_t workspace_bytes, void *stream);
+
+/*
  * tq_matmul_static_ws -- tq_matmul_ws without a caller workspace: the
  * workspace is a fixed device array of TQ_STATIC_WS_BYTES inside this
  * library, so the call allocates nothing. The paper has no counterpart to

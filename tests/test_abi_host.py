@@ -159,3 +159,32 @@ def test_workspace_errors(lib):
     assert ws(None, None, None, 64, 512, 0, None, 0, None) == tq.TQ_OK
     gs = lib.tq_matmul_groupsums_ws
     assert gs(P(A), P(B), P(C), 64, 512, 16, P(D), need - 1, None) == tq.TQ_ERR_WORKSPACE
+
+
+def test_matmul_host_errors_before_any_work(lib):
+    """tq_matmul_host checks everything its copies and kernels would before it
+    enqueues anything, so fake addresses never reach the GPU."""
+    import bit_matvec_gb300 as tq
+    H, X, D = 0x10000000, 0x7F4000000000, 0x7F3000000000
+    f = lib.tq_matmul_host
+    need = lib.tq_matmul_workspace_bytes(64, 512, 16)
+    args = lambda **k: [P(k.get("w", A)), P(k.get("xh", H)), P(k.get("x", X)), P(k.get("xq", B)),
+                        P(k.get("y", C)), P(k.get("yh", H + (1 << 20))), k.get("rows", 64),
+                        k.get("cols", 512), k.get("ntok", 16), P(k.get("ws", D)),
+                        k.get("wsb", need), None]
+    assert f(*args(cols=300)) == tq.TQ_ERR_SHAPE
+    assert f(*args(rows=-1)) == tq.TQ_ERR_SHAPE
+    assert f(*args(ntok=0)) == tq.TQ_OK
+    assert f(*args(xh=0)) == tq.TQ_ERR_NULL
+    assert f(*args(yh=0)) == tq.TQ_ERR_NULL
+    assert f(*args(x=0)) == tq.TQ_ERR_NULL
+    assert f(*args(ws=0)) == tq.TQ_ERR_NULL
+    assert f(*args(x=X + 8)) == tq.TQ_ERR_ALIGN
+    assert f(*args(y=C + 2)) == tq.TQ_ERR_ALIGN
+    assert f(*args(ws=D + 8)) == tq.TQ_ERR_ALIGN
+    assert f(*args(wsb=need - 16)) == tq.TQ_ERR_WORKSPACE
+    assert f(*args(x=B)) == tq.TQ_ERR_ALIAS
+    assert f(*args(y=B)) == tq.TQ_ERR_ALIAS
+    assert f(*args(ws=C)) == tq.TQ_ERR_ALIAS
+    # one token needs no workspace
+    assert f(*args(ntok=1, ws=0, wsb=0, x=0)) == tq.TQ_ERR_NULL

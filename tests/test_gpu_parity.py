@@ -199,6 +199,27 @@ def test_deterministic_and_stream():
     assert tq.tq_device_status() == tq.TQ_OK
 
 
+@pytest.mark.parametrize("ntok", [1, 6, 64])
+def test_matmul_host_matches_device_calls(ntok):
+    """The host-to-host step gives the bits of quantize + tq_matmul_ws on device."""
+    import bit_matvec_gb300 as tq
+    rows, cols = 300, 1024
+    wpq, x = _weights(rows, cols, 4), _acts(ntok, cols, 4)
+    Wtq = gpu_repack(wpq, rows, cols)
+    y_dev = gpu_matmul_ws(Wtq, gpu_quantize(x), rows, cols, ntok)
+    x_pin = torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    y_pin = torch.full((ntok, rows), float("nan"), dtype=torch.float32).pin_memory()
+    X = torch.empty((ntok, cols), dtype=torch.float32, device=DEV)
+    Xq = tq.q8K_empty(ntok, cols, DEV)
+    Y = torch.empty((ntok, rows), dtype=torch.float32, device=DEV)
+    ws = tq.workspace_empty(rows, cols, ntok, DEV)
+    tq.tq_matmul_host(Wtq, x_pin, X, Xq, Y, y_pin, rows, cols, ntok, ws)
+    torch.cuda.current_stream().synchronize()
+    assert np.array_equal(y_pin.numpy().view(np.uint32), y_dev.view(np.uint32))
+    y_ref, abs_sum = oracle.matmul(wpq, oracle.quantize_q8K(x), rows, cols)
+    assert_close(y_pin.numpy(), y_ref, abs_sum)
+
+
 # ---------------------------------------------------------------- full-size workloads
 
 @pytest.mark.parametrize("name", ["tiny", "decode", "small_batch", "prefill"])
