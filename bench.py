@@ -1,8 +1,9 @@
 """Benchmark of the ternary pq2_0 x q8_K hot path on GB300.
 
 One step = one pass of the hot path over one batch of synthetic input:
-quantize the activations to q8_K, then the ternary matmul (the load-time
-repack runs once, before timing, and is reported separately). The headline
+quantize the activations to q8_K, then the ternary matmul, through
+tq_quantize_matmul (one fused launch up to 8 tokens; the load-time repack
+runs once, before timing, and is reported separately). The headline
 workload is the decode GEMV (32768 x 8192 weights, 1 token), measured in
 Gweights/s; the 4-token and 64-token 17408 x 5120 tiles are measured in the
 same run in GMAC/s, and the 64-block decode-step replay (23.82 G weights,
@@ -205,10 +206,23 @@ class Workload:
         self.device = device
 
     def step(self, i, stream=None):
+        """quantize + matmul: one fused launch for ntok <= 8."""
         import bit_matvec_gb300 as tq
-        tq.tq_quantize_q8K(self.X, self.Xq, self.ntok, self.cols, stream)
-        tq.tq_matmul_ws(self.W[i % self.copies], self.Xq, self.Y, self.rows, self.cols, self.ntok,
-                        self.ws, stream)
+        tq.tq_quantize_matmul(self.W[i % self.copies], self.X, self.Xq, self.Y, self.rows,
+                              self.cols, self.ntok, self.ws, stream)
+
+    def matmul_only(self, i, stream=None):
+        """The dominant kernel alone: the fused GEMV for ntok <= 8 (it is the
+        whole step), the workspace tensor-core matmul otherwise."""
+        import bit_matvec_gb300 as tq
+        if self.ntok <= 8:
+            self.step(i, stream)
+        else:
+            tq.tq_matmul_ws(self.W[i % self.copies], self.Xq, self.Y, self.rows, self.cols,
+                            self.ntok, self.ws, stream)
+
+    def launches(self):
+        return 1 if self.ntok <= 8 else 3
 
     def weights(self):
         return self.rows * self.cols
@@ -249,12 +263,11 @@ class ReplayWorkload:
         import bit_matvec_gb300 as tq
         for b in range(self.blocks):
             for m in self.mats:
-                tq.tq_quantize_q8K(m["X"], m["Xq"], self.ntok, m["cols"], stream)
-                tq.tq_matmul_ws(m["W"][b], m["Xq"], m["Y"], m["rows"], m["cols"], self.ntok,
-                                self.ws, stream)
+                tq.tq_quantize_matmul(m["W"][b], m["X"], m["Xq"], m["Y"], m["rows"], m["cols"],
+                                      self.ntok, self.ws, stream)
 
     def launches(self):
-        return 2 * self.blocks * len(self.mats)
+        return (1 if self.ntok <= 8 else 3) * self.blocks * len(self.mats)
 
     def weights(self):
         return self.blocks * sum(m["rows"] * m["cols"] for m in self.mats)
@@ -359,13 +372,14 @@ def time_graph(wl: Workload, steps: int, warmup: int, world: int):
         gm = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gm, stream=stream):
             for i in range(n):
-                tq.tq_matmul_ws(wl.W[i], wl.Xq, wl.Y, wl.rows, wl.cols, wl.ntok, wl.ws, stream)
+                wl.matmul_only(i, stream)
         gb = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gb, stream=stream):
             for i in range(n):
-                tq.tq_quantize_q8K(wl.X, wl.Xq, wl.ntok, wl.cols, stream)
+                if wl.ntok > 8:
+                    tq.tq_quantize_q8K(wl.X, wl.Xq, wl.ntok, wl.cols, stream)
                 ev[i][0].record(stream)
-                tq.tq_matmul_ws(wl.W[i], wl.Xq, wl.Y, wl.rows, wl.cols, wl.ntok, wl.ws, stream)
+                wl.matmul_only(i, stream)
                 ev[i][1].record(stream)
         reps = -(-steps // n)
         for g in (ga, gm, gb):                          # graph warm-up replays
@@ -539,7 +553,8 @@ def measure(name, args, rank, world, device, peaks, peak_kind, steps):
         traffic = profile_traffic(f"gemv_{name}_ncu.txt", GEMV_FILES)
         res["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                            "frac": achieved / peak, "traffic": traffic,
-                           "kernel": "gemv_kernel", "kernel_ms": kern_ms, "kernel_timing": kern_how,
+                           "kernel": "gemv_kernel (quantize fused in)", "kernel_ms": kern_ms,
+                           "kernel_timing": kern_how,
                            "kernel_ms_serialised": serial_ms,
                            "algorithmic_bytes": abytes, "peak_source": peak_kind}
     else:
@@ -665,7 +680,7 @@ def main():
             "roofline": main_res["roofline"],
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 2 * main_res["steps"],
+            "gpu_launches": wl.launches() * main_res["steps"],
             "clocks": clocks.summary(),
             "repack_ms": main_res["repack_ms"],
             "also": extra,

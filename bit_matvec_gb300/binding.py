@@ -81,6 +81,7 @@ def _load():
             "tq_matmul_groupsums_ws": ([P, P, P, I64, I64, I64, P, I64, P], I),
             "tq_matmul_static_ws": ([P, P, P, I64, I64, I64, P], I),
             "tq_matmul_host": ([P, P, P, P, P, P, I64, I64, I64, P, I64, P], I),
+            "tq_quantize_matmul": ([P, P, P, P, I64, I64, I64, P, I64, P], I),
             "tq_strerror": ([I], ctypes.c_char_p),
             "tq_last_cuda_error": ([], I),
             "tq_device_status": ([], I),
@@ -208,6 +209,13 @@ def tq_matmul_static_ws(Wtq: torch.Tensor, Xq: torch.Tensor, Y: torch.Tensor, ro
     that array: calls that overlap on the GPU race, so keep them ordered."""
     _call("tq_matmul_static_ws", Wtq.device, _ptr(Wtq), _ptr(Xq), _ptr(Y), rows, cols, ntok,
           _stream(stream, Wtq.device))
+
+
+def tq_quantize_matmul(Wtq: torch.Tensor, X: torch.Tensor, Xq: torch.Tensor, Y: torch.Tensor,
+                       rows: int, cols: int, ntok: int, workspace: torch.Tensor, stream=None):
+    """Xq = q8_K(X) and Y = Wtq x Xq in one call (one fused launch for ntok <= 8)."""
+    _call("tq_quantize_matmul", Wtq.device, _ptr(Wtq), _ptr(X), _ptr(Xq), _ptr(Y), rows, cols,
+          ntok, _ptr(workspace), workspace.numel(), _stream(stream, Wtq.device))
 
 
 def _host_ptr(t: torch.Tensor):

@@ -24,7 +24,7 @@ std::map<std::pair<int, const void*>, int> g_smem_optin;
 // Last kernel this library enqueued on each stream. The GEMV may read weights
 // before the preceding kernel finishes only when that kernel is the quantizer,
 // which never writes weights.
-enum LastOp { kOpOther = 0, kOpQuantize = 1 };
+enum LastOp { kOpOther = 0, kOpQuantize = 1, kOpMatmul = 2 };
 std::mutex g_stream_mu;
 std::unordered_map<cudaStream_t, int> g_last_op;
 
@@ -37,6 +37,14 @@ bool last_op_is_quantize(cudaStream_t s) {
   std::lock_guard<std::mutex> lk(g_stream_mu);
   auto it = g_last_op.find(s);
   return it != g_last_op.end() && it->second == kOpQuantize;
+}
+
+// The last call on the stream was the quantizer or a matmul: kernels that
+// never write weights.
+bool last_op_keeps_weights(cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_stream_mu);
+  auto it = g_last_op.find(s);
+  return it != g_last_op.end() && (it->second == kOpQuantize || it->second == kOpMatmul);
 }
 
 int fail_cuda(cudaError_t e) {
@@ -228,6 +236,55 @@ int tq_matmul_groupsums_ws(const void* Wtq, const void* Xq, int32_t* S, int64_t 
                      stream);
 }
 
+int tq_quantize_matmul(const void* Wtq, const float* X, void* Xq, float* Y, int64_t rows,
+                       int64_t cols, int64_t ntok, void* workspace, int64_t workspace_bytes,
+                       void* stream) {
+  if (rows < 0 || cols < 0 || ntok < 0 || cols % kQK != 0) return TQ_ERR_SHAPE;
+  if (rows == 0 || ntok == 0) return TQ_OK;
+  if (cols == 0) return tq_matmul_ws(Wtq, Xq, Y, rows, cols, ntok, workspace, workspace_bytes, stream);
+  // every check of the calls below, before anything is enqueued
+  if (!X || !Xq || !Y || !Wtq) return TQ_ERR_NULL;
+  if (!aligned16(X) || !aligned16(Xq) || !aligned16(Wtq) || !aligned4(Y)) return TQ_ERR_ALIGN;
+  const int64_t x_bytes = ntok * cols * 4, y_bytes = ntok * rows * 4;
+  const int64_t xq_bytes = q8K_bytes(ntok, cols), w_bytes = tq_repacked_bytes(rows, cols);
+  if (overlap(X, x_bytes, Xq, xq_bytes) || overlap(Y, y_bytes, Wtq, w_bytes) ||
+      overlap(Y, y_bytes, Xq, xq_bytes) || overlap(Y, y_bytes, X, x_bytes) ||
+      overlap(Xq, xq_bytes, Wtq, w_bytes))
+    return TQ_ERR_ALIAS;
+  const int64_t need = tq::workspace_bytes(rows, cols, ntok);
+  if (need > 0) {
+    if (!workspace) return TQ_ERR_NULL;
+    if (!aligned16(workspace)) return TQ_ERR_ALIGN;
+    if (workspace_bytes < need) return TQ_ERR_WORKSPACE;
+    if (overlap(workspace, need, Y, y_bytes) || overlap(workspace, need, Wtq, w_bytes) ||
+        overlap(workspace, need, Xq, xq_bytes) || overlap(workspace, need, X, x_bytes))
+      return TQ_ERR_ALIAS;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (ntok <= gemv_max_tokens()) {
+    int* status = nullptr;
+    cudaError_t e = device_status_ptr(&status);
+    if (e != cudaSuccess) return fail_cuda(e);
+    const bool early = last_op_keeps_weights(s);
+    e = launch_gemv(static_cast<const uint8_t*>(Wtq), nullptr, Y, nullptr, rows, cols, (int)ntok,
+                    status, early, s, X, static_cast<uint8_t*>(Xq));
+    if (e == cudaSuccess) {
+      note_op(s, kOpMatmul);
+      return TQ_OK;
+    }
+    if (e != cudaErrorNotSupported) {
+      note_op(s, kOpOther);
+      return fail_cuda(e);
+    }
+    // activations too large for the GEMV's shared memory: the separate calls
+  }
+  int rc = tq_quantize_q8K(X, Xq, ntok, cols, stream);
+  if (rc != TQ_OK) return rc;
+  rc = tq_matmul_ws(Wtq, Xq, Y, rows, cols, ntok, workspace, workspace_bytes, stream);
+  if (rc == TQ_OK) note_op(s, kOpMatmul);
+  return rc;
+}
+
 int tq_matmul_host(const void* Wtq, const float* X_host, float* X, void* Xq, float* Y,
                    float* Y_host, int64_t rows, int64_t cols, int64_t ntok, void* workspace,
                    int64_t workspace_bytes, void* stream) {
@@ -255,9 +312,8 @@ int tq_matmul_host(const void* Wtq, const float* X_host, float* X, void* Xq, flo
     const cudaError_t e = cudaMemcpyAsync(X, X_host, (size_t)x_bytes, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return fail_cuda(e);
   }
-  int rc = tq_quantize_q8K(X, Xq, ntok, cols, stream);
-  if (rc != TQ_OK) return rc;
-  rc = tq_matmul_ws(Wtq, Xq, Y, rows, cols, ntok, workspace, workspace_bytes, stream);
+  const int rc = tq_quantize_matmul(Wtq, X, Xq, Y, rows, cols, ntok, workspace, workspace_bytes,
+                                    stream);
   if (rc != TQ_OK) return rc;
   const cudaError_t e = cudaMemcpyAsync(Y_host, Y, (size_t)y_bytes, cudaMemcpyDeviceToHost, s);
   note_op(s, kOpOther);

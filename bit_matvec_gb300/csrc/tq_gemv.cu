@@ -70,7 +70,7 @@ struct Cfg {
   static constexpr int kTilesPerWarp = T == 1 ? TQ_GEMV_TILES_PER_WARP_T1 : TQ_GEMV_TILES_PER_WARP;
   static constexpr int kStageTiles = kWarps * kTilesPerWarp;
   static constexpr int kStageBytes = kStageTiles * kTileBytes;
-  static constexpr int kMinCtas = (T == 1 && kThreads <= 512) ? 2 : 1;
+  static constexpr int kMinCtas = (T == 1 && kThreads <= 512) ? TQ_GEMV_CTAS_PER_SM : 1;
 };
 
 struct GemvArgs {
@@ -85,7 +85,54 @@ struct GemvArgs {
   int nrb;            // 32-row tile columns
   int stages;         // ring depth
   int early_weights;  // 1: the previous kernel does not write Wtq; prefetch before waiting
+  const float* X;     // fused form: f32 activations [T][cols] quantized here (else null)
+  uint8_t* Xq_out;    // fused form: where CTA 0 writes the q8_K blocks (may be null)
 };
+
+// Fused form: quantizes the T x cols f32 activations block by block (warp per
+// q8_K block, q8K_warp, so the bytes equal the quantizer kernel's), four
+// blocks per warp whose loads are issued together, and hands each block to
+// store(tb, w0, w1, s8, d) on every lane of the warp. CTA 0 also writes the
+// q8_K blocks to a.Xq_out.
+template <class Store>
+__device__ __forceinline__ void stage_quantize(const GemvArgs& a, int nblocks, int warp,
+                                               int nwarps, int lane, Store store) {
+  const bool write_xq = a.Xq_out != nullptr && blockIdx.x == 0;
+  for (int tb0 = warp; tb0 < nblocks; tb0 += 4 * nwarps) {
+    float4 va[4], vb[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int tb = tb0 + c * nwarps;
+      if (tb < nblocks) {
+        const float4* src = reinterpret_cast<const float4*>(a.X + (int64_t)tb * kQK) + 2 * lane;
+        va[c] = __ldg(src);
+        vb[c] = __ldg(src + 1);
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int tb = tb0 + c * nwarps;
+      if (tb < nblocks) {   // warp-uniform
+        uint32_t w0, w1;
+        int s8;
+        float d;
+        q8K_warp(va[c], vb[c], w0, w1, s8, d);
+        store(tb, w0, w1, s8, d);
+        if (write_xq) q8K_store(a.Xq_out + (int64_t)tb * kQ8KBytes, lane, w0, w1, s8, d);
+      }
+    }
+  }
+}
+
+// Sum of s8 over the 16 lanes of each half-warp (one 128-value half-block),
+// valid on lanes 0 and 16.
+__device__ __forceinline__ int half_block_sum(int s8) {
+  s8 += __shfl_xor_sync(0xffffffffu, s8, 1);
+  s8 += __shfl_xor_sync(0xffffffffu, s8, 2);
+  s8 += __shfl_xor_sync(0xffffffffu, s8, 4);
+  s8 += __shfl_xor_sync(0xffffffffu, s8, 8);
+  return s8;
+}
 
 struct GroupCodes {
   uint4 lo, hi;     // weights 0..63 and 64..127 of this lane's row
@@ -210,7 +257,16 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
   // Stage q8_K activations, every thread issuing independent loads: qs as a
   // dense int8 [T][cols] array (block tb = t * nblk + b lands at tb * 256), the
   // sum of each 128-value half-block (8 partial sums), and the block scales.
-  {
+  // The fused form quantizes a.X into the same arrays instead.
+  if (a.X) {
+    stage_quantize(a, T * a.nblk, warp, kConsumers, lane,
+                   [&](int tb, uint32_t w0, uint32_t w1, int s8, float d) {
+                     reinterpret_cast<uint2*>(sq + tb * kQK)[lane] = make_uint2(w0, w1);
+                     const int hs = half_block_sum(s8);
+                     if ((lane & 15) == 0) sgsum[2 * tb + (lane >> 4)] = hs;
+                     if (lane == 0) sdx[tb] = d;
+                   });
+  } else {
     const int nw = T * a.nblk * (kQK / 4);
 #pragma unroll 4
     for (int w = threadIdx.x; w < nw; w += Cfg<T>::kThreads) {
@@ -528,28 +584,36 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1) gemv_mma_kernel(const Gem
   // Stage the activations: f16 q * 2^(9 - 2s) per token row, the sum of each
   // 128-value half-block (8 partial sums), and the block scales. Lane l takes
   // values 8l .. 8l + 7 of a block (slots 2(l & 1) and 2(l & 1) + 1).
-  for (int tb = warp; tb < T * a.nblk; tb += kConsumers) {
+  auto put_f16 = [&](int tb, uint32_t v0, uint32_t v1) {
     const int t = tb / a.nblk, b = tb - t * a.nblk;
-    const uint8_t* blk = a.Xq + (int64_t)tb * kQ8KBytes;
-    const uint32_t* qs = reinterpret_cast<const uint32_t*>(blk + kQ8KQsOffset);
-    const uint32_t v0 = __ldg(qs + 2 * lane), v1 = __ldg(qs + 2 * lane + 1);
     uint32_t h[4];
     tc::s8x4_to_h2x2(v0, h[0], h[1]);
     tc::s8x4_to_h2x2(v1, h[2], h[3]);
     const uint32_t m0 = mma_slot_scale(2 * (lane & 1)), m1 = mma_slot_scale(2 * (lane & 1) + 1);
-    h[0] = h2_mul_rn(h[0], m0);
-    h[1] = h2_mul_rn(h[1], m0);
-    h[2] = h2_mul_rn(h[2], m1);
-    h[3] = h2_mul_rn(h[3], m1);
     uint2* dst = reinterpret_cast<uint2*>(sb + t * pl.sb_stride + ((int64_t)b * kQK + 8 * lane) * 2);
-    dst[0] = make_uint2(h[0], h[1]);
-    dst[1] = make_uint2(h[2], h[3]);
-    int s = lane < 16 ? (int)__ldg(reinterpret_cast<const int16_t*>(blk + kQ8KBsumsOffset) + lane) : 0;
-    s += __shfl_xor_sync(0xffffffffu, s, 1);
-    s += __shfl_xor_sync(0xffffffffu, s, 2);
-    s += __shfl_xor_sync(0xffffffffu, s, 4);
-    if (lane == 0 || lane == 8) sgsum[t * a.ngroups + 2 * b + (lane >> 3)] = s;
-    if (lane == 0) sdx[tb] = __ldg(reinterpret_cast<const float*>(blk));
+    dst[0] = make_uint2(h2_mul_rn(h[0], m0), h2_mul_rn(h[1], m0));
+    dst[1] = make_uint2(h2_mul_rn(h[2], m1), h2_mul_rn(h[3], m1));
+  };
+  if (a.X) {
+    stage_quantize(a, T * a.nblk, warp, kConsumers, lane,
+                   [&](int tb, uint32_t w0, uint32_t w1, int s8, float d) {
+                     put_f16(tb, w0, w1);
+                     const int hs = half_block_sum(s8);
+                     if ((lane & 15) == 0) sgsum[2 * tb + (lane >> 4)] = hs;
+                     if (lane == 0) sdx[tb] = d;
+                   });
+  } else {
+    for (int tb = warp; tb < T * a.nblk; tb += kConsumers) {
+      const uint8_t* blk = a.Xq + (int64_t)tb * kQ8KBytes;
+      const uint32_t* qs = reinterpret_cast<const uint32_t*>(blk + kQ8KQsOffset);
+      put_f16(tb, __ldg(qs + 2 * lane), __ldg(qs + 2 * lane + 1));
+      int s = lane < 16 ? (int)__ldg(reinterpret_cast<const int16_t*>(blk + kQ8KBsumsOffset) + lane) : 0;
+      s += __shfl_xor_sync(0xffffffffu, s, 1);
+      s += __shfl_xor_sync(0xffffffffu, s, 2);
+      s += __shfl_xor_sync(0xffffffffu, s, 4);
+      if (lane == 0 || lane == 8) sgsum[2 * tb + (lane >> 3)] = s;   // t * ngroups + 2b + half
+      if (lane == 0) sdx[tb] = __ldg(reinterpret_cast<const float*>(blk));
+    }
   }
   __syncthreads();
 
@@ -720,7 +784,7 @@ int gemv_max_tokens() { return kMaxTok; }
 
 cudaError_t launch_gemv(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t* S,
                         int64_t rows, int64_t cols, int ntok, int* dev_status, bool early_weights,
-                        cudaStream_t s) {
+                        cudaStream_t s, const float* X, uint8_t* Xq_out) {
   if (ntok < 1 || ntok > kMaxTok) return cudaErrorNotSupported;
   if (rows > 0x7fffffff / 2 || cols / kGroup > 0x7fffffff / kTileBytes)
     return cudaErrorNotSupported;
@@ -736,6 +800,8 @@ cudaError_t launch_gemv(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t
   a.nrb = (int)((rows + kTileRows - 1) / kTileRows);
   a.stages = 2;
   a.early_weights = early_weights ? 1 : 0;
+  a.X = X;
+  a.Xq_out = Xq_out;
   const bool gsum = S != nullptr;
   switch (ntok) {
     case 1: return launch_tok<1>(a, cols, gsum, s);

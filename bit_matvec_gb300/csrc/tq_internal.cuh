@@ -148,6 +148,59 @@ __device__ __forceinline__ void pdl_wait_primary() {
 // ---------------------------------------------------------------- launchers
 // Each returns a cudaError_t from the launch (cudaSuccess if nothing ran).
 
+__device__ __forceinline__ uint32_t pack4_s8(int a, int b, int c, int d) {
+  return (uint32_t)(a & 0xFF) | ((uint32_t)(b & 0xFF) << 8) | ((uint32_t)(c & 0xFF) << 16) |
+         ((uint32_t)(d & 0xFF) << 24);
+}
+
+// One warp quantizes one q8_K block of 256 activations; lane l holds values
+// 8l .. 8l + 7 in (a, b). Scale: the block's largest magnitude over 127
+// (the absolute max as a warp max over float bit patterns, which order like
+// non-negative floats); q = round-to-nearest-even(x * (127 / amax)) clamped to
+// +-127, with IEEE division and no contraction; an all-zero block gives zeros.
+// Out: this lane's 8 values packed as int8 (w0, w1), their sum s8, and the
+// block scale d (the same on every lane). The quantizer kernel and the fused
+// GEMV staging both use it, so their q8_K bytes are identical.
+__device__ __forceinline__ void q8K_warp(const float4 a, const float4 b, uint32_t& w0,
+                                         uint32_t& w1, int& s8, float& d) {
+  const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax)));
+  if (amax == 0.0f) {   // uniform across the warp
+    w0 = w1 = 0u;
+    s8 = 0;
+    d = 0.0f;
+    return;
+  }
+  const float iscale = __fdiv_rn(127.0f, amax);
+  int q[8];
+  s8 = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    int qi = __float2int_rn(__fmul_rn(v[i], iscale));
+    qi = max(-127, min(127, qi));
+    q[i] = qi;
+    s8 += qi;
+  }
+  w0 = pack4_s8(q[0], q[1], q[2], q[3]);
+  w1 = pack4_s8(q[4], q[5], q[6], q[7]);
+  d = __fdiv_rn(amax, 127.0f);
+}
+
+// Stores one lane's share of a q8_K block quantized by q8K_warp (the warp
+// writes the whole 292-byte block at blk).
+__device__ __forceinline__ void q8K_store(uint8_t* blk, int lane, uint32_t w0, uint32_t w1, int s8,
+                                          float d) {
+  const int s16 = s8 + __shfl_xor_sync(0xffffffffu, s8, 1);   // 16 values: lanes 2i, 2i + 1
+  uint32_t* qs = reinterpret_cast<uint32_t*>(blk + kQ8KQsOffset) + 2 * lane;
+  qs[0] = w0;
+  qs[1] = w1;
+  if ((lane & 1) == 0) reinterpret_cast<int16_t*>(blk + kQ8KBsumsOffset)[lane >> 1] = (int16_t)s16;
+  if (lane == 0) *reinterpret_cast<float*>(blk) = d;
+}
+
 cudaError_t launch_quantize_q8K(const float* X, uint8_t* Xq, int64_t nblocks, cudaStream_t s);
 cudaError_t launch_repack(const uint8_t* Wpq2, uint8_t* Wtq, int64_t rows, int64_t cols,
                           cudaStream_t s);
@@ -177,9 +230,12 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // when the activations of all tokens do not fit in shared memory.
 // early_weights: the kernel enqueued just before on the stream does not write
 // Wtq, so weight reads may start before waiting for it.
+// With X non-null the GEMV quantizes the f32 activations X itself (the fused
+// form; Xq is then an output, written once, and may be null) instead of
+// reading q8_K blocks from Xq.
 cudaError_t launch_gemv(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t* S,
                         int64_t rows, int64_t cols, int ntok, int* dev_status, bool early_weights,
-                        cudaStream_t s);
+                        cudaStream_t s, const float* X = nullptr, uint8_t* Xq_out = nullptr);
 int gemv_max_tokens();
 
 // Tensor-core path for any ntok >= 1 (used for ntok > gemv_max_tokens()).

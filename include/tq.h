@@ -195,9 +195,33 @@ int tq_matmul_groupsums_ws(const void *Wtq, const void *Xq, int32_t *S, int64_t 
                            int64_t workspace_bytes, void *stream);
 
 /*
+ * tq_quantize_matmul -- tq_quantize_q8K then tq_matmul_ws in one call: Xq =
+ * the q8_K blocks of X, Y = the product of Wtq and Xq. For ntok <= 8 it is one
+ * fused launch: every CTA of the GEMV quantizes X into its shared memory
+ * itself (with the quantizer's arithmetic, so Xq and Y carry the bits of the
+ * two separate calls), and CTA 0 writes Xq. That removes a launch and the
+ * quantizer's place on the critical path of each matmul; larger ntok runs
+ * the two calls.
+ *   X  [ntok][cols] f32, 16-byte aligned (as tq_quantize_q8K).
+ *   Xq [ntok][cols/256] q8_K, 16-byte aligned: written.
+ *   Wtq, Y, workspace, workspace_bytes: as tq_matmul_ws (the workspace is
+ *   only used for ntok >= 9).
+ * Overlap: like tq_matmul after tq_quantize_q8K, the launch may start
+ * reading Wtq before the kernel enqueued just before it ends when the
+ * previous call this library received for the stream was the quantizer or a
+ * matmul; so do not write Wtq with a kernel of your own between such a call
+ * and this one on one stream.
+ * Errors: those of tq_quantize_q8K and tq_matmul_ws, checked before anything
+ * is enqueued.
+ */
+int tq_quantize_matmul(const void *Wtq, const float *X, void *Xq, float *Y, int64_t rows,
+                       int64_t cols, int64_t ntok, void *workspace, int64_t workspace_bytes,
+                       void *stream);
+
+/*
  * tq_matmul_host -- one whole step from host memory to host memory, in one
- * call: copy X from the host, quantize it (tq_quantize_q8K), multiply
- * (tq_matmul_ws), copy Y back to the host. Everything is enqueued on `stream`
+ * call: copy X from the host, quantize and multiply (tq_quantize_matmul),
+ * copy Y back to the host. Everything is enqueued on `stream`
  * with cudaMemcpyAsync and kernel launches; the call returns at once, so the
  * caller synchronizes the stream before reading Y_host.
  *   X_host [ntok][cols] f32 host memory, pinned (page-locked) for the copy

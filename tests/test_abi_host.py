@@ -188,3 +188,27 @@ def test_matmul_host_errors_before_any_work(lib):
     assert f(*args(ws=C)) == tq.TQ_ERR_ALIAS
     # one token needs no workspace
     assert f(*args(ntok=1, ws=0, wsb=0, x=0)) == tq.TQ_ERR_NULL
+
+
+def test_quantize_matmul_errors_before_any_work(lib):
+    import bit_matvec_gb300 as tq
+    X, D = 0x7F4000000000, 0x7F3000000000
+    f = lib.tq_quantize_matmul
+    need = lib.tq_matmul_workspace_bytes(64, 512, 16)
+    args = lambda **k: [P(k.get("w", A)), P(k.get("x", X)), P(k.get("xq", B)), P(k.get("y", C)),
+                        k.get("rows", 64), k.get("cols", 512), k.get("ntok", 16),
+                        P(k.get("ws", D)), k.get("wsb", need), None]
+    assert f(*args(cols=300)) == tq.TQ_ERR_SHAPE
+    assert f(*args(ntok=-1)) == tq.TQ_ERR_SHAPE
+    assert f(*args(rows=0)) == tq.TQ_OK
+    assert f(*args(x=0)) == tq.TQ_ERR_NULL
+    assert f(*args(xq=0)) == tq.TQ_ERR_NULL
+    assert f(*args(ws=0)) == tq.TQ_ERR_NULL
+    assert f(*args(x=X + 4)) == tq.TQ_ERR_ALIGN
+    assert f(*args(xq=B + 8)) == tq.TQ_ERR_ALIGN
+    assert f(*args(wsb=need - 1)) == tq.TQ_ERR_WORKSPACE
+    assert f(*args(xq=X)) == tq.TQ_ERR_ALIAS
+    assert f(*args(y=X + 64)) == tq.TQ_ERR_ALIAS
+    assert f(*args(xq=A)) == tq.TQ_ERR_ALIAS
+    assert f(*args(ws=X)) == tq.TQ_ERR_ALIAS
+    assert f(*args(ntok=1, ws=0, wsb=0, y=0)) == tq.TQ_ERR_NULL

@@ -199,6 +199,29 @@ def test_deterministic_and_stream():
     assert tq.tq_device_status() == tq.TQ_OK
 
 
+@pytest.mark.parametrize("rows,cols,ntok", [(300, 1024, 1), (100, 768, 3), (300, 1024, 4),
+                                             (64, 8192, 8), (32, 256, 8), (128, 1024, 9),
+                                             (100, 512, 64)])
+def test_quantize_matmul_equals_separate_calls(rows, cols, ntok):
+    """The fused call gives the bits of tq_quantize_q8K + tq_matmul_ws: Xq and Y
+    (GEMV with in-CTA quantization for ntok <= 8; the two calls above)."""
+    import bit_matvec_gb300 as tq
+    wpq, x = _weights(rows, cols, 5), _acts(ntok, cols, 5)
+    Wtq = gpu_repack(wpq, rows, cols)
+    Xq_ref = gpu_quantize(x)
+    y_ref_dev = gpu_matmul_ws(Wtq, Xq_ref, rows, cols, ntok)
+    X = torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
+    Xq = torch.full_like(Xq_ref, 0xEE)
+    Y = torch.full((ntok, rows), float("nan"), dtype=torch.float32, device=DEV)
+    ws = tq.workspace_empty(rows, cols, ntok, DEV)
+    for _ in range(2):   # twice: the second call follows a matmul (weights read early)
+        tq.tq_quantize_matmul(Wtq, X, Xq, Y, rows, cols, ntok, ws)
+    assert torch.equal(Xq, Xq_ref)
+    assert np.array_equal(Y.cpu().numpy().view(np.uint32), y_ref_dev.view(np.uint32))
+    y_ref, abs_sum = oracle.matmul(wpq, oracle.quantize_q8K(x), rows, cols)
+    assert_close(Y.cpu().numpy(), y_ref, abs_sum)
+
+
 @pytest.mark.parametrize("ntok", [1, 6, 64])
 def test_matmul_host_matches_device_calls(ntok):
     """The host-to-host step gives the bits of quantize + tq_matmul_ws on device."""
