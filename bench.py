@@ -458,6 +458,11 @@ def oracle_rate(name: str, budget_s: float, rows_per_call: int | None = None):
     return work / dt / 1e9, unit, sample, 1, dt / n, rows_per_call
 
 
+def metric_name(unit, name):
+    """The metric string both arms print for a workload."""
+    return f"ternary matvec {unit} & HBM GB/s ({WORKLOADS[name]})"
+
+
 def run_reference(args, rank, world):
     """--impl reference: the oracle on the host cores, --steps/--warmup of row samples."""
     if rank != 0:
@@ -488,7 +493,7 @@ def run_reference(args, rank, world):
               f"{cfg['cols']} cols, ntok={ntok}")
     line = {
         "impl": "reference",
-        "metric": f"ternary matvec {unit} ({WORKLOADS[name]})",
+        "metric": metric_name(unit, name),
         "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -663,7 +668,7 @@ def main():
         unit = "Gweights/s" if wl.ntok == 1 else "GMAC/s"
         value = main_res["gweights_per_s"] if wl.ntok == 1 else main_res["gmac_per_s"]
         line = {
-            "metric": f"ternary matvec {unit} & HBM GB/s ({WORKLOADS[args.workload]})",
+            "metric": metric_name(unit, args.workload),
             "value": value, "unit": unit, "n_gpus": world, "steps": main_res["steps"],
             "warmup": args.warmup, "ms_per_step": main_res["ms_per_step"],
             "higher_is_better": True, "scaling": "weak",

@@ -85,3 +85,6 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["unit"] == "Gweights/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+    sys.path.insert(0, ROOT)
+    import bench
+    assert d["metric"] == bench.metric_name("Gweights/s", "decode")   # the GPU arm's string
