@@ -67,6 +67,7 @@ constexpr uint32_t kBlkCols = kGPB * kN;             // 128: one block's accumul
 constexpr uint32_t kAccCol = 0;                      // accumulator stage c: c*128 + gi*64
 constexpr uint32_t kACol = kAccStages * kBlkCols;    // A stage a: kACol + a*128 + gi*64
 static_assert(kACol + kAStages * kBlkCols <= kTmemCols, "tensor memory overflow");
+static_assert(kAStages == kAccStages, "mma_ready pairs A stage b % 2 with accumulator stage b % 2");
 
 // B operands in UMMA canonical K-major layout without swizzle: a core matrix
 // is 8 rows x 8 f16 (16 bytes each) stored as 128 contiguous bytes; LBO = 128
@@ -92,7 +93,7 @@ constexpr int kInBytes = kInDx + kDxBytes;
 static_assert(kInBytes % 16 == 0 && kWRun % 16 == 0, "bulk copies need 16-byte multiples");
 constexpr int kSmemUsed = kInStages * kInBytes + kACorrBytes +
                           kScaleStages * (kGPB * kM + kN) * 4 +
-                          (2 * kInStages + 2 * kAStages + 2 * kAccStages) * 8 + 16;
+                          (2 * kInStages + 2 * kAStages + kAccStages) * 8 + 16;
 // Enough shared memory that only one CTA fits on an SM: each CTA allocates
 // all 512 tensor-memory columns.
 constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
@@ -233,11 +234,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
   float* sdx = sdw + kScaleStages * kGPB * kM;                                 // [scale][64]
   uint64_t* in_full = reinterpret_cast<uint64_t*>(sdx + kScaleStages * kN);    // [in]
   uint64_t* in_empty = in_full + kInStages;                                    // [in]
-  uint64_t* conv_full = in_empty + kInStages;                                  // [A]
-  uint64_t* a_free = conv_full + kAStages;                                     // [A]
+  // mma_ready[s]: the MMAs of block b (stage s = b % 2) may go: the converters
+  // have written A(b) and the epilogue has read the accumulators of b - 2 (one
+  // barrier, so the issuing thread waits once per block; the epilogue
+  // pre-arrives for blocks 0 and 1).
+  uint64_t* mma_ready = in_empty + kInStages;                                  // [A]
+  uint64_t* a_free = mma_ready + kAStages;                                     // [A]
   uint64_t* mma_done = a_free + kAStages;                                      // [acc]
-  uint64_t* acc_free = mma_done + kAccStages;                                  // [acc]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_free + kAccStages);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + kAccStages);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.ngroups;
@@ -266,12 +270,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
       mbarrier_init(smem_u32(in_empty + i), kConvWarps + 1);
     }
     for (int s = 0; s < kAStages; ++s) {
-      mbarrier_init(smem_u32(conv_full + s), kConvWarps);
+      mbarrier_init(smem_u32(mma_ready + s), kConvWarps + kEpiWarps);
       mbarrier_init(smem_u32(a_free + s), 1);
-    }
-    for (int c = 0; c < kAccStages; ++c) {
-      mbarrier_init(smem_u32(mma_done + c), 1);
-      mbarrier_init(smem_u32(acc_free + c), kEpiWarps);
+      mbarrier_init(smem_u32(mma_done + s), 1);
     }
     mbarrier_init_fence();
   }
@@ -363,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbarrier_arrive(smem_u32(conv_full + sa));
+      if (lane == 0) mbarrier_arrive(smem_u32(mma_ready + sa));
       if (++sa == kAStages) { sa = 0; pa ^= 1u; }
       if (++ss == kScaleStages) ss = 0;
     }
@@ -379,6 +380,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
     for (int p = 0; p < 16; ++p) y2[p] = 0ull;
     int c = 0, ss = 0;
     uint32_t pc = 0;
+    if (lane == 0) {   // both accumulator stages start free (blocks 0 and 1)
+      for (int s = 0; s < kAccStages; ++s) mbarrier_arrive(smem_u32(mma_ready + s));
+    }
     for (int b = 0; b < nb; ++b) {
       if (!failed && !mbarrier_wait_bounded(smem_u32(mma_done + c), pc, kWaitLimitNs)) failed = true;
       failed = __any_sync(0xffffffffu, failed);   // tcgen05.ld below is warp-wide
@@ -428,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbarrier_arrive(smem_u32(acc_free + c));
+      if (lane == 0) mbarrier_arrive(smem_u32(mma_ready + c));   // for block b + 2
       if (++c == kAccStages) { c = 0; pc ^= 1u; }
       if (++ss == kScaleStages) ss = 0;
     }
@@ -445,26 +449,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
     // ---------------- MMA issuer
     const uint64_t ac_desc = smem_desc(smem_u32(sAc), kLBO, kSBOc);
     int i = 0, sa = 0, c = 0;
-    uint32_t pa = 0, pc = 0;
+    uint32_t pa = 0;
     for (int b = 0; b < nb; ++b) {
-      if (!failed && !mbarrier_wait_bounded(smem_u32(conv_full + sa), pa, kWaitLimitNs)) failed = true;
-      // accumulator stage c is free once the epilogue has read block b - kAccStages
-      if (b >= kAccStages && !failed &&
-          !mbarrier_wait_bounded(smem_u32(acc_free + c), pc ^ 1u, kWaitLimitNs))
-        failed = true;
+      // A(b) written and the accumulators of block b - 2 read
+      if (!failed && !mbarrier_wait_bounded(smem_u32(mma_ready + sa), pa, kWaitLimitNs)) failed = true;
       tc_fence_after();
       if (!failed) {
         const uint32_t d = tmem + kAccCol + (uint32_t)c * kBlkCols;
         const uint32_t at = tmem + kACol + (uint32_t)sa * kBlkCols;
+        // Descriptors of this slot, once: the start address field (bits 0-13,
+        // address >> 4) then advances by plain adds, as no address passes 2^18.
         const uint32_t b0 = smem_u32(sIn + i * kInBytes + kInB);
+        const uint64_t bd0 = smem_desc(b0, kLBO, kSBO);
+        const uint64_t cd0 = smem_desc(b0 + kBMain, kLBO, kSBOc);
 #pragma unroll
         for (int gi = 0; gi < kGPB; ++gi) {
-          const uint32_t bg = b0 + gi * kBTile;
 #pragma unroll
           for (int kk = 0; kk < kGroup / 16; ++kk)
             mma_f16_tmem_a(d + gi * kN, at + gi * kN + 8 * kk,
-                           smem_desc(bg + kk * 2 * kLBO, kLBO, kSBO), kIdesc, kk > 0 ? 1u : 0u);
-          mma_f16_ss(d + gi * kN, ac_desc, smem_desc(bg + kBMain, kLBO, kSBOc), kIdesc, 1u);
+                           bd0 + (uint64_t)((gi * kBTile + kk * 2 * kLBO) >> 4), kIdesc,
+                           kk > 0 ? 1u : 0u);
+          mma_f16_ss(d + gi * kN, ac_desc, cd0 + (uint64_t)((gi * kBTile) >> 4), kIdesc, 1u);
         }
       }
       // the commits fire when these MMAs are done (at once if none were issued)
@@ -473,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
       mma_commit(smem_u32(in_empty + i));
       if (++i == kInStages) i = 0;
       if (++sa == kAStages) { sa = 0; pa ^= 1u; }
-      if (++c == kAccStages) { c = 0; pc ^= 1u; }
+      if (++c == kAccStages) c = 0;
     }
   }
 
