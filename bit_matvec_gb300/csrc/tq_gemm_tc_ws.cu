@@ -1,41 +1,52 @@
 // tq_gemm_tc_ws.cu -- the tensor-core path with a caller-provided workspace.
 //
-// Converting the int8 activations to the MMA's f16 B operand is the same work
-// for every 128-row tile of the weights; without a workspace each CTA repeats
-// it (tq_gemm_tc.cu). Here a pre-pass does it once: act_pack writes, for each
-// 64-token tile and each 128-weight group, the f16 B operand laid out exactly
-// as the MMA reads it (UMMA K-major, no swizzle), a small correction operand,
-// and the q8_K block scales. The tensor-core kernel stages a q8_K block with
-// one bulk copy for B, one per 32-row weight tile and one for the scales.
+// Turning the int8 activations into the MMA's B operand is the same work for
+// every 128-row tile of the weights; without a workspace each CTA repeats it
+// (tq_gemm_tc.cu). Here a pre-pass does it once: act_pack writes, for each
+// 64-token tile and each 128-weight group, the e4m3 B operand laid out exactly
+// as the MMA reads it (UMMA K-major, no swizzle), and per q8_K block the block
+// scales and the per-group activation sums (as e4m3 digits). The
+// tensor-core kernel stages a q8_K block with one bulk copy for B, one per
+// 32-row weight tile and one for the scales and sums.
 //
-// Operands. A weight code u (w = u - 1) at bits 2s..2s+1 of a byte is turned
-// into an f16 by one AND: with the exponent field zero, the half is the
-// subnormal u * 4^s * 2^-24 (exact; the tensor cores take subnormal f16
-// operands exactly). The pre-pass scales each activation by the matching
-// 2^(9 - 2s), so every product is u * q * 2^-15 exactly. A sixteen-column
-// correction MMA per group adds -2^-15 * sum_k q_k (A = constant -2^-9 and
-// -2^-15 columns, B = the sum split as 64 * hi + lo), so the accumulator ends
-// at isum * 2^-15 with isum = sum_k (u_k - 1) q_k. Every partial sum is an
-// integer multiple of 2^-15 below 2^16 * 2^-15 in magnitude, so the f32
-// accumulation is exact; the epilogue scales by d_w * 2^15 * d_x.
+// Operands (kind::f8f6f4, e4m3 x e4m3, f32 accumulate). An int8 activation q
+// is 16 * hi + lo with lo = q & 15 in [0, 15] and hi = q >> 4 in [-8, 7]; both
+// are exact in e4m3 (four significant bits), and so are lo / 4 and 16 * hi /
+// 4. B holds 128 columns per 64-token tile: lo of the 64 tokens, then 16 * hi,
+// so one MMA (M = 128, N = 128, K = 32) produces both halves and
+// sum_k u q = acc_lo + acc_hi. A weight code u (w = u - 1) at bits 2s..2s+1 of
+// a byte becomes an e4m3 byte by one AND (and a shift for s >= 2): bits 0-1
+// give the subnormal u * 2^-9, bits 2-3 give u * 4 * 2^-9 (u = 2 sets the
+// lowest exponent bit, 2^-6 = 8 * 2^-9). The pre-pass divides B by 4 at the
+// k whose A carries the factor 4, so every product is u * lo * 2^-9 or
+// u * 16 hi * 2^-9 exactly. For w = u - 1 a fifth MMA per group adds
+// -2^-9 * sum_k q (the group's sum from the q8_K bsums): B holds the sum's
+// four base-16 digits d0..d3 (d3 signed, all exact in e4m3) at k = 0..3 of
+// the low columns, A the constants -2^-9 * 16^i. Every partial sum is an
+// integer multiple of 2^-9 below 2^15 in magnitude, so the accumulation is
+// exact and ends at isum * 2^-9 (low plus high columns); the epilogue scales
+// by d_w * 2^9 * d_x.
 //
 // Per CTA (128 weight rows x 64 tokens) the work goes one q8_K block (two
 // 128-weight groups) at a time:
-//   - a producer warp stages the block's two B tiles (one 36 KB bulk copy),
+//   - a producer warp stages the block's two B tiles (one 32 KB bulk copy),
 //     the weight tiles of both groups (one 2176-byte copy per 32-row tile:
-//     consecutive groups of a tile are adjacent in the repacked layout) and 64
-//     block scales into a shared-memory ring. Few large copies: issuing a bulk
-//     copy stalls once many are in flight, and no other role issues copies;
-//   - 8 converter warps mask the codes of both groups into A and store them
-//     into tensor memory (tcgen05.st), 2 x 64 weights per thread;
-//   - one thread issues per group 8 tcgen05.mma kind::f16 (M=128, N=64, K=16)
-//     with A in tensor memory and B read from the staged slot, plus the
-//     correction MMA, into one accumulator per group in tensor memory;
-//   - 8 epilogue warps tcgen05.ld both accumulators and add
-//     d_x * (d_w0 * acc0 + d_w1 * acc1) in packed f32x2 arithmetic.
-// The A operand and the accumulators have separate rings in tensor memory: an
-// A stage is free again as soon as its MMAs finish, an accumulator once the
-// epilogue has read it.
+//     consecutive groups of a tile are adjacent in the repacked layout) and
+//     the block's scales and sums into a shared-memory ring;
+//   - 8 converter warps mask the codes of each group into A and store them
+//     into tensor memory (tcgen05.st), 64 weights per thread and group;
+//   - one thread issues per group 4 tcgen05.mma (K = 32 each) with A in
+//     tensor memory and B read from the staged slot, and the sum MMA, into one
+//     accumulator of 128 columns per group;
+//   - 8 epilogue warps tcgen05.ld each accumulator and add
+//     d_x * d_w * (acc_lo + acc_hi) in packed f32x2 arithmetic.
+// The A operands, the sum operands and the accumulators form one ring of three
+// group stages (3 x 128 accumulator and 3 x 32 A columns of tensor memory, 3 x
+// 4 KB of shared memory for the digits). The MMAs of group g wait on a single
+// barrier: the converters have written A(g) and the digits of g, and the
+// epilogue has read the accumulator of g - 3.
+#include <cuda_fp8.h>
+
 #include "tq_tcgen05.cuh"
 
 namespace tq {
@@ -43,15 +54,19 @@ namespace {
 
 using namespace tc;
 
-constexpr int kM = 128;          // weight rows per CTA (UMMA M)
-constexpr int kN = 64;           // tokens per CTA (UMMA N)
-constexpr int kGPB = kQK / kGroup;   // groups per q8_K block (2)
-constexpr int kAStages = 2;      // A operand ring in tensor memory (one block each)
-constexpr int kAccStages = 2;    // accumulator ring in tensor memory (one block each)
-// d_w / d_x per block, written by the converters and read by the epilogue: a
-// converter at block b has seen the MMAs of b - kAStages finish, which were
-// issued after the epilogue released block b - kAStages - kAccStages.
-constexpr int kScaleStages = kAStages + kAccStages;
+constexpr int kM = 128;            // weight rows per CTA (UMMA M)
+constexpr int kN = 64;             // tokens per CTA
+constexpr int kNB = 2 * kN;        // UMMA N: low and high parts of 64 tokens
+constexpr int kK = 32;             // UMMA K of kind::f8f6f4
+constexpr int kGPB = kQK / kGroup;     // groups per q8_K block (2)
+constexpr int kMmaPerGroup = kGroup / kK;   // 4
+constexpr int kStages = 3;         // A + accumulator ring in tensor memory, one group each
+// d_w, d_x and the group sums per block, written by the converters and read by
+// the epilogue. A converter writing block b has seen the MMAs of group
+// 2b - kStages finish, which were issued after the epilogue released group
+// 2b - 2 kStages; the epilogue then is past block b - kStages, so a ring of
+// kStages + 1 blocks is never overwritten while read.
+constexpr int kScaleStages = kStages + 1;
 #ifndef TQ_TC_IN_STAGES
 #define TQ_TC_IN_STAGES 3
 #endif
@@ -63,47 +78,57 @@ constexpr int kProdWarp = kMmaWarp + 1;
 constexpr int kThreads = (kProdWarp + 1) * 32;
 constexpr int kTilesPerCta = kM / kTileRows;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kBlkCols = kGPB * kN;             // 128: one block's accumulators (or A)
-constexpr uint32_t kAccCol = 0;                      // accumulator stage c: c*128 + gi*64
-constexpr uint32_t kACol = kAccStages * kBlkCols;    // A stage a: kACol + a*128 + gi*64
-static_assert(kACol + kAStages * kBlkCols <= kTmemCols, "tensor memory overflow");
-static_assert(kAStages == kAccStages, "mma_ready pairs A stage b % 2 with accumulator stage b % 2");
+constexpr uint32_t kAccCols = kNB;                   // 128 per group
+constexpr uint32_t kACols = kGroup / 4;              // 32 per group: four e4m3 per column
+constexpr uint32_t kAccCol = 0;                      // accumulator stage s: s * 128
+constexpr uint32_t kACol = kStages * kAccCols;       // A stage s: kACol + s * 32
+constexpr uint32_t kASumCol = kACol + kStages * kACols;   // constant A of the sum MMA (16)
+static_assert(kASumCol + 16 <= kTmemCols, "tensor memory overflow");
+// A of the sum MMA, k = 0..3 of every row: e4m3 -2^-9, -2^-5, -2^-1, -2^3.
+constexpr uint32_t kASumWord = 0xD0B09081u;
 
-// B operands in UMMA canonical K-major layout without swizzle: a core matrix
-// is 8 rows x 8 f16 (16 bytes each) stored as 128 contiguous bytes; LBO = 128
-// (next 8 k). Main tile: 64 tokens x 128 k, SBO = 2048 (next 8 tokens).
-// Correction tile: 64 tokens x 16 k, SBO = 256. The constant correction A
-// operand (128 rows x 16 k) uses the layout of the correction tile.
+// B operand per (token tile, group) in UMMA canonical K-major layout without
+// swizzle: 128 rows (row n < 64: lo of token n; row 64 + n: 16 * hi of token
+// n) x 128 k, one byte each. A core matrix is 8 rows x 16 bytes stored as 128
+// contiguous bytes; LBO = 128 (next 16 k), SBO = 1024 (next 8 rows). The MMA
+// for k = 32 kk.. starts kk * 256 bytes in.
 constexpr uint32_t kLBO = 128;
-constexpr uint32_t kSBO = 16 * 128;
-constexpr uint32_t kSBOc = 2 * 128;
-constexpr int kBMain = kN * kGroup * 2;                // 16384
-constexpr int kBCorr = kN * 16 * 2;                    // 2048
-constexpr int kBTile = kBMain + kBCorr;                // per (token tile, group)
-constexpr int kACorrBytes = kM * 16 * 2;               // 4096
-constexpr float kProdScale = 32768.0f;                 // products carry 2^-15
-constexpr int kDxBytes = kN * 4;                       // scales of one block, 64 tokens
+constexpr uint32_t kSBO = 8 * 128;
+constexpr int kBTile = kNB * kGroup;                   // 16384
+// B of the sum MMA per group stage: 128 rows x 32 k, the digits of row n < 64
+// at k = 0..3, zeros elsewhere; LBO = 128, SBO = 256.
+constexpr uint32_t kSBOs = 2 * 128;
+constexpr int kBSumBytes = kNB * kK;                   // 4096
+constexpr float kProdScale = 512.0f;                   // products carry 2^-9
+// per (token tile, block): d_x of 64 tokens (f32), then per group the four
+// e4m3 digits of each token's sum as one 32-bit word
+constexpr int kSumOff = kN;                            // words
+constexpr int kDxFloats = kN + kGPB * kN;              // 192
+constexpr int kDxBytes = kDxFloats * 4;                // 768
 // one staged slot: the block's B tiles, its weight tiles (per 32-row tile both
-// groups, adjacent), its block scales
+// groups, adjacent), its scales and sums
 constexpr int kInB = 0;
 constexpr int kInW = kGPB * kBTile;
 constexpr int kWRun = kGPB * kTileBytes;               // one 32-row tile, both groups
 constexpr int kInDx = kInW + kTilesPerCta * kWRun;
 constexpr int kInBytes = kInDx + kDxBytes;
-static_assert(kInBytes % 16 == 0 && kWRun % 16 == 0, "bulk copies need 16-byte multiples");
-constexpr int kSmemUsed = kInStages * kInBytes + kACorrBytes +
-                          kScaleStages * (kGPB * kM + kN) * 4 +
-                          (2 * kInStages + 2 * kAStages + kAccStages) * 8 + 16;
+static_assert(kInBytes % 16 == 0 && kWRun % 16 == 0 && kInW % 16 == 0,
+              "bulk copies need 16-byte multiples");
+// scale ring stage: d_w * 2^9 per group and row, then the block's d_x
+constexpr int kScaleFloats = kGPB * kM + kN;
+constexpr int kNumBars = 2 * kInStages + 3 * kStages;
+constexpr int kSmemUsed = kInStages * kInBytes + kStages * kBSumBytes +
+                          kScaleStages * kScaleFloats * 4 + kNumBars * 8 + 16;
 // Enough shared memory that only one CTA fits on an SM: each CTA allocates
 // all 512 tensor-memory columns.
 constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
-constexpr uint32_t kIdesc = idesc_f16(kM, kN);
+constexpr uint32_t kIdesc = idesc_e4m3(kM, kNB);
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 struct Layout {
   int64_t ntile;      // 64-token tiles
-  int64_t b_bytes;    // ntile * G * 18 KB
-  int64_t dx_bytes;   // ntile * nblk * 64 * 4
+  int64_t b_bytes;    // ntile * G * 16 KB
+  int64_t dx_bytes;   // ntile * nblk * 768
 };
 
 __host__ __device__ inline Layout ws_layout(int64_t cols, int64_t ntok) {
@@ -116,21 +141,29 @@ __host__ __device__ inline Layout ws_layout(int64_t cols, int64_t ntok) {
 
 // ---------------------------------------------------------------- pre-pass
 
-// f16x2 bits of 2^(9 - 2s), s = 0..3: the activation scale matching slot s.
-__device__ __forceinline__ uint32_t slot_scale(int s) {
-  return s == 0 ? 0x60006000u : s == 1 ? 0x58005800u : s == 2 ? 0x50005000u : 0x48004800u;
+// Two e4m3 bytes (x in the low byte); the values passed are exact in e4m3.
+__device__ __forceinline__ uint32_t e4m3x2(float x, float y) {
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(x, y), __NV_SATFINITE, __NV_E4M3);
 }
 
-__device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
+// Four int8 activations (bytes of v, k = 4j..) -> their lo and 16 * hi parts
+// as e4m3 bytes, both multiplied by m (1 or 1/4).
+__device__ __forceinline__ void split_e4m3(uint32_t v, float m, uint32_t& lo, uint32_t& hi) {
+  float l[4], h[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int q = (int)(int8_t)(v >> (8 * j));
+    l[j] = (float)(q & 15) * m;
+    h[j] = (float)((q >> 4) * 16) * m;
+  }
+  lo = e4m3x2(l[0], l[1]) | (e4m3x2(l[2], l[3]) << 16);
+  hi = e4m3x2(h[0], h[1]) | (e4m3x2(h[2], h[3]) << 16);
 }
 
-// One CTA per (group g, token tile): thread t converts token t % 64, k quarter
-// t / 64 (32 activations, scaled by 2^(9 - 2s)) and writes them as 4 core-
-// matrix rows of 16 bytes; the k-quarter-0 threads also write the token's
-// correction row and (for even g) its block scale.
+// One CTA per (group g, token tile): thread t takes token t % 64 and k
+// quarter t / 64 (32 activations) and writes two 16-byte core-matrix rows of
+// the low part and two of the high part; the k-quarter-0 threads also write
+// the token's group sum and (for even g) its block scale.
 __global__ void __launch_bounds__(256) act_pack_kernel(const uint8_t* __restrict__ Xq,
                                                        uint8_t* __restrict__ Bt,
                                                        float* __restrict__ Dx, int64_t ntok,
@@ -153,7 +186,7 @@ __global__ void __launch_bounds__(256) act_pack_kernel(const uint8_t* __restrict
     d = __ldg(reinterpret_cast<const float*>(blk));
     if (kq == 0) {
       // bsums: 16 int16 after the 256 values, 16 activations each
-      const int16_t* bs = reinterpret_cast<const int16_t*>(blk + kQ8KQsOffset + kQK);
+      const int16_t* bs = reinterpret_cast<const int16_t*>(blk + kQ8KBsumsOffset);
 #pragma unroll
       for (int i = 0; i < 8; ++i) sq += __ldg(bs + (g & 1) * 8 + i);
     }
@@ -162,29 +195,27 @@ __global__ void __launch_bounds__(256) act_pack_kernel(const uint8_t* __restrict
     for (int i = 0; i < 8; ++i) q[i] = 0u;   // padded tokens: zero activations, zero scale
   }
   uint8_t* tile = Bt + (nt * ngroups + g) * kBTile;
-  uint8_t* row = tile + (n >> 3) * kSBO + (n & 7) * 16;
+  uint8_t* row_lo = tile + (n >> 3) * kSBO + (n & 7) * 16;
+  uint8_t* row_hi = tile + ((kN + n) >> 3) * kSBO + (n & 7) * 16;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    // words 2c, 2c+1: k = kq*32 + 8c + 0..7, slots s = (2c) % 4 and (2c + 1) % 4
-    uint4 h;
-    s8x4_to_h2x2(q[2 * c], h.x, h.y);
-    s8x4_to_h2x2(q[2 * c + 1], h.z, h.w);
-    const uint32_t m0 = slot_scale((2 * c) & 3), m1 = slot_scale((2 * c + 1) & 3);
-    h.x = h2_mul(h.x, m0);
-    h.y = h2_mul(h.y, m0);
-    h.z = h2_mul(h.z, m1);
-    h.w = h2_mul(h.w, m1);
-    *reinterpret_cast<uint4*>(row + (kq * 4 + c) * kLBO) = h;
+  for (int c = 0; c < 2; ++c) {
+    // words 4c..4c+3: k = kq*32 + 16c + 4w' + j; the A bytes of odd words
+    // (bit 2 of k set) carry the factor 4, so those activations take 1/4
+    uint4 lo, hi;
+    split_e4m3(q[4 * c + 0], 1.0f, lo.x, hi.x);
+    split_e4m3(q[4 * c + 1], 0.25f, lo.y, hi.y);
+    split_e4m3(q[4 * c + 2], 1.0f, lo.z, hi.z);
+    split_e4m3(q[4 * c + 3], 0.25f, lo.w, hi.w);
+    *reinterpret_cast<uint4*>(row_lo + (kq * 2 + c) * kLBO) = lo;
+    *reinterpret_cast<uint4*>(row_hi + (kq * 2 + c) * kLBO) = hi;
   }
   if (kq == 0) {
-    // correction row: k0 = hi, k1 = lo with sq = 64 * hi + lo, 0 <= lo < 64
-    const int hi = sq >> 6, lo = sq & 63;
-    const uint32_t w0 = (uint32_t)__half_as_ushort(__int2half_rn(hi)) |
-                        ((uint32_t)__half_as_ushort(__int2half_rn(lo)) << 16);
-    uint8_t* crow = tile + kBMain + (n >> 3) * kSBOc + (n & 7) * 16;
-    *reinterpret_cast<uint4*>(crow) = make_uint4(w0, 0u, 0u, 0u);
-    *reinterpret_cast<uint4*>(crow + kLBO) = make_uint4(0u, 0u, 0u, 0u);
-    if ((g & 1) == 0) Dx[(nt * nblk + (g >> 1)) * kN + n] = d;
+    float* rec = Dx + (nt * nblk + (g >> 1)) * kDxFloats;
+    // sq = d0 + 16 d1 + 256 d2 + 4096 d3, d0..d2 in [0, 15], d3 in [-4, 3]
+    const uint32_t dig = e4m3x2((float)(sq & 15), (float)((sq >> 4) & 15)) |
+                         (e4m3x2((float)((sq >> 8) & 15), (float)(sq >> 12)) << 16);
+    reinterpret_cast<uint32_t*>(rec)[kSumOff + (g & 1) * kN + n] = dig;
+    if ((g & 1) == 0) rec[n] = d;
   }
 }
 
@@ -204,44 +235,39 @@ struct WsArgs {
   int nrb;
 };
 
-// One group's codes (this thread: one row, 64 weights) -> subnormal f16 A
-// values u * 4^s * 2^-24, stored to tensor memory at taddr. Register 8w + 2s + p
-// holds weights 16w + 4s + 2p and +1 (k local to this half), the pairs the
-// MMA reads from that column.
+// One group's codes (this thread: one row, the 64 weights of one k half) ->
+// 16 A columns of e4m3 bytes. Code word w holds weights 16w + 4s + j (k local
+// to the half) in byte j at bits 2s; column 4w + s takes the four weights of
+// slot s, k = 16w + 4s + 0..3, as bytes 0..3.
 __device__ __forceinline__ void convert_store(const uint4 codes, uint32_t taddr) {
-  uint32_t wa[32];
+  uint32_t wa[16];
   const uint32_t wv[4] = {codes.x, codes.y, codes.z, codes.w};
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
-    // word w: weights 16w + 4s + j in byte j at bits 2s
-    const uint32_t x01 = __byte_perm(wv[w], 0, 0x4140);
-    const uint32_t x23 = __byte_perm(wv[w], 0, 0x4342);
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      wa[8 * w + 2 * s + 0] = x01 & (0x00030003u << (2 * s));
-      wa[8 * w + 2 * s + 1] = x23 & (0x00030003u << (2 * s));
-    }
+    const uint32_t x = wv[w], x4 = wv[w] >> 4;
+    wa[4 * w + 0] = x & 0x03030303u;    // u * 2^-9
+    wa[4 * w + 1] = x & 0x0c0c0c0cu;    // u * 4 * 2^-9
+    wa[4 * w + 2] = x4 & 0x03030303u;
+    wa[4 * w + 3] = x4 & 0x0c0c0c0cu;
   }
-  tmem_st32(taddr, wa);
+  tmem_st16(taddr, wa);
 }
 
 template <bool kGroupSums>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sIn = smem;                                                         // [in][slot]
-  uint8_t* sAc = smem + kInStages * kInBytes;                                  // [4096]
-  float* sdw = reinterpret_cast<float*>(sAc + kACorrBytes);                    // [scale][2][128]
-  float* sdx = sdw + kScaleStages * kGPB * kM;                                 // [scale][64]
-  uint64_t* in_full = reinterpret_cast<uint64_t*>(sdx + kScaleStages * kN);    // [in]
+  uint8_t* sBSum = smem + kInStages * kInBytes;                                // [stage][4096]
+  float* sScale = reinterpret_cast<float*>(sBSum + kStages * kBSumBytes);      // [scale][320]
+  uint64_t* in_full = reinterpret_cast<uint64_t*>(sScale + kScaleStages * kScaleFloats);  // [in]
   uint64_t* in_empty = in_full + kInStages;                                    // [in]
-  // mma_ready[s]: the MMAs of block b (stage s = b % 2) may go: the converters
-  // have written A(b) and the epilogue has read the accumulators of b - 2 (one
-  // barrier, so the issuing thread waits once per block; the epilogue
-  // pre-arrives for blocks 0 and 1).
-  uint64_t* mma_ready = in_empty + kInStages;                                  // [A]
-  uint64_t* a_free = mma_ready + kAStages;                                     // [A]
-  uint64_t* mma_done = a_free + kAStages;                                      // [acc]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + kAccStages);
+  // mma_ready[s]: the MMAs of group g (stage s = g % 3) may go: the converters
+  // have written A(g) and its digits, and the epilogue has read the
+  // accumulator of g - 3 (the epilogue pre-arrives for groups 0..2).
+  uint64_t* mma_ready = in_empty + kInStages;                                  // [stage]
+  uint64_t* a_free = mma_ready + kStages;                                      // [stage]
+  uint64_t* mma_done = a_free + kStages;                                       // [stage]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + kStages);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.ngroups;
@@ -255,13 +281,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
                  ::"r"(smem_u32(tmem_slot)), "r"(kTmemCols) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  if (tid < kM) {
-    // constant correction A: row r, k0 = -2^-9, k1 = -2^-15 (subnormal), rest 0
-    uint8_t* r = sAc + (tid >> 3) * kSBOc + (tid & 7) * 16;
-    *reinterpret_cast<uint4*>(r) = make_uint4(0x82009800u, 0u, 0u, 0u);
-    *reinterpret_cast<uint4*>(r + kLBO) = make_uint4(0u, 0u, 0u, 0u);
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  }
+  // the digit tiles are zero outside k = 0..3 of rows 0..63
+  for (int i = tid; i < kStages * kBSumBytes / 16; i += kThreads)
+    reinterpret_cast<uint4*>(sBSum)[i] = make_uint4(0u, 0u, 0u, 0u);
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   if (tid == 0) {
     // Consumer warps arrive once per warp (lane 0, after __syncwarp).
     for (int i = 0; i < kInStages; ++i) {
@@ -269,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
       // converters have read the slot's weights and scales, the MMAs its B
       mbarrier_init(smem_u32(in_empty + i), kConvWarps + 1);
     }
-    for (int s = 0; s < kAStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbarrier_init(smem_u32(mma_ready + s), kConvWarps + kEpiWarps);
       mbarrier_init(smem_u32(a_free + s), 1);
       mbarrier_init(smem_u32(mma_done + s), 1);
@@ -281,6 +304,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool failed = false;
+  if (warp < 4) {   // constant A of the sum MMA, one warp per lane quarter
+    uint32_t r[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) r[j] = j == 0 ? kASumWord : 0u;
+    tmem_st16(tmem + ((uint32_t)(warp * 32) << 16) + kASumCol, r);
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
 
   if (warp == kProdWarp) {
     // ---------------- producer: stage block j into slot j % kInStages
@@ -307,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
         for (int q = 0; q < nvalid; ++q)
           bulk_copy_g2s(smem_u32(st + kInW + q * kWRun), a.Wtq + ((rb0 + q) * G + g0) * kTileBytes,
                         kWRun, full, policy);
-        bulk_copy_g2s(smem_u32(st + kInDx), a.Dx + (nt * a.nblk + j) * kN, kDxBytes, full,
+        bulk_copy_g2s(smem_u32(st + kInDx), a.Dx + (nt * a.nblk + j) * kDxFloats, kDxBytes, full,
                       policy);
         if (++i == kInStages) { i = 0; ph ^= 1u; }
       }
@@ -316,56 +349,72 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
     // ---------------- converters
     const int q4 = warp & 3, khalf = warp >> 2;          // row quarter, k half of A
     const bool row_ok = rb0 + q4 < a.nrb;
-    const int ct = warp * 32 + lane;                      // 0..255; ct < 64 copies scales
-    const uint32_t a_base = tmem + ((uint32_t)(q4 * 32) << 16) + kACol + (uint32_t)khalf * 32;
-    int i = 0, sa = 0, ss = 0;
+    // ct < 64 copies d_x of token ct; 64 <= ct < 192 the digits of group
+    // (ct - 64) / 64, token ct % 64
+    const int ct = warp * 32 + lane;
+    const uint32_t a_base = tmem + ((uint32_t)(q4 * 32) << 16) + kACol + (uint32_t)khalf * 16;
+    int i = 0, sa = 0, ss = 0, g = 0;
     uint32_t pin = 0, pa = 0;
     for (int b = 0; b < nb; ++b) {
       if (!failed && !mbarrier_wait_bounded(smem_u32(in_full + i), pin, kWaitLimitNs)) failed = true;
       const uint8_t* st = sIn + i * kInBytes;
       const uint8_t* tile = st + kInW + q4 * kWRun;
-      uint4 c0 = make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);  // w = 0
-      uint4 c1 = c0;
-      uint32_t sc0 = 0u, sc1 = 0u;
-      float dx = 0.0f;
+      uint4 cw[kGPB];
+      uint32_t sc[kGPB] = {0u, 0u};
+      uint32_t rec = 0u;                                  // d_x bits or a digit word
+#pragma unroll
+      for (int gi = 0; gi < kGPB; ++gi)
+        cw[gi] = make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);  // w = 0
       if (!failed) {
         if (row_ok) {
-          c0 = *reinterpret_cast<const uint4*>(tile + khalf * 512 + lane * 16);
-          c1 = *reinterpret_cast<const uint4*>(tile + kTileBytes + khalf * 512 + lane * 16);
-          if (khalf == 0) {
-            sc0 = *reinterpret_cast<const uint16_t*>(tile + kTileCodeBytes + lane * 2);
-            sc1 = *reinterpret_cast<const uint16_t*>(tile + kTileBytes + kTileCodeBytes + lane * 2);
+#pragma unroll
+          for (int gi = 0; gi < kGPB; ++gi) {
+            cw[gi] = *reinterpret_cast<const uint4*>(tile + gi * kTileBytes + khalf * 512 + lane * 16);
+            if (khalf == 0)
+              sc[gi] = *reinterpret_cast<const uint16_t*>(tile + gi * kTileBytes + kTileCodeBytes +
+                                                          lane * 2);
           }
         }
-        if (ct < kN) dx = reinterpret_cast<const float*>(st + kInDx)[ct];
+        if (ct < kDxFloats) rec = reinterpret_cast<const uint32_t*>(st + kInDx)[ct];
       }
       __syncwarp();
       if (lane == 0) mbarrier_arrive(smem_u32(in_empty + i));
       if (++i == kInStages) { i = 0; pin ^= 1u; }
 
-      // A stage sa is free once the MMAs of block b - kAStages have finished
-      if (b >= kAStages && !failed &&
-          !mbarrier_wait_bounded(smem_u32(a_free + sa), pa ^ 1u, kWaitLimitNs))
-        failed = true;
-      failed = __any_sync(0xffffffffu, failed);   // tcgen05.st below is warp-wide
-      tc_fence_after();
-      if (!failed) {
-        const uint32_t ta = a_base + (uint32_t)sa * kBlkCols;
-        convert_store(c0, ta);
-        convert_store(c1, ta + kN);
-        if (khalf == 0) {
-          sdw[(ss * kGPB + 0) * kM + q4 * 32 + lane] =
-              __half2float(__ushort_as_half((unsigned short)sc0)) * kProdScale;
-          sdw[(ss * kGPB + 1) * kM + q4 * 32 + lane] =
-              __half2float(__ushort_as_half((unsigned short)sc1)) * kProdScale;
+#pragma unroll
+      for (int gi = 0; gi < kGPB; ++gi) {
+        // A stage sa is free once the MMAs of group g - kStages have finished
+        if (g >= kStages && !failed &&
+            !mbarrier_wait_bounded(smem_u32(a_free + sa), pa ^ 1u, kWaitLimitNs))
+          failed = true;
+        failed = __any_sync(0xffffffffu, failed);   // tcgen05.st below is warp-wide
+        tc_fence_after();
+        if (!failed) {
+          convert_store(cw[gi], a_base + (uint32_t)sa * kACols);
+          if (ct >= kSumOff + gi * kN && ct < kSumOff + (gi + 1) * kN) {
+            const int n = ct - kSumOff - gi * kN;
+            *reinterpret_cast<uint32_t*>(sBSum + sa * kBSumBytes + (n >> 3) * kSBOs + (n & 7) * 16) =
+                rec;
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          }
+          if (gi == 0) {
+            float* sst = sScale + ss * kScaleFloats;
+            if (khalf == 0) {
+#pragma unroll
+              for (int gj = 0; gj < kGPB; ++gj)
+                sst[gj * kM + q4 * 32 + lane] =
+                    __half2float(__ushort_as_half((unsigned short)sc[gj])) * kProdScale;
+            }
+            if (ct < kN) sst[kGPB * kM + ct] = __uint_as_float(rec);
+          }
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         }
-        if (ct < kN) sdx[ss * kN + ct] = dx;
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbarrier_arrive(smem_u32(mma_ready + sa));
+        if (++sa == kStages) { sa = 0; pa ^= 1u; }
+        ++g;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbarrier_arrive(smem_u32(mma_ready + sa));
-      if (++sa == kAStages) { sa = 0; pa ^= 1u; }
       if (++ss == kScaleStages) ss = 0;
     }
   } else if (warp < kMmaWarp) {
@@ -378,62 +427,62 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
     uint64_t y2[16];                                      // tokens n0 + 2p, +1
 #pragma unroll
     for (int p = 0; p < 16; ++p) y2[p] = 0ull;
-    int c = 0, ss = 0;
-    uint32_t pc = 0;
-    if (lane == 0) {   // both accumulator stages start free (blocks 0 and 1)
-      for (int s = 0; s < kAccStages; ++s) mbarrier_arrive(smem_u32(mma_ready + s));
+    int sa = 0, ss = 0;
+    uint32_t pa = 0;
+    if (lane == 0) {   // all accumulator stages start free (groups 0..kStages-1)
+      for (int s = 0; s < kStages; ++s) mbarrier_arrive(smem_u32(mma_ready + s));
     }
     for (int b = 0; b < nb; ++b) {
-      if (!failed && !mbarrier_wait_bounded(smem_u32(mma_done + c), pc, kWaitLimitNs)) failed = true;
-      failed = __any_sync(0xffffffffu, failed);   // tcgen05.ld below is warp-wide
-      tc_fence_after();
-      if (!failed) {
-        const uint32_t tc0 = acc_base + (uint32_t)c * kBlkCols;
-        if (kGroupSums) {
+      const float* sst = sScale + ss * kScaleFloats;
+      const float4* dx4 = reinterpret_cast<const float4*>(sst + kGPB * kM + n0);
 #pragma unroll
-          for (int gi = 0; gi < kGPB; ++gi) {
-            uint32_t acc[32];
-            tmem_ld32(tc0 + (uint32_t)gi * kN, acc);
-            if (row < a.rows) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const int64_t t = tok0 + n0 + j;
-                if (t < a.ntok)
-                  a.S[(t * a.rows + row) * G + b * kGPB + gi] =
-                      __float2int_rn(__uint_as_float(acc[j]) * kProdScale);
-              }
-            }
-          }
-        } else {
-          const float dw0 = sdw[(ss * kGPB + 0) * kM + q4 * 32 + lane];
-          const float dw1 = sdw[(ss * kGPB + 1) * kM + q4 * 32 + lane];
-          const uint64_t w0 = f2_packf(dw0, dw0), w1 = f2_packf(dw1, dw1);
-          const float4* dx4 = reinterpret_cast<const float4*>(sdx + ss * kN + n0);
+      for (int gi = 0; gi < kGPB; ++gi) {
+        if (!failed && !mbarrier_wait_bounded(smem_u32(mma_done + sa), pa, kWaitLimitNs))
+          failed = true;
+        failed = __any_sync(0xffffffffu, failed);   // tcgen05.ld below is warp-wide
+        tc_fence_after();
+        if (!failed) {
+          const uint32_t tc0 = acc_base + (uint32_t)sa * kAccCols;
+          const float dw = sst[gi * kM + q4 * 32 + lane];
+          const uint64_t w2 = f2_packf(dw, dw);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            uint32_t a0[16], a1[16];
-            tmem_ld16_nowait(tc0 + (uint32_t)h * 16, a0);
-            tmem_ld16_nowait(tc0 + kN + (uint32_t)h * 16, a1);
+            uint32_t lo[16], hi[16];
+            tmem_ld16_nowait(tc0 + (uint32_t)h * 16, lo);
+            tmem_ld16_nowait(tc0 + kN + (uint32_t)h * 16, hi);
             tmem_wait_ld();
 #pragma unroll
             for (int j4 = 0; j4 < 4; ++j4) {
-              const float4 d = dx4[h * 4 + j4];
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
                 const int j = 4 * j4 + 2 * e;             // token pair n0 + 16h + j, +1
-                const uint64_t z = f2_fma(w1, f2_pack(a1[j], a1[j + 1]),
-                                          f2_mul(w0, f2_pack(a0[j], a0[j + 1])));
-                const uint64_t dxp = e == 0 ? f2_packf(d.x, d.y) : f2_packf(d.z, d.w);
-                y2[8 * h + j / 2] = f2_fma(dxp, z, y2[8 * h + j / 2]);
+                // isum * 2^-9 for the two tokens, exact
+                const uint64_t z = f2_add(f2_pack(lo[j], lo[j + 1]), f2_pack(hi[j], hi[j + 1]));
+                if (kGroupSums) {
+                  if (row < a.rows) {
+                    const float2 zz = f2_unpack(z);
+                    const int64_t t = tok0 + n0 + 16 * h + j;
+                    if (t < a.ntok)
+                      a.S[(t * a.rows + row) * G + b * kGPB + gi] =
+                          __float2int_rn(zz.x * kProdScale);
+                    if (t + 1 < a.ntok)
+                      a.S[((t + 1) * a.rows + row) * G + b * kGPB + gi] =
+                          __float2int_rn(zz.y * kProdScale);
+                  }
+                } else {
+                  const float4 d = dx4[h * 4 + j4];
+                  const uint64_t dxp = e == 0 ? f2_packf(d.x, d.y) : f2_packf(d.z, d.w);
+                  y2[8 * h + j / 2] = f2_fma(f2_mul(dxp, w2), z, y2[8 * h + j / 2]);
+                }
               }
             }
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbarrier_arrive(smem_u32(mma_ready + sa));   // for group g + kStages
+        if (++sa == kStages) { sa = 0; pa ^= 1u; }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbarrier_arrive(smem_u32(mma_ready + c));   // for block b + 2
-      if (++c == kAccStages) { c = 0; pc ^= 1u; }
       if (++ss == kScaleStages) ss = 0;
     }
     if (!kGroupSums && !failed && row < a.rows) {
@@ -447,38 +496,36 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
     }
   } else if (lane == 0) {
     // ---------------- MMA issuer
-    const uint64_t ac_desc = smem_desc(smem_u32(sAc), kLBO, kSBOc);
-    int i = 0, sa = 0, c = 0;
+    const uint64_t sd0 = smem_desc(smem_u32(sBSum), kLBO, kSBOs);
+    int i = 0, sa = 0;
     uint32_t pa = 0;
     for (int b = 0; b < nb; ++b) {
-      // A(b) written and the accumulators of block b - 2 read
-      if (!failed && !mbarrier_wait_bounded(smem_u32(mma_ready + sa), pa, kWaitLimitNs)) failed = true;
-      tc_fence_after();
-      if (!failed) {
-        const uint32_t d = tmem + kAccCol + (uint32_t)c * kBlkCols;
-        const uint32_t at = tmem + kACol + (uint32_t)sa * kBlkCols;
-        // Descriptors of this slot, once: the start address field (bits 0-13,
-        // address >> 4) then advances by plain adds, as no address passes 2^18.
-        const uint32_t b0 = smem_u32(sIn + i * kInBytes + kInB);
-        const uint64_t bd0 = smem_desc(b0, kLBO, kSBO);
-        const uint64_t cd0 = smem_desc(b0 + kBMain, kLBO, kSBOc);
+      // Descriptor of this slot's B, once: the start address field (bits 0-13,
+      // address >> 4) then advances by plain adds, as no address passes 2^18.
+      const uint64_t bd0 = smem_desc(smem_u32(sIn + i * kInBytes + kInB), kLBO, kSBO);
 #pragma unroll
-        for (int gi = 0; gi < kGPB; ++gi) {
+      for (int gi = 0; gi < kGPB; ++gi) {
+        // A(g) written and the accumulator of group g - 3 read
+        if (!failed && !mbarrier_wait_bounded(smem_u32(mma_ready + sa), pa, kWaitLimitNs))
+          failed = true;
+        tc_fence_after();
+        if (!failed) {
+          const uint32_t d = tmem + kAccCol + (uint32_t)sa * kAccCols;
+          const uint32_t at = tmem + kACol + (uint32_t)sa * kACols;
 #pragma unroll
-          for (int kk = 0; kk < kGroup / 16; ++kk)
-            mma_f16_tmem_a(d + gi * kN, at + gi * kN + 8 * kk,
-                           bd0 + (uint64_t)((gi * kBTile + kk * 2 * kLBO) >> 4), kIdesc,
-                           kk > 0 ? 1u : 0u);
-          mma_f16_ss(d + gi * kN, ac_desc, cd0 + (uint64_t)((gi * kBTile) >> 4), kIdesc, 1u);
+          for (int kk = 0; kk < kMmaPerGroup; ++kk)
+            mma_e4m3_tmem_a(d, at + (uint32_t)(kK / 4) * kk,
+                            bd0 + (uint64_t)((gi * kBTile + kk * 2 * kLBO) >> 4), kIdesc,
+                            kk > 0 ? 1u : 0u);
+          mma_e4m3_tmem_a(d, tmem + kASumCol, sd0 + (uint64_t)((sa * kBSumBytes) >> 4), kIdesc, 1u);
         }
+        // the commits fire when these MMAs are done (at once if none were issued)
+        mma_commit(smem_u32(mma_done + sa));
+        mma_commit(smem_u32(a_free + sa));
+        if (++sa == kStages) { sa = 0; pa ^= 1u; }
       }
-      // the commits fire when these MMAs are done (at once if none were issued)
-      mma_commit(smem_u32(mma_done + c));
-      mma_commit(smem_u32(a_free + sa));
       mma_commit(smem_u32(in_empty + i));
       if (++i == kInStages) i = 0;
-      if (++sa == kAStages) { sa = 0; pa ^= 1u; }
-      if (++c == kAccStages) c = 0;
     }
   }
 

@@ -243,7 +243,7 @@ cudaError_t launch_gemm_tc(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int3
                            int64_t rows, int64_t cols, int64_t ntok, int* dev_status,
                            cudaStream_t s);
 
-// Tensor-core path with a workspace: an activation pre-pass writes f16 B
+// Tensor-core path with a workspace: an activation pre-pass writes e4m3 B
 // tiles into `ws` (tc_workspace_bytes(cols, ntok) bytes, 16-byte aligned).
 int64_t tc_workspace_bytes(int64_t cols, int64_t ntok);
 cudaError_t launch_gemm_tc_ws(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t* S,

@@ -164,7 +164,7 @@ int tq_matmul_groupsums(const void *Wtq, const void *Xq, int32_t *S, int64_t row
 /*
  * tq_matmul_workspace_bytes -- scratch needed by tq_matmul_ws for this shape:
  * 0 when ntok <= 8 (the GEMV needs none); otherwise
- * ceil(ntok/64) * (cols/128) * 18432 + ceil(ntok/64) * (cols/256) * 256 bytes.
+ * ceil(ntok/64) * (cols/128) * 16384 + ceil(ntok/64) * (cols/256) * 768 bytes.
  * -1 for a bad shape.
  */
 int64_t tq_matmul_workspace_bytes(int64_t rows, int64_t cols, int64_t ntok);
@@ -172,9 +172,10 @@ int64_t tq_matmul_workspace_bytes(int64_t rows, int64_t cols, int64_t ntok);
 /*
  * tq_matmul_ws -- tq_matmul with a caller-provided workspace, the faster form
  * for ntok >= 9: a pre-pass converts the q8_K activations once into the
- * tensor cores' f16 operand layout in the workspace (instead of every
- * 128-row tile of the weights converting them again), then the tensor-core
- * kernel reads them with one bulk copy per 128-weight group. Same results
+ * tensor cores' operand layout in the workspace (each int8 split exactly
+ * into two e4m3 parts, instead of every 128-row tile of the weights
+ * converting them again), then the tensor-core kernel reads them with one
+ * bulk copy per q8_K block. Same results
  * and tolerance as tq_matmul; for ntok <= 8 it is tq_matmul.
  *   workspace  device buffer of at least tq_matmul_workspace_bytes(rows, cols,
  *              ntok) bytes, 16-byte aligned, owned by the caller; its contents
@@ -252,7 +253,7 @@ int tq_matmul_host(const void *Wtq, const float *X_host, float *X, void *Xq, flo
  *   Same arguments, results and errors as tq_matmul_ws, minus the workspace.
  *   Limit: tq_matmul_workspace_bytes(rows, cols, ntok) <= TQ_STATIC_WS_BYTES,
  *   else TQ_ERR_WORKSPACE before anything runs (for example cols = 5120
- *   allows ntok <= 704; ntok <= 8 needs no workspace and has no limit).
+ *   allows ntok <= 768; ntok <= 8 needs no workspace and has no limit).
  *   Set-up: the first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current), which may also load the
  *   library's code for the array onto that device; make that first call

@@ -138,8 +138,8 @@ def test_workspace_bytes(lib):
     # none for the GEMV route; B tiles + block scales per 64-token tile otherwise
     assert lib.tq_matmul_workspace_bytes(32768, 8192, 1) == 0
     assert lib.tq_matmul_workspace_bytes(17408, 5120, 8) == 0
-    assert lib.tq_matmul_workspace_bytes(17408, 5120, 64) == 40 * 18432 + 20 * 256
-    assert lib.tq_matmul_workspace_bytes(100, 512, 65) == 2 * (4 * 18432 + 2 * 256)
+    assert lib.tq_matmul_workspace_bytes(17408, 5120, 64) == 40 * 16384 + 20 * 768
+    assert lib.tq_matmul_workspace_bytes(100, 512, 65) == 2 * (4 * 16384 + 2 * 768)
     assert lib.tq_matmul_workspace_bytes(0, 512, 65) == 0
     assert lib.tq_matmul_workspace_bytes(32, 300, 9) == -1
     assert lib.tq_matmul_workspace_bytes(-1, 512, 9) == -1
