@@ -536,7 +536,7 @@ def profile_traffic(summary_name, files, launch_bytes_key="dram_bytes_per_launch
         return None
 
 
-GEMV_FILES = ("tq_gemv.cu", "tq_internal.cuh")
+GEMV_FILES = ("tq_gemv.cu", "tq_tcgen05.cuh", "tq_internal.cuh")
 TC_FILES = ("tq_gemm_tc_ws.cu", "tq_tcgen05.cuh", "tq_internal.cuh")
 
 

@@ -45,8 +45,6 @@
 // 4 KB of shared memory for the digits). The MMAs of group g wait on a single
 // barrier: the converters have written A(g) and the digits of g, and the
 // epilogue has read the accumulator of g - 3.
-#include <cuda_fp8.h>
-
 #include "tq_tcgen05.cuh"
 
 namespace tq {
@@ -140,25 +138,6 @@ __host__ __device__ inline Layout ws_layout(int64_t cols, int64_t ntok) {
 }
 
 // ---------------------------------------------------------------- pre-pass
-
-// Two e4m3 bytes (x in the low byte); the values passed are exact in e4m3.
-__device__ __forceinline__ uint32_t e4m3x2(float x, float y) {
-  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(x, y), __NV_SATFINITE, __NV_E4M3);
-}
-
-// Four int8 activations (bytes of v, k = 4j..) -> their lo and 16 * hi parts
-// as e4m3 bytes, both multiplied by m (1 or 1/4).
-__device__ __forceinline__ void split_e4m3(uint32_t v, float m, uint32_t& lo, uint32_t& hi) {
-  float l[4], h[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int q = (int)(int8_t)(v >> (8 * j));
-    l[j] = (float)(q & 15) * m;
-    h[j] = (float)((q >> 4) * 16) * m;
-  }
-  lo = e4m3x2(l[0], l[1]) | (e4m3x2(l[2], l[3]) << 16);
-  hi = e4m3x2(h[0], h[1]) | (e4m3x2(h[2], h[3]) << 16);
-}
 
 // One CTA per (group g, token tile): thread t takes token t % 64 and k
 // quarter t / 64 (32 activations) and writes two 16-byte core-matrix rows of

@@ -3,6 +3,8 @@
 // tensor-core kernels. Internal to the library.
 #pragma once
 
+#include <cuda_fp8.h>
+
 #include "tq_internal.cuh"
 
 namespace tq {
@@ -112,6 +114,37 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
         "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
+}
+
+// ---------------------------------------------------------------- e4m3 operands
+//
+// The e4m3 paths split an int8 activation q exactly into lo = q & 15 (0..15)
+// and 16 * hi with hi = q >> 4 (-8..7); both parts, and both divided by 4,
+// have at most four significant bits, so they are exact in e4m3. A weight
+// code u at bits 2s..2s+1 of a byte, masked in place, is the e4m3 byte of
+// u * 2^-9 (s = 0) or u * 4 * 2^-9 (s = 1; u = 2 sets the lowest exponent
+// bit, 2^-6); after a right shift by 4 the same holds for s = 2, 3. Where A
+// carries the factor 4 (odd s) the activation part is divided by 4, so every
+// product is u * lo * 2^-9 or u * 16 hi * 2^-9 exactly, and f32 sums of up
+// to 2^15 such products are exact.
+
+// Two e4m3 bytes (x in the low byte); the values passed are exact in e4m3.
+__device__ __forceinline__ uint32_t e4m3x2(float x, float y) {
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(x, y), __NV_SATFINITE, __NV_E4M3);
+}
+
+// Four int8 activations (bytes of v) -> their lo and 16 * hi parts as e4m3
+// bytes, both multiplied by m (1 or 1/4).
+__device__ __forceinline__ void split_e4m3(uint32_t v, float m, uint32_t& lo, uint32_t& hi) {
+  float l[4], h[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int q = (int)(int8_t)(v >> (8 * j));
+    l[j] = (float)(q & 15) * m;
+    h[j] = (float)((q >> 4) * 16) * m;
+  }
+  lo = e4m3x2(l[0], l[1]) | (e4m3x2(l[2], l[3]) << 16);
+  hi = e4m3x2(h[0], h[1]) | (e4m3x2(h[2], h[3]) << 16);
 }
 
 // Codes of slot s (bits 2s..2s+1 of two bytes, placed in the low byte of each
