@@ -278,6 +278,18 @@ int tq_quantize_matmul(const void* Wtq, const float* X, void* Xq, float* Y, int6
     }
     // activations too large for the GEMV's shared memory: the separate calls
   }
+  if (need > 0) {
+    // one kernel quantizes and packs the workspace, then the tensor-core kernel
+    int* status = nullptr;
+    cudaError_t e = device_status_ptr(&status);
+    if (e != cudaSuccess) return fail_cuda(e);
+    note_op(s, kOpOther);
+    e = launch_quantize_gemm_tc_ws(X, static_cast<uint8_t*>(Xq), static_cast<const uint8_t*>(Wtq),
+                                   Y, rows, cols, ntok, static_cast<uint8_t*>(workspace), status, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    note_op(s, kOpMatmul);
+    return TQ_OK;
+  }
   int rc = tq_quantize_q8K(X, Xq, ntok, cols, stream);
   if (rc != TQ_OK) return rc;
   rc = tq_matmul_ws(Wtq, Xq, Y, rows, cols, ntok, workspace, workspace_bytes, stream);

@@ -139,6 +139,13 @@ __host__ __device__ inline Layout ws_layout(int64_t cols, int64_t ntok) {
 
 // ---------------------------------------------------------------- pre-pass
 
+// A group's activation sum as the four e4m3 digits the sum MMA reads: sq = d0 + 16 d1 + 256 d2 + 4096 d3, d0..d2 in [0, 15], d3 in
+// [-4, 3].
+__device__ __forceinline__ uint32_t sum_digits(int sq) {
+  return e4m3x2((float)(sq & 15), (float)((sq >> 4) & 15)) |
+         (e4m3x2((float)((sq >> 8) & 15), (float)(sq >> 12)) << 16);
+}
+
 // One CTA per (group g, token tile): thread t takes token t % 64 and k
 // quarter t / 64 (32 activations) and writes two 16-byte core-matrix rows of
 // the low part and two of the high part; the k-quarter-0 threads also write
@@ -190,12 +197,57 @@ __global__ void __launch_bounds__(256) act_pack_kernel(const uint8_t* __restrict
   }
   if (kq == 0) {
     float* rec = Dx + (nt * nblk + (g >> 1)) * kDxFloats;
-    // sq = d0 + 16 d1 + 256 d2 + 4096 d3, d0..d2 in [0, 15], d3 in [-4, 3]
-    const uint32_t dig = e4m3x2((float)(sq & 15), (float)((sq >> 4) & 15)) |
-                         (e4m3x2((float)((sq >> 8) & 15), (float)(sq >> 12)) << 16);
-    reinterpret_cast<uint32_t*>(rec)[kSumOff + (g & 1) * kN + n] = dig;
+    reinterpret_cast<uint32_t*>(rec)[kSumOff + (g & 1) * kN + n] = sum_digits(sq);
     if ((g & 1) == 0) rec[n] = d;
   }
+}
+
+// Fused form of the quantizer and the pre-pass (tq_quantize_matmul): one warp
+// per (token slot, q8_K block) quantizes the f32 activations exactly as the
+// quantizer kernel does (q8K_warp), writes the q8_K block, and writes the
+// token's e4m3 rows of both groups' B tiles, the group sums' digits and the
+// block scale. Token slots past ntok (the last tile's padding) get zeros.
+// Lane l holds values 8l .. 8l + 7: group l / 16, k = 8 (l % 16) .. + 7 of it,
+// bit 2 of k clear for the first four and set for the last four.
+constexpr int kPackWarps = 8;
+
+__global__ void __launch_bounds__(kPackWarps * 32) quantize_pack_kernel(
+    const float* __restrict__ X, uint8_t* __restrict__ Xq, uint8_t* __restrict__ Bt,
+    float* __restrict__ Dx, int64_t ntok, int ngroups, int nblk, int64_t nslots) {
+  pdl_launch_dependents();
+  // the workspace and Xq may still be read by the previous kernel in the stream
+  pdl_wait_primary();
+  const int lane = threadIdx.x & 31;
+  const int64_t w = (int64_t)blockIdx.x * kPackWarps + (threadIdx.x >> 5);
+  if (w >= nslots * nblk) return;   // whole warp leaves together
+  const int64_t tok = w / nblk;
+  const int b = (int)(w - tok * nblk);
+  uint32_t w0 = 0u, w1 = 0u;
+  int s8 = 0;
+  float d = 0.0f;
+  if (tok < ntok) {
+    const float4* src = reinterpret_cast<const float4*>(X + (tok * nblk + b) * kQK) + 2 * lane;
+    q8K_warp(__ldg(src), __ldg(src + 1), w0, w1, s8, d);
+    q8K_store(Xq + (tok * nblk + b) * kQ8KBytes, lane, w0, w1, s8, d);
+  }
+  // group sums: the 16 lanes of each half-warp
+  int sq = s8;
+  sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+  sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+  sq += __shfl_xor_sync(0xffffffffu, sq, 4);
+  sq += __shfl_xor_sync(0xffffffffu, sq, 8);
+  const int64_t nt = tok / kN;
+  const int n = (int)(tok - nt * kN), gi = lane >> 4, kl = 8 * (lane & 15);
+  uint8_t* tile = Bt + (nt * ngroups + 2 * b + gi) * kBTile;
+  uint32_t l0, h0, l1, h1;
+  split_e4m3(w0, 1.0f, l0, h0);
+  split_e4m3(w1, 0.25f, l1, h1);
+  const int off = (kl >> 4) * kLBO + (kl & 15);
+  *reinterpret_cast<uint2*>(tile + (n >> 3) * kSBO + (n & 7) * 16 + off) = make_uint2(l0, l1);
+  *reinterpret_cast<uint2*>(tile + ((kN + n) >> 3) * kSBO + (n & 7) * 16 + off) = make_uint2(h0, h1);
+  uint32_t* rec = reinterpret_cast<uint32_t*>(Dx + (nt * nblk + b) * kDxFloats);
+  if ((lane & 15) == 0) rec[kSumOff + gi * kN + n] = sum_digits(sq);
+  if (lane == 0) rec[n] = __float_as_uint(d);
 }
 
 // ---------------------------------------------------------------- tensor cores
@@ -533,19 +585,16 @@ int64_t tc_workspace_bytes(int64_t cols, int64_t ntok) {
   return l.b_bytes + l.dx_bytes;
 }
 
-cudaError_t launch_gemm_tc_ws(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t* S,
-                              int64_t rows, int64_t cols, int64_t ntok, uint8_t* ws,
-                              int* dev_status, cudaStream_t s) {
-  if (rows <= 0 || ntok <= 0 || cols <= 0) return cudaSuccess;
+namespace {
+
+// The tensor-core kernel over a workspace already packed.
+cudaError_t launch_main(const uint8_t* Wtq, float* Y, int32_t* S, int64_t rows, int64_t cols,
+                        int64_t ntok, uint8_t* ws, int* dev_status, cudaStream_t s) {
   const Layout l = ws_layout(cols, ntok);
   const int G = (int)(cols / kGroup), nblk = (int)(cols / kQK);
-  if (l.ntile > 65535) return cudaErrorInvalidConfiguration;
   uint8_t* Bt = ws;
   float* Dx = reinterpret_cast<float*>(ws + l.b_bytes);
-  cudaError_t e = launch_pdl(act_pack_kernel, dim3((unsigned)G, (unsigned)l.ntile), dim3(256), 0,
-                             s, Xq, Bt, Dx, ntok, G, nblk);
-  if (e != cudaSuccess) return e;
-
+  cudaError_t e;
   WsArgs a;
   a.Wtq = Wtq;
   a.Bt = Bt;
@@ -569,6 +618,38 @@ cudaError_t launch_gemm_tc_ws(const uint8_t* Wtq, const uint8_t* Xq, float* Y, i
   e = ensure_dynamic_smem(reinterpret_cast<const void*>(&gemm_tc_ws_kernel<false>), kSmemBytes);
   if (e != cudaSuccess) return e;
   return launch_pdl(gemm_tc_ws_kernel<false>, grid, dim3(kThreads), kSmemBytes, s, a);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc_ws(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t* S,
+                              int64_t rows, int64_t cols, int64_t ntok, uint8_t* ws,
+                              int* dev_status, cudaStream_t s) {
+  if (rows <= 0 || ntok <= 0 || cols <= 0) return cudaSuccess;
+  const Layout l = ws_layout(cols, ntok);
+  const int G = (int)(cols / kGroup), nblk = (int)(cols / kQK);
+  if (l.ntile > 65535) return cudaErrorInvalidConfiguration;
+  cudaError_t e = launch_pdl(act_pack_kernel, dim3((unsigned)G, (unsigned)l.ntile), dim3(256), 0,
+                             s, Xq, ws, reinterpret_cast<float*>(ws + l.b_bytes), ntok, G, nblk);
+  if (e != cudaSuccess) return e;
+  return launch_main(Wtq, Y, S, rows, cols, ntok, ws, dev_status, s);
+}
+
+cudaError_t launch_quantize_gemm_tc_ws(const float* X, uint8_t* Xq, const uint8_t* Wtq, float* Y,
+                                       int64_t rows, int64_t cols, int64_t ntok, uint8_t* ws,
+                                       int* dev_status, cudaStream_t s) {
+  if (rows <= 0 || ntok <= 0 || cols <= 0) return cudaSuccess;
+  const Layout l = ws_layout(cols, ntok);
+  const int nblk = (int)(cols / kQK);
+  if (l.ntile > 65535) return cudaErrorInvalidConfiguration;
+  const int64_t warps = l.ntile * kN * nblk;
+  const int64_t grid = (warps + kPackWarps - 1) / kPackWarps;
+  if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  cudaError_t e = launch_pdl(quantize_pack_kernel, dim3((unsigned)grid), dim3(kPackWarps * 32), 0,
+                             s, X, Xq, ws, reinterpret_cast<float*>(ws + l.b_bytes), ntok,
+                             (int)(cols / kGroup), nblk, l.ntile * kN);
+  if (e != cudaSuccess) return e;
+  return launch_main(Wtq, Y, nullptr, rows, cols, ntok, ws, dev_status, s);
 }
 
 }  // namespace tq

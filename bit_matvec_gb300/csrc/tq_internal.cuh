@@ -249,6 +249,11 @@ int64_t tc_workspace_bytes(int64_t cols, int64_t ntok);
 cudaError_t launch_gemm_tc_ws(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t* S,
                               int64_t rows, int64_t cols, int64_t ntok, uint8_t* ws,
                               int* dev_status, cudaStream_t s);
+// The same from f32 activations: one kernel quantizes them into Xq (q8_K, as
+// launch_quantize_q8K) and packs the workspace, then the tensor-core kernel.
+cudaError_t launch_quantize_gemm_tc_ws(const float* X, uint8_t* Xq, const uint8_t* Wtq, float* Y,
+                                       int64_t rows, int64_t cols, int64_t ntok, uint8_t* ws,
+                                       int* dev_status, cudaStream_t s);
 
 // Opt a kernel in to `bytes` of dynamic shared memory on the current device
 // (cached per device and kernel).

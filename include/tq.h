@@ -201,8 +201,10 @@ int tq_matmul_groupsums_ws(const void *Wtq, const void *Xq, int32_t *S, int64_t 
  * fused launch: every CTA of the GEMV quantizes X into its shared memory
  * itself (with the quantizer's arithmetic, so Xq and Y carry the bits of the
  * two separate calls), and CTA 0 writes Xq. That removes a launch and the
- * quantizer's place on the critical path of each matmul; larger ntok runs
- * the two calls.
+ * quantizer's place on the critical path of each matmul. For ntok >= 9 one
+ * kernel quantizes X (the same arithmetic), writes Xq and packs the
+ * workspace, which the tensor-core kernel then reads: two launches instead
+ * of three, the same bits.
  *   X  [ntok][cols] f32, 16-byte aligned (as tq_quantize_q8K).
  *   Xq [ntok][cols/256] q8_K, 16-byte aligned: written.
  *   Wtq, Y, workspace, workspace_bytes: as tq_matmul_ws (the workspace is

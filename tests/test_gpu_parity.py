@@ -152,18 +152,23 @@ def test_exact_integer_mode(ntok):
 
 @pytest.mark.parametrize("ntok", [1, 8, 64], ids=lambda t: f"{'tc' if t > 8 else 'gemv'}{t}")
 def test_extremes(ntok):
-    """All u = 2 (w = +1) or all u = 0 against q = +-127: the largest group sums."""
+    """All u = 2 (w = +1) or all u = 0 against q = +-127: the largest group sums,
+    and activation sums of -16256, 0 and +16256 (the e4m3 path splits each q
+    into q & 15 and 16 (q >> 4) and the sum into four base-16 digits; these are
+    the extremes of both), on the plain and the workspace forms."""
     rows, cols = 64, 512
     for code in (0, 2):
         wpq = synth.pack_pq2_0(np.full((rows, cols), code, np.uint8),
                                np.ones((rows, cols // 128), np.float16))
-        x = np.where(np.arange(cols) % 2 == 0, 127.0, -127.0).astype(np.float32)
-        x = np.tile(x, (ntok, 1))
-        x[ntok // 2:] = 127.0
+        alt = np.where(np.arange(cols) % 2 == 0, 127.0, -127.0)
+        pats = [np.full(cols, -127.0), alt, np.full(cols, 127.0)]
+        x = np.stack([pats[t % 3] for t in range(ntok)]).astype(np.float32)
         Wtq, Xq = gpu_repack(wpq, rows, cols), gpu_quantize(x)
-        S = gpu_groupsums(Wtq, Xq, rows, cols, ntok)
-        assert np.array_equal(S, oracle.groupsums(wpq, oracle.quantize_q8K(x), rows, cols))
-        assert np.abs(S).max() == 16256
+        S_ref = oracle.groupsums(wpq, oracle.quantize_q8K(x), rows, cols)
+        for gs in (gpu_groupsums, gpu_groupsums_ws):
+            S = gs(Wtq, Xq, rows, cols, ntok)
+            assert np.array_equal(S, S_ref)
+            assert np.abs(S).max() == 16256
 
 
 def test_empty_and_degenerate():
@@ -201,10 +206,12 @@ def test_deterministic_and_stream():
 
 @pytest.mark.parametrize("rows,cols,ntok", [(300, 1024, 1), (100, 768, 3), (300, 1024, 4),
                                              (64, 8192, 8), (32, 256, 8), (128, 1024, 9),
-                                             (100, 512, 64)])
+                                             (100, 512, 64), (300, 1024, 65), (160, 2048, 130)])
 def test_quantize_matmul_equals_separate_calls(rows, cols, ntok):
     """The fused call gives the bits of tq_quantize_q8K + tq_matmul_ws: Xq and Y
-    (GEMV with in-CTA quantization for ntok <= 8; the two calls above)."""
+    (GEMV with in-CTA quantization for ntok <= 8; above, one kernel that
+    quantizes and packs the workspace, including the zero padding of a
+    ragged last token tile, before the tensor-core kernel)."""
     import bit_matvec_gb300 as tq
     wpq, x = _weights(rows, cols, 5), _acts(ntok, cols, 5)
     Wtq = gpu_repack(wpq, rows, cols)
