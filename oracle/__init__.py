@@ -27,6 +27,7 @@ _LIB = os.path.join(_OUT_DIR, "libtq_ref.so")
 QK_K = 256
 GROUP = 128
 PQ2_BYTES = 34
+PTQ1_BYTES = 28
 Q8K_BYTES = 292
 
 # numpy view of one q8_K block, matching ref_block_q8K
@@ -66,10 +67,17 @@ def _load():
             lib.ref_repacked_bytes.restype = I64
             lib.ref_repack.argtypes = [P, I64, I64, P]
             lib.ref_unrepack.argtypes = [P, I64, I64, P]
+            lib.ref_ptq1_trit.argtypes = [ctypes.c_uint8, ctypes.c_int]
+            lib.ref_ptq1_trit.restype = ctypes.c_int
+            lib.ref_ptq1_byte.argtypes = [P]
+            lib.ref_ptq1_byte.restype = ctypes.c_uint8
+            lib.ref_encode_ptq1_0.argtypes = [P, P, I64, I64, P]
+            lib.ref_ptq1_0_to_pq2_0.argtypes = [P, I64, I64, P]
             lib.ref_groupsums.argtypes = [P, P, I64, I64, I64, P]
             lib.ref_matmul.argtypes = [P, P, I64, I64, I64, P, P]
             for f in ("ref_quantize_q8K", "ref_decode_pq2_0", "ref_repack",
-                      "ref_unrepack", "ref_groupsums", "ref_matmul"):
+                      "ref_unrepack", "ref_groupsums", "ref_matmul", "ref_encode_ptq1_0",
+                      "ref_ptq1_0_to_pq2_0"):
                 getattr(lib, f).restype = None
             _lib = lib
     return _lib
@@ -102,6 +110,39 @@ def decode_pq2_0(wpq: np.ndarray, rows: int, cols: int):
     sb = np.empty((rows, cols // GROUP), dtype=np.uint16)
     _load().ref_decode_pq2_0(_ptr(wpq), rows, cols, _ptr(w), _ptr(sb))
     return w, sb
+
+
+def ptq1_trit(b: int, n: int) -> int:
+    """Trit n (0..4) of a ptq1_0 code byte b: the code u in {0, 1, 2}."""
+    return int(_load().ref_ptq1_trit(b & 0xFF, n))
+
+
+def ptq1_byte(trits) -> int:
+    """The ptq1_0 code byte of five trits (each 0, 1 or 2)."""
+    t = np.ascontiguousarray(np.asarray(trits, dtype=np.int32))
+    assert t.shape == (5,)
+    return int(_load().ref_ptq1_byte(_ptr(t)))
+
+
+def encode_ptq1_0(w: np.ndarray, scale_bits: np.ndarray) -> np.ndarray:
+    """Ternary w int8 [rows][cols] and fp16 scale bits [rows][cols/128] ->
+    flat ptq1_0 bytes (28 per 128 weights)."""
+    w = np.ascontiguousarray(w, dtype=np.int8)
+    rows, cols = w.shape
+    sb = np.ascontiguousarray(scale_bits, dtype=np.uint16)
+    assert cols % GROUP == 0 and sb.shape == (rows, cols // GROUP)
+    out = np.empty(rows * cols // GROUP * PTQ1_BYTES, dtype=np.uint8)
+    _load().ref_encode_ptq1_0(_ptr(w), _ptr(sb), rows, cols, _ptr(out))
+    return out
+
+
+def ptq1_0_to_pq2_0(wpt: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    """ptq1_0 bytes -> pq2_0 bytes of the same weights and scales."""
+    wpt = np.ascontiguousarray(wpt, dtype=np.uint8)
+    assert wpt.size == rows * cols // GROUP * PTQ1_BYTES
+    out = np.empty(rows * cols // GROUP * PQ2_BYTES, dtype=np.uint8)
+    _load().ref_ptq1_0_to_pq2_0(_ptr(wpt), rows, cols, _ptr(out))
+    return out
 
 
 def repacked_bytes(rows: int, cols: int) -> int:

@@ -98,6 +98,65 @@ void ref_decode_pq2_0(const uint8_t *wpq, int64_t rows, int64_t cols,
 }
 
 /*
+ * ptq1_0 (declared with its readings in tq_ref.h). A code byte's trit n is
+ * the page's formula as written: floor(3 * ((b * 3^n) mod 256) / 256).
+ */
+int ref_ptq1_trit(uint8_t b, int n)
+{
+    int p = 1;
+    for (int i = 0; i < n; ++i) p *= 3;
+    const int v = (b * p) % 256;
+    return (3 * v) / 256;
+}
+
+uint8_t ref_ptq1_byte(const int *t)
+{
+    int q = 0;
+    for (int n = 0; n < 5; ++n) q = 3 * q + t[n];   /* sum t_n 3^(4 - n) */
+    return (uint8_t)((256 * q + 242) / 243);         /* ceil(256 q / 243) */
+}
+
+void ref_encode_ptq1_0(const int8_t *w, const uint16_t *scale_bits, int64_t rows,
+                       int64_t cols, uint8_t *wpt)
+{
+    const int64_t ng = cols / REF_GROUP;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t g = 0; g < ng; ++g) {
+            uint8_t *blk = wpt + (r * ng + g) * REF_PTQ1_BYTES;
+            const uint16_t sb = scale_bits[r * ng + g];
+            blk[0] = (uint8_t)(sb & 0xFF);
+            blk[1] = (uint8_t)(sb >> 8);
+            for (int c = 0; c < REF_PTQ1_CODES; ++c) {
+                int t[5];
+                for (int n = 0; n < 5; ++n) {
+                    const int k = 5 * c + n;
+                    t[n] = k < REF_GROUP ? w[r * cols + g * REF_GROUP + k] + 1 : 0;
+                }
+                blk[2 + c] = ref_ptq1_byte(t);
+            }
+        }
+    }
+}
+
+void ref_ptq1_0_to_pq2_0(const uint8_t *wpt, int64_t rows, int64_t cols, uint8_t *wpq)
+{
+    const int64_t ng = cols / REF_GROUP;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t g = 0; g < ng; ++g) {
+            const uint8_t *src = wpt + (r * ng + g) * REF_PTQ1_BYTES;
+            uint8_t *dst = wpq + (r * ng + g) * REF_PQ2_BYTES;
+            memset(dst, 0, REF_PQ2_BYTES);
+            dst[0] = src[0];
+            dst[1] = src[1];
+            for (int k = 0; k < REF_GROUP; ++k) {
+                const int u = ref_ptq1_trit(src[2 + k / 5], k % 5);
+                dst[2 + (k >> 2)] |= (uint8_t)(u << (2 * (k & 3)));
+            }
+        }
+    }
+}
+
+/*
  * The GPU weight layout ("tq"). Same bits as pq2_0, another order:
  *  - rows are taken in blocks of 32 (the last block padded); groups of 128
  *    weights along a row as in pq2_0;

@@ -65,6 +65,34 @@ int64_t ref_repacked_bytes(int64_t rows, int64_t cols);
 void ref_repack(const uint8_t *wpq, int64_t rows, int64_t cols, uint8_t *wtq);
 void ref_unrepack(const uint8_t *wtq, int64_t rows, int64_t cols, uint8_t *wpq);
 
+/*
+ * ptq1_0, the 1.75-bit file ("how i made a 27b ternary model ... faster",
+ * section *the detour that lost*): five weights per byte in base 3, since
+ * 3^5 = 243 fits in 256; weight n of byte b is floor(3 * (b * 3^n mod 256) /
+ * 256), which the page notes equals (v >= 86) + (v >= 171) for
+ * v = b * 3^n mod 256. Readings where the page is silent:
+ *  - block = { uint16 fp16 scale; uint8 codes[26] }, 28 bytes per 128
+ *    weights: 1.75 bits per weight, and 28 / 34 makes the file 18% smaller
+ *    than pq2_0, as the page says;
+ *  - weight k of the block is trit k % 5 of code byte k / 5; the last byte
+ *    holds weights 125..127 as trits 0..2 and zero trits 3 and 4;
+ *  - a trit is the code u = w + 1 in {0, 1, 2}, as in pq2_0;
+ *  - a byte for trits t0..t4 is the smallest b whose trits decode to them:
+ *    b = ceil(256 q / 243) with q = sum_n t_n 3^(4 - n).
+ */
+#define REF_PTQ1_BYTES 28
+#define REF_PTQ1_CODES 26
+
+/* Trit n (0..4) of a ptq1_0 code byte, from the page's formula. */
+int ref_ptq1_trit(uint8_t b, int n);
+/* The code byte of trits t[0..4], each in {0, 1, 2}. */
+uint8_t ref_ptq1_byte(const int *t);
+/* ternary w[rows][cols] (-1, 0, 1) and scale bits -> ptq1_0 blocks. */
+void ref_encode_ptq1_0(const int8_t *w, const uint16_t *scale_bits, int64_t rows,
+                       int64_t cols, uint8_t *wpt);
+/* ptq1_0 -> pq2_0 blocks of the same weights and scales. */
+void ref_ptq1_0_to_pq2_0(const uint8_t *wpt, int64_t rows, int64_t cols, uint8_t *wpq);
+
 /* S[t][r][g] = sum_{k<128} (u[r][128g+k] - 1) * q[t][128g+k]. */
 void ref_groupsums(const uint8_t *wpq, const ref_block_q8K *xq, int64_t rows,
                    int64_t cols, int64_t ntok, int32_t *S);
