@@ -32,6 +32,7 @@ TQ_ERR_WORKSPACE = -7
 QK_K = 256
 GROUP = 128
 PQ2_0_BYTES = 34
+PTQ1_0_BYTES = 28
 Q8K_BYTES = 292
 TILE_ROWS = 32
 TILE_BYTES = 1088
@@ -74,6 +75,8 @@ def _load():
             "tq_repacked_bytes": ([I64, I64], I64),
             "tq_repack": ([P, P, I64, I64, P], I),
             "tq_unrepack": ([P, P, I64, I64, P], I),
+            "tq_ptq1_0_bytes": ([I64, I64], I64),
+            "tq_repack_ptq1_0": ([P, P, I64, I64, P], I),
             "tq_matmul": ([P, P, P, I64, I64, I64, P], I),
             "tq_matmul_groupsums": ([P, P, P, I64, I64, I64, P], I),
             "tq_matmul_workspace_bytes": ([I64, I64, I64], I64),
@@ -163,6 +166,19 @@ def tq_repack(Wpq2: torch.Tensor, Wtq: torch.Tensor, rows: int, cols: int, strea
 def tq_unrepack(Wtq: torch.Tensor, Wpq2: torch.Tensor, rows: int, cols: int, stream=None):
     _call("tq_unrepack", Wtq.device, _ptr(Wtq), _ptr(Wpq2), rows, cols,
           _stream(stream, Wtq.device))
+
+
+def tq_ptq1_0_bytes(rows: int, cols: int) -> int:
+    n = _load().tq_ptq1_0_bytes(rows, cols)
+    if n < 0:
+        raise TQError(TQ_ERR_SHAPE, "tq_ptq1_0_bytes")
+    return int(n)
+
+
+def tq_repack_ptq1_0(Wpt: torch.Tensor, Wtq: torch.Tensor, rows: int, cols: int, stream=None):
+    """ptq1_0 (1.75-bit) weights -> the tq layout, decoded once at load."""
+    _call("tq_repack_ptq1_0", Wpt.device, _ptr(Wpt), _ptr(Wtq), rows, cols,
+          _stream(stream, Wpt.device))
 
 
 def tq_matmul(Wtq: torch.Tensor, Xq: torch.Tensor, Y: torch.Tensor, rows: int, cols: int,

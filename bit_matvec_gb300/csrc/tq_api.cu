@@ -195,6 +195,24 @@ int tq_repack(const void* Wpq2, void* Wtq, int64_t rows, int64_t cols, void* str
   return e == cudaSuccess ? TQ_OK : fail_cuda(e);
 }
 
+int64_t tq_ptq1_0_bytes(int64_t rows, int64_t cols) {
+  if (rows < 0 || cols < 0 || cols % kGroup != 0) return -1;
+  return rows * (cols / kGroup) * kPtq1Bytes;
+}
+
+int tq_repack_ptq1_0(const void* Wpt, void* Wtq, int64_t rows, int64_t cols, void* stream) {
+  if (rows < 0 || cols < 0 || cols % kGroup != 0) return TQ_ERR_SHAPE;
+  if (rows == 0 || cols == 0) return TQ_OK;
+  if (!Wpt || !Wtq) return TQ_ERR_NULL;
+  if (!aligned16(Wpt) || !aligned16(Wtq)) return TQ_ERR_ALIGN;
+  if (overlap(Wpt, tq_ptq1_0_bytes(rows, cols), Wtq, tq_repacked_bytes(rows, cols)))
+    return TQ_ERR_ALIAS;
+  note_op(static_cast<cudaStream_t>(stream), kOpOther);
+  cudaError_t e = launch_repack_ptq1(static_cast<const uint8_t*>(Wpt), static_cast<uint8_t*>(Wtq),
+                                     rows, cols, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TQ_OK : fail_cuda(e);
+}
+
 int tq_unrepack(const void* Wtq, void* Wpq2, int64_t rows, int64_t cols, void* stream) {
   if (rows < 0 || cols < 0 || cols % kGroup != 0) return TQ_ERR_SHAPE;
   if (rows == 0 || cols == 0) return TQ_OK;

@@ -14,6 +14,7 @@ namespace tq {
 constexpr int kQK = TQ_QK_K;             // activations per q8_K block
 constexpr int kGroup = TQ_GROUP;         // weights per scale
 constexpr int kPq2Bytes = TQ_PQ2_0_BYTES;
+constexpr int kPtq1Bytes = TQ_PTQ1_0_BYTES;
 constexpr int kQ8KBytes = TQ_Q8K_BYTES;
 constexpr int kTileRows = TQ_TILE_ROWS;  // rows per tile of the tq layout
 constexpr int kTileBytes = TQ_TILE_BYTES;
@@ -206,6 +207,8 @@ cudaError_t launch_repack(const uint8_t* Wpq2, uint8_t* Wtq, int64_t rows, int64
                           cudaStream_t s);
 cudaError_t launch_unrepack(const uint8_t* Wtq, uint8_t* Wpq2, int64_t rows, int64_t cols,
                             cudaStream_t s);
+cudaError_t launch_repack_ptq1(const uint8_t* Wpt, uint8_t* Wtq, int64_t rows, int64_t cols,
+                               cudaStream_t s);
 
 // Launch with programmatic stream serialization: the kernel may start while
 // the previous kernel in the stream finishes; it must call pdl_wait_primary()

@@ -1,5 +1,6 @@
 // tq_repack.cu -- load-time permutation of pq2_0 weights into the tq layout,
-// and its inverse.
+// its inverse, and the load-time decode of the 1.75-bit ptq1_0 file into the
+// same layout.
 //
 // The ternary post ("the layout") repacks once at model load so that
 // unpacking costs one AND per vector; this is the GPU version of that step,
@@ -79,6 +80,51 @@ unrepack_kernel(const uint8_t* __restrict__ Wtq, uint8_t* __restrict__ Wpq2, int
   }
 }
 
+// ptq1_0 (five weights per code byte in base 3; block = fp16 scale + 26 code
+// bytes, 28 bytes per 128 weights; weight k is trit k % 5 of code byte k / 5)
+// into the tq layout: lane l decodes row l of the tile. Trit n of byte b is
+// floor(3 * (b * 3^n mod 256) / 256) (the ternary post, "the detour that
+// lost"), the code u = w + 1, written where tq_repack puts weight k.
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+repack_ptq1_kernel(const uint8_t* __restrict__ Wpt, uint8_t* __restrict__ Wtq, int64_t rows,
+                   int64_t ngroups, int64_t ntiles) {
+  const int lane = threadIdx.x & 31;
+  const int64_t tile = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  if (tile >= ntiles) return;
+  const int64_t rb = tile / ngroups, g = tile - rb * ngroups;
+  const int64_t r = rb * kTileRows + lane;
+  uint8_t* out = Wtq + tile * kTileBytes;
+
+  uint32_t w[8];
+  uint16_t scale = 0;
+  if (r < rows) {
+    // 28-byte blocks: 4-byte alignment. Byte 2 + c of the block is code byte c.
+    const uint32_t* blk = reinterpret_cast<const uint32_t*>(Wpt + (r * ngroups + g) * kPtq1Bytes);
+    uint32_t bw[kPtq1Bytes / 4];
+#pragma unroll
+    for (int i = 0; i < kPtq1Bytes / 4; ++i) bw[i] = blk[i];
+    scale = (uint16_t)(bw[0] & 0xFFFFu);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = 0u;
+#pragma unroll
+    for (int k = 0; k < kGroup; ++k) {
+      const int c = k / 5, n = k % 5;
+      const uint32_t b = (bw[(2 + c) >> 2] >> (8 * ((2 + c) & 3))) & 0xFFu;
+      const uint32_t p3 = n == 0 ? 1u : n == 1 ? 3u : n == 2 ? 9u : n == 3 ? 27u : 81u;
+      const uint32_t u = (((b * p3) & 0xFFu) * 3u) >> 8;
+      // tq position of weight k: word (k / 64) * 4 + (k % 64) / 16, byte k % 4,
+      // bits 2 * ((k % 16) / 4)
+      w[(k >> 6) * 4 + ((k & 63) >> 4)] |= u << (8 * (k & 3) + 2 * ((k & 15) >> 2));
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = 0x55555555u;  // padding rows: code 1, w = 0
+  }
+  *reinterpret_cast<uint4*>(out + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  *reinterpret_cast<uint4*>(out + 512 + lane * 16) = make_uint4(w[4], w[5], w[6], w[7]);
+  reinterpret_cast<uint16_t*>(out + kTileCodeBytes)[lane] = scale;
+}
+
 int64_t tile_count(int64_t rows, int64_t cols) {
   return (rows + kTileRows - 1) / kTileRows * (cols / kGroup);
 }
@@ -93,6 +139,17 @@ cudaError_t launch_repack(const uint8_t* Wpq2, uint8_t* Wtq, int64_t rows, int64
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
   repack_kernel<<<(unsigned)grid, kWarpsPerCta * 32, 0, s>>>(Wpq2, Wtq, rows, cols / kGroup,
                                                              ntiles);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repack_ptq1(const uint8_t* Wpt, uint8_t* Wtq, int64_t rows, int64_t cols,
+                               cudaStream_t s) {
+  const int64_t ntiles = tile_count(rows, cols);
+  if (ntiles <= 0) return cudaSuccess;
+  const int64_t grid = (ntiles + kWarpsPerCta - 1) / kWarpsPerCta;
+  if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  repack_ptq1_kernel<<<(unsigned)grid, kWarpsPerCta * 32, 0, s>>>(Wpt, Wtq, rows, cols / kGroup,
+                                                                  ntiles);
   return cudaGetLastError();
 }
 

@@ -51,6 +51,7 @@ extern "C" {
 #define TQ_QK_K 256          /* activations per q8_K block */
 #define TQ_GROUP 128         /* weights per pq2_0 scale */
 #define TQ_PQ2_0_BYTES 34    /* bytes per pq2_0 block (fp16 scale + 32 code bytes) */
+#define TQ_PTQ1_0_BYTES 28   /* bytes per ptq1_0 block (fp16 scale + 26 code bytes) */
 #define TQ_Q8K_BYTES 292     /* bytes per q8_K block */
 #define TQ_TILE_ROWS 32      /* rows per tile of the repacked layout */
 #define TQ_TILE_BYTES 1088   /* bytes per tile: 32 rows x 128 weights */
@@ -125,6 +126,31 @@ int tq_repack(const void *Wpq2, void *Wtq, int64_t rows, int64_t cols, void *str
 
 /* tq_unrepack -- the exact inverse of tq_repack (padding rows are dropped). */
 int tq_unrepack(const void *Wtq, void *Wpq2, int64_t rows, int64_t cols, void *stream);
+
+/*
+ * ptq1_0, the 1.75-bit file (post, "the detour that lost"): five ternary
+ * weights per code byte in base 3 (3^5 = 243 fits in 256); trit n of byte b
+ * is floor(3 * (b * 3^n mod 256) / 256) = (v >= 86) + (v >= 171) with
+ * v = b * 3^n mod 256, and a trit is the code u = w + 1. Block (where the
+ * post is silent, our reading): { uint16 fp16 scale; uint8 codes[26] } per
+ * 128 weights of a row, 28 bytes, weight k in trit k % 5 of code byte k / 5;
+ * blocks row-major like pq2_0.
+ *
+ * tq_ptq1_0_bytes -- rows * cols/128 * 28; -1 if cols % 128 != 0 or a size is
+ * negative.
+ *
+ * tq_repack_ptq1_0 -- load-time decode of ptq1_0 weights into the tq layout:
+ * writes exactly the bytes tq_repack writes for the pq2_0 file of the same
+ * weights and scales, so every matmul entry point takes the result. The file
+ * is 18% smaller; the weights stream at 2.125 bits per weight, because base-3
+ * decoding costs several integer operations per weight where the tq layout
+ * needs one AND per four (the post found the same trade on the CPU).
+ *   Wpt [rows][cols/128] ptq1_0 blocks, 16-byte aligned.
+ *   Wtq tq_repacked_bytes(rows, cols) bytes, 16-byte aligned, written.
+ * Errors: as tq_repack.
+ */
+int64_t tq_ptq1_0_bytes(int64_t rows, int64_t cols);
+int tq_repack_ptq1_0(const void *Wpt, void *Wtq, int64_t rows, int64_t cols, void *stream);
 
 /*
  * tq_matmul -- Y = the ternary x q8_K product (definition at the top).

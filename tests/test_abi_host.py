@@ -74,6 +74,10 @@ def test_shape_errors(lib):
     assert lib.tq_quantize_q8K(P(A), P(B), -1, 256, None) == S
     assert lib.tq_repack(P(A), P(B), 32, 100, None) == S
     assert lib.tq_unrepack(P(A), P(B), -3, 256, None) == S
+    assert lib.tq_repack_ptq1_0(P(A), P(B), 32, 100, None) == S
+    assert lib.tq_ptq1_0_bytes(32, 100) == -1
+    assert lib.tq_ptq1_0_bytes(-1, 256) == -1
+    assert lib.tq_ptq1_0_bytes(3, 256) == 3 * 2 * 28
 
 
 def test_empty_calls_are_noops(lib):
@@ -86,6 +90,7 @@ def test_empty_calls_are_noops(lib):
     assert lib.tq_quantize_q8K(None, None, 3, 0, None) == tq.TQ_OK
     assert lib.tq_repack(None, None, 0, 256, None) == tq.TQ_OK
     assert lib.tq_unrepack(None, None, 32, 0, None) == tq.TQ_OK
+    assert lib.tq_repack_ptq1_0(None, None, 0, 256, None) == tq.TQ_OK
 
 
 def test_null_errors(lib):
@@ -100,6 +105,7 @@ def test_null_errors(lib):
     assert lib.tq_quantize_q8K(P(A), None, 1, 256, None) == N
     assert lib.tq_repack(None, P(B), 32, 256, None) == N
     assert lib.tq_unrepack(P(A), None, 32, 256, None) == N
+    assert lib.tq_repack_ptq1_0(None, P(B), 32, 256, None) == N
 
 
 def test_alignment_errors(lib):
@@ -113,6 +119,7 @@ def test_alignment_errors(lib):
     assert lib.tq_quantize_q8K(P(A), P(B + 12), 1, 256, None) == E
     assert lib.tq_repack(P(A + 2), P(B), 32, 256, None) == E
     assert lib.tq_unrepack(P(A), P(B + 8), 32, 256, None) == E
+    assert lib.tq_repack_ptq1_0(P(A + 4), P(B), 32, 256, None) == E
 
 
 def test_alias_errors(lib):
@@ -124,6 +131,7 @@ def test_alias_errors(lib):
     assert lib.tq_quantize_q8K(P(A), P(A + 16), 1, 256, None) == E
     assert lib.tq_repack(P(A), P(A), 32, 256, None) == E                      # in place
     assert lib.tq_unrepack(P(A), P(A + 1088 - 16), 32, 256, None) == E
+    assert lib.tq_repack_ptq1_0(P(A), P(A + 32 * 2 * 28 - 16), 32, 256, None) == E
 
 
 def test_binding_rejects_cpu_tensors(lib):
