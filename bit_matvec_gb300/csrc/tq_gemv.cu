@@ -397,24 +397,36 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
 
 constexpr int kMmaReducers = 8;   // warps that add one of the 8 C positions per lane
 
+// The tensor-core variant's shape: T's warps, and TPW tiles per warp and stage
+// (two, or one where the larger ring and T rows of f16 activations do not fit
+// in shared memory).
+template <int T, int TPW>
+struct MmaCfg {
+  static constexpr int kWarps = Cfg<T>::kWarps;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kTilesPerWarp = TPW;
+  static constexpr int kStageTiles = kWarps * TPW;
+  static constexpr int kStageBytes = kStageTiles * kTileBytes;
+};
+
 struct MmaPlan {
   int64_t ring, bars, counters, sb, sgsum, sdx, red, total;
   int64_t sb_stride;   // bytes per token row of f16 activations (+8: bank spread)
 };
 
-template <int T>
+template <int T, int TPW>
 __host__ __device__ inline MmaPlan plan_mma(int stages, int64_t cols) {
   MmaPlan p;
   const int64_t g = cols / kGroup, b = cols / kQK;
   p.sb_stride = cols * 2 + 8;
   p.ring = 0;
-  p.bars = (int64_t)stages * Cfg<T>::kStageBytes;
+  p.bars = (int64_t)stages * MmaCfg<T, TPW>::kStageBytes;
   p.counters = p.bars + (stages + 4) * 8;
   p.sb = (p.counters + stages * 4 + 15) / 16 * 16;
   p.sgsum = p.sb + T * p.sb_stride;
   p.sdx = p.sgsum + T * g * 4;
   p.red = (p.sdx + T * b * 4 + 15) / 16 * 16;
-  p.total = p.red + (int64_t)2 * Cfg<T>::kWarps * 8 * 32 * 4;
+  p.total = p.red + (int64_t)2 * MmaCfg<T, TPW>::kWarps * 8 * 32 * 4;
   return p;
 }
 
@@ -524,15 +536,16 @@ __device__ __forceinline__ void group_mma(const MmaCodes& m, int g, const uint8_
     }
 }
 
-template <int T, bool kGroupSums>
-__global__ void __launch_bounds__(Cfg<T>::kThreads, 1) gemv_mma_kernel(const GemvArgs a) {
-  constexpr int kConsumers = Cfg<T>::kWarps;
-  constexpr int kStageTiles = Cfg<T>::kStageTiles;
-  constexpr int kStageBytes = Cfg<T>::kStageBytes;
+template <int T, bool kGroupSums, int TPW>
+__global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(const GemvArgs a) {
+  using Mc = MmaCfg<T, TPW>;
+  constexpr int kConsumers = Mc::kWarps;
+  constexpr int kStageTiles = Mc::kStageTiles;
+  constexpr int kStageBytes = Mc::kStageBytes;
   extern __shared__ __align__(128) uint8_t smem[];
   const int S = a.stages;
   const int cols = a.ngroups * kGroup;
-  const MmaPlan pl = plan_mma<T>(S, cols);
+  const MmaPlan pl = plan_mma<T, TPW>(S, cols);
   uint8_t* ring = smem + pl.ring;                                 // [S][stage]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + pl.bars);  // [S]
   uint64_t* redfull = full + S;                                   // [2]
@@ -633,9 +646,9 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1) gemv_mma_kernel(const Gem
         failed = true;
       failed = __any_sync(0xffffffffu, failed);   // mma.sync below is warp-wide
       const uint8_t* stage = ring + (size_t)slot * kStageBytes;
-      MmaCodes mc[Cfg<T>::kTilesPerWarp];
+      MmaCodes mc[Mc::kTilesPerWarp];
 #pragma unroll
-      for (int u = 0; u < Cfg<T>::kTilesPerWarp; ++u) {
+      for (int u = 0; u < Mc::kTilesPerWarp; ++u) {
         const int tl = warp + u * kConsumers;
         if (!failed && tl < nt) load_mma_codes(stage + tl * kTileBytes, lane, mc[u]);
       }
@@ -653,7 +666,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1) gemv_mma_kernel(const Gem
         }
       }
 #pragma unroll
-      for (int u = 0; u < Cfg<T>::kTilesPerWarp; ++u) {
+      for (int u = 0; u < Mc::kTilesPerWarp; ++u) {
         const int tl = warp + u * kConsumers;
         if (!failed && tl < nt)
           group_mma<T, kGroupSums>(mc[u], gs + tl, sb, pl.sb_stride, sgsum, sdx, a, row_base, lane, y);
@@ -698,9 +711,9 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1) gemv_mma_kernel(const Gem
   }
 }
 
-template <int T, bool G>
+template <int T, bool G, int TPW>
 cudaError_t launch_mma(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
-  auto kernel = gemv_mma_kernel<T, G>;
+  auto kernel = gemv_mma_kernel<T, G, TPW>;
   GemvArgs a = a0;
   int dev = 0, optin = 0, nsm = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -710,14 +723,14 @@ cudaError_t launch_mma(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
       (e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
   int stages = TQ_GEMV_MAX_STAGES;
-  while (stages > 2 && plan_mma<T>(stages, cols).total > optin) --stages;
-  const int64_t smem = plan_mma<T>(stages, cols).total;
+  while (stages > 2 && plan_mma<T, TPW>(stages, cols).total > optin) --stages;
+  const int64_t smem = plan_mma<T, TPW>(stages, cols).total;
   if (smem > optin) return cudaErrorNotSupported;
   a.stages = stages;
   e = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), (int)smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, Cfg<T>::kThreads, (size_t)smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, MmaCfg<T, TPW>::kThreads, (size_t)smem);
   if (e != cudaSuccess) return e;
   per_sm = max(1, min(per_sm, TQ_GEMV_CTAS_PER_SM));
   int grid = (int)std::min<int64_t>(a.nrb, (int64_t)nsm * per_sm);
@@ -725,7 +738,7 @@ cudaError_t launch_mma(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
   for (int g = grid; g >= grid - grid / 4 && g >= 1; --g)
     if (a.nrb % g == 0) { grid = g; break; }
 #endif
-  return launch_pdl(kernel, dim3(grid), dim3(Cfg<T>::kThreads), (size_t)smem, s, a);
+  return launch_pdl(kernel, dim3(grid), dim3(MmaCfg<T, TPW>::kThreads), (size_t)smem, s, a);
 }
 
 template <int T, bool G>
@@ -771,8 +784,11 @@ cudaError_t launch_t(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
 template <int T>
 cudaError_t launch_tok(const GemvArgs& a, int64_t cols, bool gsum, cudaStream_t s) {
   if (T >= TQ_GEMV_MMA_MIN_TOK) {
-    const cudaError_t e = gsum ? launch_mma<T, true>(a, cols, s) : launch_mma<T, false>(a, cols, s);
-    // its f16 activations did not fit in shared memory: the dp4a loop
+    cudaError_t e = gsum ? launch_mma<T, true, 2>(a, cols, s) : launch_mma<T, false, 2>(a, cols, s);
+    // the ring and the f16 activations did not fit in shared memory: half the
+    // stage, then the dp4a loop
+    if (e == cudaErrorNotSupported)
+      e = gsum ? launch_mma<T, true, 1>(a, cols, s) : launch_mma<T, false, 1>(a, cols, s);
     if (e != cudaErrorNotSupported) return e;
   }
   return gsum ? launch_t<T, true>(a, cols, s) : launch_t<T, false>(a, cols, s);
