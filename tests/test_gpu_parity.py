@@ -204,6 +204,38 @@ def test_deterministic_and_stream():
     assert tq.tq_device_status() == tq.TQ_OK
 
 
+def test_concurrent_streams():
+    """Two streams run the fused quantize + matmul at once (GEMV and tensor-core
+    routes), each with its own buffers and workspace, several calls deep; every
+    result equals the same call run alone."""
+    import bit_matvec_gb300 as tq
+    rows, cols = 300, 1024
+    wpq = _weights(rows, cols, 7)
+    Wtq = gpu_repack(wpq, rows, cols)
+    cases = [(1, 7), (64, 8), (9, 9), (130, 10)]
+    refs, lanes = [], []
+    for ntok, seed in cases:
+        x = torch.from_numpy(np.ascontiguousarray(_acts(ntok, cols, seed))).to(DEV)
+        Xq, Y = tq.q8K_empty(ntok, cols, DEV), torch.empty((ntok, rows), device=DEV)
+        ws = tq.workspace_empty(rows, cols, ntok, DEV)
+        tq.tq_quantize_matmul(Wtq, x, Xq, Y, rows, cols, ntok, ws)
+        torch.cuda.synchronize()
+        refs.append((Xq.clone(), Y.clone()))
+        lanes.append((x, tq.q8K_empty(ntok, cols, DEV), torch.empty((ntok, rows), device=DEV),
+                      tq.workspace_empty(rows, cols, ntok, DEV), ntok))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    for rep in range(3):
+        for i, (x, Xq, Y, ws, ntok) in enumerate(lanes):
+            tq.tq_quantize_matmul(Wtq, x, Xq, Y, rows, cols, ntok, ws, stream=streams[i % 2])
+    torch.cuda.synchronize()
+    for (Xq_ref, Y_ref), (_, Xq, Y, _, _) in zip(refs, lanes):
+        assert torch.equal(Xq, Xq_ref)
+        assert torch.equal(Y.view(torch.int32), Y_ref.view(torch.int32))
+    assert tq.tq_device_status() == tq.TQ_OK
+
+
 @pytest.mark.parametrize("rows,cols,ntok", [(300, 1024, 1), (100, 768, 3), (300, 1024, 4),
                                              (64, 8192, 8), (32, 256, 8), (128, 1024, 9),
                                              (100, 512, 64), (300, 1024, 65), (160, 2048, 130)])

@@ -60,3 +60,21 @@ def test_matmul_through_ptq1(ntok):
     assert np.array_equal(gpu_groupsums(Wtq, Xq, rows, cols, ntok), oracle.groupsums(wpq, xq, rows, cols))
     y_ref, abs_sum = oracle.matmul(wpq, xq, rows, cols)
     assert_close(gpu_matmul(Wtq, Xq, rows, cols, ntok), y_ref, abs_sum)
+
+
+def test_repack_ptq1_decode_size():
+    """The decode workload's 32768 x 8192 weights as a ptq1_0 file: the whole
+    repacked buffer equals tq_repack of the pq2_0 file of the same weights."""
+    import bit_matvec_gb300 as tq
+    rows, cols = 32768, 8192
+    s = synth.seeds(synth.CONFIGS["decode"]["index"])
+    codes = synth.ternary_codes(rows, cols, s["weights"])
+    scales = synth.group_scales(rows, cols, s["scales"])
+    sb = np.ascontiguousarray(scales.astype(np.float16)).view(np.uint16)
+    wpt = oracle.encode_ptq1_0(codes.astype(np.int8) - 1, sb)
+    a = _repack_ptq1(wpt, rows, cols)
+    del wpt
+    W = to_dev(synth.pack_pq2_0(codes, scales))
+    b = tq.repacked_empty(rows, cols, DEV)
+    tq.tq_repack(W, b, rows, cols)
+    assert torch.equal(a, b)
