@@ -21,30 +21,106 @@ std::mutex g_mu;
 int* g_status_ptr[kMaxDevices] = {};
 std::map<std::pair<int, const void*>, int> g_smem_optin;
 
-// Last kernel this library enqueued on each stream. The GEMV may read weights
-// before the preceding kernel finishes only when that kernel is the quantizer,
-// which never writes weights.
-enum LastOp { kOpOther = 0, kOpQuantize = 1, kOpMatmul = 2 };
+bool overlap(const void* a, int64_t na, const void* b, int64_t nb) {
+  const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return na > 0 && nb > 0 && x < y + (uintptr_t)nb && y < x + (uintptr_t)na;
+}
+
+// What this library last enqueued on each stream. A GEMV may read weights
+// before the preceding kernel finishes when that kernel writes none (the
+// quantizer, a matmul, a GEMV whose outputs miss them). After a GEMV it may
+// also read its activations early, but only inside a stream capture whose one
+// dependency is that GEMV's node: then nothing else sits between the two
+// kernels, and since a GEMV lets its successor start only after its own wait,
+// that GEMV is the only kernel that can still be running; its outputs must
+// miss every input of the new one. Outside a capture the library cannot see
+// other work on the stream, so it does not read activations early there.
+enum LastOp { kOpOther = 0, kOpQuantize = 1, kOpMatmul = 2, kOpGemv = 3 };
+struct StreamLast {
+  int op = kOpOther;
+  unsigned long long capture_id = 0;   // kOpGemv inside a capture: its id and
+  cudaGraphNode_t node = nullptr;      // the GEMV's node (else 0, null)
+  const void* out[2] = {nullptr, nullptr};
+  int64_t out_bytes[2] = {0, 0};
+};
 std::mutex g_stream_mu;
-std::unordered_map<cudaStream_t, int> g_last_op;
+std::unordered_map<cudaStream_t, StreamLast> g_last_op;
 
 void note_op(cudaStream_t s, int op) {
+  StreamLast l;
+  l.op = op;
   std::lock_guard<std::mutex> lk(g_stream_mu);
-  g_last_op[s] = op;
+  g_last_op[s] = l;
+}
+
+// The single node the next captured operation on s will depend on; false when
+// s is not capturing or depends on several nodes (or none).
+bool capture_tail(cudaStream_t s, unsigned long long* id, cudaGraphNode_t* node) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  const cudaGraphNode_t* deps = nullptr;
+  const cudaGraphEdgeData* edges = nullptr;
+  size_t n = 0;
+  if (cudaStreamGetCaptureInfo(s, &st, id, nullptr, &deps, &edges, &n) != cudaSuccess) {
+    (void)cudaGetLastError();   // a failed query is no error of the caller's
+    return false;
+  }
+  if (st != cudaStreamCaptureStatusActive || n != 1 || !deps) return false;
+  *node = deps[0];
+  return true;
+}
+
+// Called right after a GEMV launch on s, with the ranges it writes.
+void note_gemv(cudaStream_t s, const void* out0, int64_t bytes0, const void* out1,
+               int64_t bytes1) {
+  StreamLast l;
+  l.op = kOpGemv;
+  if (!capture_tail(s, &l.capture_id, &l.node)) {
+    l.capture_id = 0;
+    l.node = nullptr;
+  }
+  l.out[0] = out0;
+  l.out_bytes[0] = bytes0;
+  l.out[1] = out1;
+  l.out_bytes[1] = bytes1;
+  std::lock_guard<std::mutex> lk(g_stream_mu);
+  g_last_op[s] = l;
+}
+
+bool misses_outputs(const StreamLast& l, const void* p, int64_t n) {
+  return !overlap(p, n, l.out[0], l.out_bytes[0]) && !overlap(p, n, l.out[1], l.out_bytes[1]);
 }
 
 bool last_op_is_quantize(cudaStream_t s) {
   std::lock_guard<std::mutex> lk(g_stream_mu);
   auto it = g_last_op.find(s);
-  return it != g_last_op.end() && it->second == kOpQuantize;
+  return it != g_last_op.end() && it->second.op == kOpQuantize;
 }
 
-// The last call on the stream was the quantizer or a matmul: kernels that
-// never write weights.
-bool last_op_keeps_weights(cudaStream_t s) {
+// The last call on the stream enqueued kernels that do not write the weights.
+bool last_op_keeps_weights(cudaStream_t s, const void* W, int64_t w_bytes) {
   std::lock_guard<std::mutex> lk(g_stream_mu);
   auto it = g_last_op.find(s);
-  return it != g_last_op.end() && (it->second == kOpQuantize || it->second == kOpMatmul);
+  if (it == g_last_op.end()) return false;
+  const StreamLast& l = it->second;
+  return l.op == kOpQuantize || l.op == kOpMatmul || (l.op == kOpGemv && misses_outputs(l, W, w_bytes));
+}
+
+// The GEMV about to be enqueued on s may read all its inputs (the activations
+// in0 and the weights in1) before waiting for the kernel before it.
+bool gemv_inputs_final(cudaStream_t s, const void* in0, int64_t bytes0, const void* in1,
+                       int64_t bytes1) {
+  StreamLast l;
+  {
+    std::lock_guard<std::mutex> lk(g_stream_mu);
+    auto it = g_last_op.find(s);
+    if (it == g_last_op.end()) return false;
+    l = it->second;
+  }
+  if (l.op != kOpGemv || !l.node) return false;
+  unsigned long long id = 0;
+  cudaGraphNode_t node = nullptr;
+  if (!capture_tail(s, &id, &node) || id != l.capture_id || node != l.node) return false;
+  return misses_outputs(l, in0, bytes0) && misses_outputs(l, in1, bytes1);
 }
 
 int fail_cuda(cudaError_t e) {
@@ -54,11 +130,6 @@ int fail_cuda(cudaError_t e) {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 bool aligned4(const void* p) { return ((uintptr_t)p & 3u) == 0; }
-
-bool overlap(const void* a, int64_t na, const void* b, int64_t nb) {
-  const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
-  return na > 0 && nb > 0 && x < y + (uintptr_t)nb && y < x + (uintptr_t)na;
-}
 
 cudaError_t device_status_ptr(int** out) {
   int dev = 0;
@@ -122,10 +193,16 @@ int matmul_impl(const void* Wtq, const void* Xq, float* Y, int32_t* S, int64_t r
   cudaError_t e = device_status_ptr(&status);
   if (e != cudaSuccess) return fail_cuda(e);
   const bool after_quantize = last_op_is_quantize(s);
+  const bool inputs_final =
+      ntok <= gemv_max_tokens() &&
+      gemv_inputs_final(s, Xq, q8K_bytes(ntok, cols), Wtq, tq_repacked_bytes(rows, cols));
   note_op(s, kOpOther);
   if (ntok <= gemv_max_tokens()) {
-    e = launch_gemv(W, X, Y, S, rows, cols, (int)ntok, status, after_quantize, s);
-    if (e == cudaSuccess) return TQ_OK;
+    e = launch_gemv(W, X, Y, S, rows, cols, (int)ntok, status, after_quantize, inputs_final, s);
+    if (e == cudaSuccess) {
+      note_gemv(s, out, out_bytes, nullptr, 0);
+      return TQ_OK;
+    }
     if (e != cudaErrorNotSupported) return fail_cuda(e);
     // activations too large for the GEMV's shared memory: tensor-core path
   }
@@ -283,11 +360,12 @@ int tq_quantize_matmul(const void* Wtq, const float* X, void* Xq, float* Y, int6
     int* status = nullptr;
     cudaError_t e = device_status_ptr(&status);
     if (e != cudaSuccess) return fail_cuda(e);
-    const bool early = last_op_keeps_weights(s);
+    const bool early = last_op_keeps_weights(s, Wtq, w_bytes);
+    const bool inputs_final = gemv_inputs_final(s, X, x_bytes, Wtq, w_bytes);
     e = launch_gemv(static_cast<const uint8_t*>(Wtq), nullptr, Y, nullptr, rows, cols, (int)ntok,
-                    status, early, s, X, static_cast<uint8_t*>(Xq));
+                    status, early, inputs_final, s, X, static_cast<uint8_t*>(Xq));
     if (e == cudaSuccess) {
-      note_op(s, kOpMatmul);
+      note_gemv(s, Y, y_bytes, Xq, xq_bytes);
       return TQ_OK;
     }
     if (e != cudaErrorNotSupported) {

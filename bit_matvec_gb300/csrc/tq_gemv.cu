@@ -86,18 +86,21 @@ struct GemvArgs {
   int stages;         // ring depth
   int early_weights;  // 1: the previous kernel does not write Wtq; prefetch before waiting
   const float* X;     // fused form: f32 activations [T][cols] quantized here (else null)
-  uint8_t* Xq_out;    // fused form: where CTA 0 writes the q8_K blocks (may be null)
+  uint8_t* Xq_out;    // fused form: where the q8_K blocks are written (may be null)
+  int defer;          // 1: the inputs are final when the kernel starts; wait for the
+                      // previous kernel only before the first global write
 };
 
 // Fused form: quantizes the T x cols f32 activations block by block (warp per
 // q8_K block, q8K_warp, so the bytes equal the quantizer kernel's), four
 // blocks per warp whose loads are issued together, and hands each block to
 // store(tb, w0, w1, s8, d) on every lane of the warp. CTA 0 also writes the
-// q8_K blocks to a.Xq_out.
+// q8_K blocks to a.Xq_out, unless the kernel defers its writes (then each CTA
+// writes some of them from shared memory after its wait).
 template <class Store>
 __device__ __forceinline__ void stage_quantize(const GemvArgs& a, int nblocks, int warp,
                                                int nwarps, int lane, Store store) {
-  const bool write_xq = a.Xq_out != nullptr && blockIdx.x == 0;
+  const bool write_xq = a.Xq_out != nullptr && blockIdx.x == 0 && !a.defer;
   for (int tb0 = warp; tb0 < nblocks; tb0 += 4 * nwarps) {
     float4 va[4], vb[4];
 #pragma unroll
@@ -246,12 +249,18 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
       mbarrier_init(smem_u32(redempty + i), T);
     }
     mbarrier_init_fence();
-    // When the previous kernel in the stream is the quantizer (it does not
-    // write weights) the first stages go out before waiting for it.
+    // When the previous kernel in the stream writes no weights, the first
+    // stages go out before waiting for it.
     if (a.early_weights) issue_first();
   }
-  pdl_launch_dependents();
-  pdl_wait_primary();   // the q8_K activations are written by the previous kernel
+  // The activations may come from the previous kernel: wait for it first,
+  // unless the host has shown they do not (defer). Either way the next kernel
+  // is let in only after this kernel's wait, so when it starts, only this
+  // kernel can still be running before it.
+  if (!a.defer) {
+    pdl_wait_primary();
+    pdl_launch_dependents();
+  }
   if (threadIdx.x == 0 && !a.early_weights) issue_first();
 
   // Stage q8_K activations, every thread issuing independent loads: qs as a
@@ -286,6 +295,23 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
     }
   }
   __syncthreads();
+
+  // Deferred form: the wait (and the next kernel's start) comes after the
+  // first tile column's dot products, before any global write; then this
+  // CTA's share of the q8_K blocks goes out from the staged copy.
+  bool waited = !a.defer;
+  auto finish_wait = [&]() {
+    pdl_wait_primary();
+    pdl_launch_dependents();
+    if (a.X && a.Xq_out) {
+      for (int tb = blockIdx.x + warp * gridDim.x; tb < T * a.nblk; tb += gridDim.x * kConsumers) {
+        const uint2 q = reinterpret_cast<const uint2*>(sq + tb * kQK)[lane];
+        const int s8 = __dp4a((int)q.x, 0x01010101, 0) + __dp4a((int)q.y, 0x01010101, 0);
+        q8K_store(a.Xq_out + (int64_t)tb * kQ8KBytes, lane, q.x, q.y, s8, sdx[tb]);
+      }
+    }
+    waited = true;
+  };
 
   bool failed = false;
   int j = 0, slot = 0;
@@ -333,6 +359,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
       }
       if (++slot == S) { slot = 0; phase ^= 1u; }
     }
+    if (!waited) finish_wait();
     if (!kGroupSums) {
       // The warps' partial sums of each row meet in shared memory; warp
       // (i*T + t) % warps adds those of token t in warp order (deterministic) and
@@ -362,6 +389,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
       }
     }
   }
+  if (!waited) finish_wait();   // a CTA without tile columns
   if (failed && lane == 0) atomicExch(a.status, kDevTimeout);
   // Copies can still be in flight only after a failed wait: then let the last
   // stage of each slot land before the CTA's shared memory is released.
@@ -591,8 +619,10 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
     mbarrier_init_fence();
     if (a.early_weights) issue_first();
   }
-  pdl_launch_dependents();
-  pdl_wait_primary();   // the q8_K activations are written by the previous kernel
+  if (!a.defer) {   // as in the one-token kernel
+    pdl_wait_primary();
+    pdl_launch_dependents();
+  }
   if (threadIdx.x == 0 && !a.early_weights) issue_first();
 
   // Stage the activations: f16 q * 2^(9 - 2s) per token row, the sum of each
@@ -630,6 +660,41 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
     }
   }
   __syncthreads();
+
+  // Deferred form, as in the one-token kernel; the q8_K values come back
+  // exactly from their staged f16 copies (q * 2^(9 - 2s), |q| <= 127).
+  bool waited = !a.defer;
+  auto finish_wait = [&]() {
+    pdl_wait_primary();
+    pdl_launch_dependents();
+    if (a.X && a.Xq_out) {
+      const float inv0 = (lane & 1) ? 0.03125f : 0.001953125f;   // 2^-5 : 2^-9
+      const float inv1 = (lane & 1) ? 0.125f : 0.0078125f;       // 2^-3 : 2^-7
+      for (int tb = blockIdx.x + warp * gridDim.x; tb < T * a.nblk; tb += gridDim.x * kConsumers) {
+        const int t = tb / a.nblk, b = tb - t * a.nblk;
+        const uint2* src =
+            reinterpret_cast<const uint2*>(sb + t * pl.sb_stride + ((int64_t)b * kQK + 8 * lane) * 2);
+        int q[8];
+        int s8 = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint2 v = src[h];
+          const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+          const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+          const float inv = h ? inv1 : inv0;
+          q[4 * h + 0] = __float2int_rn(f0.x * inv);
+          q[4 * h + 1] = __float2int_rn(f0.y * inv);
+          q[4 * h + 2] = __float2int_rn(f1.x * inv);
+          q[4 * h + 3] = __float2int_rn(f1.y * inv);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s8 += q[e];
+        q8K_store(a.Xq_out + (int64_t)tb * kQ8KBytes, lane, pack4_s8(q[0], q[1], q[2], q[3]),
+                  pack4_s8(q[4], q[5], q[6], q[7]), s8, sdx[tb]);
+      }
+    }
+    waited = true;
+  };
 
   bool failed = false;
   int j = 0, slot = 0;
@@ -673,6 +738,7 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
       }
       if (++slot == S) { slot = 0; phase ^= 1u; }
     }
+    if (!waited) finish_wait();
     if (!kGroupSums) {
       // The warps' partial sums of this tile column meet in shared memory;
       // warp (i*8 + e) % 16 adds C position e over the warps in warp order.
@@ -702,6 +768,7 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
       }
     }
   }
+  if (!waited) finish_wait();   // a CTA without tile columns
   if (failed && lane == 0) atomicExch(a.status, kDevTimeout);
   if (__syncthreads_or(failed) && threadIdx.x == 0) {
     for (int sl = 0; sl < S && sl < nstage; ++sl) {
@@ -709,6 +776,15 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
       mbarrier_wait_bounded(smem_u32(full + sl), (uint32_t)((last / S) & 1), kWaitLimitNs);
     }
   }
+}
+
+// Whether a launch the host allowed to defer its wait (a.defer) does so: only
+// for Y outputs, and only when every CTA has two or more tile columns, so the
+// wait after the first one leaves the rest of the stream to overlap the
+// previous kernel's end; with a single column per CTA the wait would come at
+// the end and hold back the next kernel's start (measured slower).
+inline int defer_wait(const GemvArgs& a, bool group_sums, int grid) {
+  return a.defer && !group_sums && a.nrb >= 2 * grid ? 1 : 0;
 }
 
 template <int T, bool G, int TPW>
@@ -738,6 +814,7 @@ cudaError_t launch_mma(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
   for (int g = grid; g >= grid - grid / 4 && g >= 1; --g)
     if (a.nrb % g == 0) { grid = g; break; }
 #endif
+  a.defer = defer_wait(a, G, grid);
   return launch_pdl(kernel, dim3(grid), dim3(MmaCfg<T, TPW>::kThreads), (size_t)smem, s, a);
 }
 
@@ -772,6 +849,7 @@ cudaError_t launch_t(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
   for (int g = grid; g >= grid - grid / 4 && g >= 1; --g)
     if (a.nrb % g == 0) { grid = g; break; }
 #endif
+  a.defer = defer_wait(a, G, grid);
   return launch_pdl(kernel, dim3(grid), dim3(Cfg<T>::kThreads), (size_t)smem, s, a);
 }
 
@@ -781,13 +859,44 @@ cudaError_t launch_t(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
 #define TQ_GEMV_MMA_MIN_TOK 4
 #endif
 
+// Tiles per warp and stage of the tensor-core variant: 0 picks by shape;
+// 1..3 force a value (where it fits in shared memory).
+#ifndef TQ_GEMV_MMA_TPW
+#define TQ_GEMV_MMA_TPW 0
+#endif
+
+// A tile column's groups run in stages of (warps x TPW) tiles; the last
+// stage of each column leaves warps idle when the count does not divide. Of
+// two and three tiles per warp, take the one with fewer idle tiles (two on a
+// tie): measured on GB300, three is 2-4% faster at 40 groups (5120 columns),
+// two 3-10% faster at 64 (8192); four never won.
+inline int mma_tiles_per_warp(int ngroups) {
+  if (TQ_GEMV_MMA_TPW) return TQ_GEMV_MMA_TPW;
+  auto idle = [&](int tpw) {
+    const int st = TQ_GEMV_WARPS * tpw;
+    return (ngroups + st - 1) / st * st - ngroups;
+  };
+  return idle(3) < idle(2) ? 3 : 2;
+}
+
+template <int T, bool G>
+cudaError_t launch_mma_tpw(int tpw, const GemvArgs& a, int64_t cols, cudaStream_t s) {
+  switch (tpw) {
+    case 1: return launch_mma<T, G, 1>(a, cols, s);
+    case 2: return launch_mma<T, G, 2>(a, cols, s);
+    default: return launch_mma<T, G, 3>(a, cols, s);
+  }
+}
+
 template <int T>
 cudaError_t launch_tok(const GemvArgs& a, int64_t cols, bool gsum, cudaStream_t s) {
-  if (T >= TQ_GEMV_MMA_MIN_TOK) {
-    cudaError_t e = gsum ? launch_mma<T, true, 2>(a, cols, s) : launch_mma<T, false, 2>(a, cols, s);
-    // the ring and the f16 activations did not fit in shared memory: half the
-    // stage, then the dp4a loop
-    if (e == cudaErrorNotSupported)
+  if constexpr (T >= TQ_GEMV_MMA_MIN_TOK) {
+    const int tpw = mma_tiles_per_warp(a.ngroups);
+    cudaError_t e = gsum ? launch_mma_tpw<T, true>(tpw, a, cols, s)
+                         : launch_mma_tpw<T, false>(tpw, a, cols, s);
+    // the ring and the f16 activations did not fit in shared memory: one
+    // tile per warp and stage, then the dp4a loop
+    if (e == cudaErrorNotSupported && tpw != 1)
       e = gsum ? launch_mma<T, true, 1>(a, cols, s) : launch_mma<T, false, 1>(a, cols, s);
     if (e != cudaErrorNotSupported) return e;
   }
@@ -801,7 +910,7 @@ int gemv_max_tokens() { return kMaxTok; }
 
 cudaError_t launch_gemv(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t* S,
                         int64_t rows, int64_t cols, int ntok, int* dev_status, bool early_weights,
-                        cudaStream_t s, const float* X, uint8_t* Xq_out) {
+                        bool inputs_final, cudaStream_t s, const float* X, uint8_t* Xq_out) {
   if (ntok < 1 || ntok > kMaxTok) return cudaErrorNotSupported;
   if (rows > 0x7fffffff / 2 || cols / kGroup > 0x7fffffff / kTileBytes)
     return cudaErrorNotSupported;
@@ -816,9 +925,10 @@ cudaError_t launch_gemv(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t
   a.nblk = (int)(cols / kQK);
   a.nrb = (int)((rows + kTileRows - 1) / kTileRows);
   a.stages = 2;
-  a.early_weights = early_weights ? 1 : 0;
+  a.early_weights = early_weights || inputs_final ? 1 : 0;
   a.X = X;
   a.Xq_out = Xq_out;
+  a.defer = inputs_final ? 1 : 0;
   const bool gsum = S != nullptr;
   switch (ntok) {
     case 1: return launch_tok<1>(a, cols, gsum, s);

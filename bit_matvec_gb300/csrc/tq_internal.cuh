@@ -233,12 +233,18 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // when the activations of all tokens do not fit in shared memory.
 // early_weights: the kernel enqueued just before on the stream does not write
 // Wtq, so weight reads may start before waiting for it.
+// inputs_final: the kernel enqueued just before is a GEMV (which lets its
+// successor start only after its own wait, so nothing older still runs) and
+// none of its outputs overlaps Wtq, Xq or X; the kernel may then read all its
+// inputs before waiting for it and wait only before its first global write.
+// Every GEMV kernel lets the next kernel start only after its own wait.
 // With X non-null the GEMV quantizes the f32 activations X itself (the fused
 // form; Xq is then an output, written once, and may be null) instead of
 // reading q8_K blocks from Xq.
 cudaError_t launch_gemv(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t* S,
                         int64_t rows, int64_t cols, int ntok, int* dev_status, bool early_weights,
-                        cudaStream_t s, const float* X = nullptr, uint8_t* Xq_out = nullptr);
+                        bool inputs_final, cudaStream_t s, const float* X = nullptr,
+                        uint8_t* Xq_out = nullptr);
 int gemv_max_tokens();
 
 // Tensor-core path for any ntok >= 1 (used for ntok > gemv_max_tokens()).

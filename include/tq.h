@@ -173,6 +173,16 @@ int tq_repack_ptq1_0(const void *Wpt, void *Wtq, int64_t rows, int64_t cols, voi
  * that wait, since the quantizer never writes weights; so do not write Wtq
  * with a kernel of your own between tq_quantize_q8K and tq_matmul on one
  * stream (copies and events are fine).
+ * GEMV chains in a graph: a GEMV lets the next kernel start only after its
+ * own wait. While a stream is being captured, a GEMV whose one dependency in
+ * the capture is the previous call's GEMV node (nothing else was captured
+ * between them), and none of whose inputs (Wtq, Xq, or X for
+ * tq_quantize_matmul) overlaps that GEMV's outputs (Y or S, and Xq it
+ * wrote), reads its inputs before waiting, and waits only before its first
+ * store, when every CTA has two or more 32-row tile columns (the one-token
+ * decode matrices). Back-to-back decode matmuls in a graph then overlap
+ * each other's start and end. Outside a capture the library cannot see what
+ * else is on the stream and always waits first.
  * Errors: TQ_ERR_SHAPE if cols % 256 != 0; TQ_ERR_ALIAS if Y overlaps an input.
  */
 int tq_matmul(const void *Wtq, const void *Xq, float *Y, int64_t rows, int64_t cols,
@@ -226,7 +236,8 @@ int tq_matmul_groupsums_ws(const void *Wtq, const void *Xq, int32_t *S, int64_t 
  * the q8_K blocks of X, Y = the product of Wtq and Xq. For ntok <= 8 it is one
  * fused launch: every CTA of the GEMV quantizes X into its shared memory
  * itself (with the quantizer's arithmetic, so Xq and Y carry the bits of the
- * two separate calls), and CTA 0 writes Xq. That removes a launch and the
+ * two separate calls), and writes Xq (CTA 0 at its start; in the graph chains
+ * tq_matmul describes, every CTA a share after its wait). That removes a launch and the
  * quantizer's place on the critical path of each matmul. For ntok >= 9 one
  * kernel quantizes X (the same arithmetic), writes Xq and packs the
  * workspace, which the tensor-core kernel then reads: two launches instead
@@ -239,7 +250,8 @@ int tq_matmul_groupsums_ws(const void *Wtq, const void *Xq, int32_t *S, int64_t 
  * reading Wtq before the kernel enqueued just before it ends when the
  * previous call this library received for the stream was the quantizer or a
  * matmul; so do not write Wtq with a kernel of your own between such a call
- * and this one on one stream.
+ * and this one on one stream. In a captured chain of GEMVs it may read X and
+ * Wtq before the previous GEMV ends, under the conditions tq_matmul states.
  * Errors: those of tq_quantize_q8K and tq_matmul_ws, checked before anything
  * is enqueued.
  */

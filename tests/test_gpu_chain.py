@@ -1,0 +1,191 @@
+"""GEMV calls chained back to back in a captured CUDA graph.
+
+Inside a capture, a GEMV that directly follows another GEMV of this library
+(no other node between them) and reads nothing that GEMV writes may read its
+weights and activations before the earlier one finishes, waiting for it only
+before its first store. These tests run such chains, and chains where a call
+reads the previous call's output (which must wait), and check that every
+output and every q8_K byte equals the same calls run one at a time.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import DEV, assert_close, ensure_built, gpu_quantize, gpu_repack
+
+pytestmark = pytest.mark.gpu
+
+# 640 tile columns: at least two per CTA for every GEMV launch shape, the
+# condition for the early reads
+ROWS = 20480
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ensure_built()
+
+
+def _acts(ntok, cols, seed_index):
+    s = synth.seeds(seed_index)
+    return synth.activations(ntok, cols, s["acts"], s["outliers"])
+
+
+def _capture(fn):
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fn(s)
+    return g
+
+
+def _bits(t):
+    return t.view(torch.int32) if t.dtype == torch.float32 else t
+
+
+@pytest.mark.parametrize("ntok", [1, 3, 4, 8])
+def test_graph_chain_of_independent_calls(ntok):
+    """Four fused calls and two tq_matmul calls, each on its own weights, all
+    reading activations no call of the chain writes (the fused calls share
+    one q8_K output buffer): the early-read form runs from the second call on."""
+    import bit_matvec_gb300 as tq
+    cols, n = 1024, 4
+    wpq = [synth.pq2_0_weights(ROWS, cols, 40 + i) for i in range(n + 2)]
+    Ws = [gpu_repack(w, ROWS, cols) for w in wpq]
+    x = _acts(ntok, cols, 41)
+    X = torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
+    Xq_in = gpu_quantize(_acts(ntok, cols, 42))
+    ws = tq.workspace_empty(ROWS, cols, ntok, DEV)
+
+    def run(s, Ys, Xq):
+        for i in range(n):
+            tq.tq_quantize_matmul(Ws[i], X, Xq, Ys[i], ROWS, cols, ntok, ws, stream=s)
+        for i in range(2):
+            tq.tq_matmul(Ws[n + i], Xq_in, Ys[n + i], ROWS, cols, ntok, stream=s)
+
+    # one call at a time
+    refs = []
+    Xq_ref = tq.q8K_empty(ntok, cols, DEV)
+    for i in range(n + 2):
+        Y = torch.empty((ntok, ROWS), device=DEV)
+        if i < n:
+            tq.tq_quantize_matmul(Ws[i], X, Xq_ref, Y, ROWS, cols, ntok, ws)
+        else:
+            tq.tq_matmul(Ws[i], Xq_in, Y, ROWS, cols, ntok)
+        torch.cuda.synchronize()
+        refs.append(Y)
+    assert torch.equal(Xq_ref, gpu_quantize(x))
+
+    Ys = [torch.full((ntok, ROWS), float("nan"), device=DEV) for _ in range(n + 2)]
+    Xq = torch.full_like(Xq_ref, 0xEE)
+    g = _capture(lambda s: run(s, Ys, Xq))
+    for _ in range(3):
+        g.replay()
+        torch.cuda.synchronize()
+        for Y, R in zip(Ys, refs):
+            assert torch.equal(_bits(Y), _bits(R))
+        assert torch.equal(Xq, Xq_ref)
+        for Y in Ys:
+            Y.fill_(float("nan"))
+        Xq.fill_(0xEE)
+    assert tq.tq_device_status() == tq.TQ_OK
+
+    # and against the oracle, for the first and the last weights
+    xq = oracle.quantize_q8K(x)
+    for i in (0, n - 1):
+        rows_s = np.r_[0:64, ROWS - 64:ROWS]
+        y_ref, abs_sum = oracle.matmul(wpq[i].reshape(ROWS, -1)[rows_s].reshape(-1), xq,
+                                       len(rows_s), cols)
+        assert_close(refs[i].cpu().numpy()[:, rows_s], y_ref, abs_sum)
+
+
+def _wide(wpq, rows, cols, reps):
+    """pq2_0 bytes of a rows x (cols * reps) matrix: each row repeated reps times."""
+    return np.tile(wpq.reshape(rows, -1), (1, reps)).reshape(-1)
+
+
+@pytest.mark.parametrize("ntok", [1, 4])
+def test_graph_chain_reading_previous_outputs(ntok):
+    """Each call reads what the call before it wrote (its Y as the next
+    activations, or its q8_K bytes): those calls wait before reading, and the
+    results equal the calls run one at a time. One call in the chain reads
+    only older outputs and may read early."""
+    import bit_matvec_gb300 as tq
+    c0, reps = 1024, ROWS // 1024
+    w0 = synth.pq2_0_weights(ROWS, c0, 50)
+    W1 = gpu_repack(w0, ROWS, c0)                               # c0 -> ROWS
+    W2 = gpu_repack(_wide(synth.pq2_0_weights(ROWS, c0, 51), ROWS, c0, reps), ROWS, ROWS)
+    W3 = gpu_repack(_wide(synth.pq2_0_weights(ROWS, c0, 52), ROWS, c0, reps), ROWS, ROWS)
+    W4 = gpu_repack(_wide(synth.pq2_0_weights(ROWS, c0, 53), ROWS, c0, reps), ROWS, ROWS)
+    X0 = torch.from_numpy(np.ascontiguousarray(_acts(ntok, c0, 54))).to(DEV)
+    ws0 = tq.workspace_empty(ROWS, c0, ntok, DEV)
+    ws = tq.workspace_empty(ROWS, ROWS, ntok, DEV)
+
+    def buffers():
+        return dict(Y1=torch.full((ntok, ROWS), float("nan"), device=DEV),
+                    Y2=torch.full((ntok, ROWS), float("nan"), device=DEV),
+                    Y3=torch.full((ntok, ROWS), float("nan"), device=DEV),
+                    Y4=torch.full((ntok, ROWS), float("nan"), device=DEV),
+                    Y5=torch.full((ntok, ROWS), float("nan"), device=DEV),
+                    Xq0=torch.full((tq.q8K_nbytes(ntok, c0),), 0xEE, dtype=torch.uint8, device=DEV),
+                    Xq1=torch.full((tq.q8K_nbytes(ntok, ROWS),), 0xEE, dtype=torch.uint8, device=DEV),
+                    Xq2=torch.full((tq.q8K_nbytes(ntok, ROWS),), 0xEE, dtype=torch.uint8, device=DEV))
+
+    def steps(b):
+        return [
+            lambda s: tq.tq_quantize_matmul(W1, X0, b["Xq0"], b["Y1"], ROWS, c0, ntok, ws0, stream=s),
+            # activations = the previous call's Y
+            lambda s: tq.tq_quantize_matmul(W2, b["Y1"], b["Xq1"], b["Y2"], ROWS, ROWS, ntok, ws, stream=s),
+            # q8_K bytes the previous call wrote
+            lambda s: tq.tq_matmul(W3, b["Xq1"], b["Y3"], ROWS, ROWS, ntok, stream=s),
+            # Y of two calls back (complete once the previous call has waited)
+            lambda s: tq.tq_quantize_matmul(W4, b["Y2"], b["Xq2"], b["Y4"], ROWS, ROWS, ntok, ws, stream=s),
+            # the previous call's Y again
+            lambda s: tq.tq_quantize_matmul(W2, b["Y4"], b["Xq1"], b["Y5"], ROWS, ROWS, ntok, ws, stream=s),
+        ]
+
+    ref = buffers()
+    for step in steps(ref):
+        step(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+    got = buffers()
+    g = _capture(lambda s: [step(s) for step in steps(got)])
+    for _ in range(2):
+        g.replay()
+        torch.cuda.synchronize()
+        for k in ref:
+            assert torch.equal(_bits(got[k]), _bits(ref[k])), k
+    assert all(torch.isfinite(ref[k]).all() for k in ("Y1", "Y2", "Y3", "Y4", "Y5"))
+    assert tq.tq_device_status() == tq.TQ_OK
+
+
+def test_eager_chain_equals_graph():
+    """The same independent chain run eagerly (where calls always wait before
+    reading) and captured give the same bits."""
+    import bit_matvec_gb300 as tq
+    cols, ntok = 2048, 1
+    Ws = [gpu_repack(synth.pq2_0_weights(ROWS, cols, 60 + i), ROWS, cols) for i in range(3)]
+    X = torch.from_numpy(np.ascontiguousarray(_acts(ntok, cols, 61))).to(DEV)
+    ws = tq.workspace_empty(ROWS, cols, ntok, DEV)
+
+    def run(s, Ys, Xq):
+        for W, Y in zip(Ws, Ys):
+            tq.tq_quantize_matmul(W, X, Xq, Y, ROWS, cols, ntok, ws, stream=s)
+
+    eager = ([torch.empty((ntok, ROWS), device=DEV) for _ in Ws], tq.q8K_empty(ntok, cols, DEV))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        run(s, *eager)
+    s.synchronize()
+    graph = ([torch.empty((ntok, ROWS), device=DEV) for _ in Ws], tq.q8K_empty(ntok, cols, DEV))
+    g = _capture(lambda st: run(st, *graph))
+    g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(eager[0], graph[0]):
+        assert torch.equal(_bits(a), _bits(b))
+    assert torch.equal(eager[1], graph[1])

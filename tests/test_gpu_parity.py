@@ -111,11 +111,14 @@ def test_gemv_groupsums_exact_matmul_close(rows, cols, ntok):
     _check_product(rows, cols, ntok)
 
 
-@pytest.mark.parametrize("rows,cols,ntok", [(64, 8192, 4), (64, 8192, 8), (96, 16384, 6)])
+@pytest.mark.parametrize("rows,cols,ntok", [(64, 8192, 4), (64, 8192, 8), (96, 16384, 6),
+                                             (64, 5120, 5), (100, 5120, 8), (40, 6144, 4)])
 def test_gemv_wide_rows(rows, cols, ntok):
     """Long rows: from 4 tokens the tensor-core (mma.sync) variant runs while its
     f16 activations fit in shared memory (8 x 8192 do not: the dp4a loop takes
-    over); 16384 columns at 6 tokens exercise the largest staged activations."""
+    over); 16384 columns at 6 tokens exercise the largest staged activations;
+    5120 and 6144 columns (40 and 48 groups) take three tiles per warp and
+    stage, the others two."""
     _check_product(rows, cols, ntok)
 
 
