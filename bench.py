@@ -338,16 +338,25 @@ def measure_replay(ntok, steps, warmup, world, device, peaks, peak_kind):
     return res
 
 
+# Steps per captured graph (a multiple of the weight copies): a decode graph
+# holds many matmuls back to back, and consecutive kernels overlap only within
+# one graph launch.
+STEPS_PER_GRAPH = 40
+
+
 def time_graph(wl: Workload, steps: int, warmup: int, world: int):
     """Device time per step, and the matmul kernel's average launch duration.
 
-    Graph A holds `copies` steps (quantize + matmul, one per weight copy) and is
-    replayed ceil(steps / copies) times between two events: the step time, with
+    Graph A holds G steps (quantize + matmul, cycling over the weight copies;
+    G = the largest multiple of `copies` up to STEPS_PER_GRAPH, at least
+    `copies`), and graph A' the steps % G left over: A replayed steps // G
+    times and A' once, between two events, time exactly `steps` steps, with
     consecutive kernels overlapping as they do in a real decode (programmatic
-    dependent launch). Graph M holds `copies` matmul launches only and is
-    replayed as often: the timed region's length over its launches is the
-    kernel's average launch duration. Graph B (steps with events around each
-    matmul, which serialise the kernels) gives the isolated per-launch time too.
+    dependent launch). Graphs M and M' hold the matmul launches alone and are
+    replayed the same way: the timed region's length over its launches is the
+    kernel's average launch duration. Graph B (`copies` steps with events
+    around each matmul, which serialise the kernels) gives the isolated
+    per-launch time too.
     """
     import torch
     import bit_matvec_gb300 as tq
@@ -363,28 +372,36 @@ def time_graph(wl: Workload, steps: int, warmup: int, world: int):
 
     ev = [(timing_event(), timing_event()) for _ in range(n)]
 
-    def timed(graph, reps):
+    G = n * max(1, STEPS_PER_GRAPH // n)
+    reps, rest = divmod(steps, G)
+
+    def timed(graph, graph_rest):
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         start.record(stream)
         for _ in range(reps):
             graph.replay()
+        if graph_rest is not None:
+            graph_rest.replay()
         end.record(stream)
         stream.synchronize()
         return start.elapsed_time(end)
+
+    def capture(fn, count):
+        if count == 0:
+            return None
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(count):
+                fn(i, stream)
+        return g
 
     with torch.cuda.stream(stream):
         for i in range(max(warmup, 3)):                 # un-captured warm-up (kernel attributes)
             wl.step(i, stream)
         stream.synchronize()
-        ga = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(ga, stream=stream):
-            for i in range(n):
-                wl.step(i, stream)
-        gm = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gm, stream=stream):
-            for i in range(n):
-                wl.matmul_only(i, stream)
+        ga, ga_rest = capture(wl.step, G), capture(wl.step, rest)
+        gm, gm_rest = capture(wl.matmul_only, G), capture(wl.matmul_only, rest)
         gb = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gb, stream=stream):
             for i in range(n):
@@ -393,15 +410,17 @@ def time_graph(wl: Workload, steps: int, warmup: int, world: int):
                 ev[i][0].record(stream)
                 wl.matmul_only(i, stream)
                 ev[i][1].record(stream)
-        reps = -(-steps // n)
         for g in (ga, gm, gb):                          # graph warm-up replays
-            for _ in range(max(1, warmup // n)):
+            for _ in range(max(1, -(-warmup // G))):
+                g.replay()
+        for g in (ga_rest, gm_rest):
+            if g is not None:
                 g.replay()
         stream.synchronize()
         barrier(world)
         torch.cuda.synchronize(wl.device)
-        total_ms = timed(ga, reps)
-        kern_ms = timed(gm, reps) / (reps * n)
+        total_ms = timed(ga, ga_rest)
+        kern_ms = timed(gm, gm_rest) / steps
         gb.replay()
         stream.synchronize()
         try:
@@ -409,9 +428,9 @@ def time_graph(wl: Workload, steps: int, warmup: int, world: int):
         except RuntimeError:
             serial_ms = None
         barrier(world)
-    done_steps = reps * n
-    how = "timed graph of back-to-back matmul launches (events around the region)"
-    return total_ms / done_steps, kern_ms, done_steps, how, serial_ms
+    how = (f"timed graphs of back-to-back matmul launches ({G} per graph, events around "
+           f"the region)")
+    return total_ms / steps, kern_ms, steps, how, serial_ms
 
 
 E2E_STREAMS = 2
@@ -709,7 +728,8 @@ def main():
                        "ntok": wl.ntok,
                        "l2": f"{wl.copies} rotating weight copies "
                              f"({wl.copies * wl.W[0].numel() / 1e6:.0f} MB > 2x 129 MB L2)",
-                       "timing": "CUDA graph of quantize+matmul steps, CUDA events"},
+                       "timing": f"CUDA graphs of {wl.copies * max(1, STEPS_PER_GRAPH // wl.copies)} "
+                                 f"quantize+matmul steps each, CUDA events"},
             "hbm_gbs": main_res["hbm_gbs_step"],
             "roofline": main_res["roofline"],
             "cpu_baseline": cpu,
