@@ -87,8 +87,9 @@ struct GemvArgs {
   int early_weights;  // 1: the previous kernel does not write Wtq; prefetch before waiting
   const float* X;     // fused form: f32 activations [T][cols] quantized here (else null)
   uint8_t* Xq_out;    // fused form: where the q8_K blocks are written (may be null)
-  int defer;          // 1: the inputs are final when the kernel starts; wait for the
-                      // previous kernel only before the first global write
+  int defer;          // the inputs are final when the kernel starts: wait for the
+                      // previous kernel only after the first tile column (1) or
+                      // after the first ring stage (2), before any global write
 };
 
 // Fused form: quantizes the T x cols f32 activations block by block (warp per
@@ -297,8 +298,9 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
   __syncthreads();
 
   // Deferred form: the wait (and the next kernel's start) comes after the
-  // first tile column's dot products, before any global write; then this
-  // CTA's share of the q8_K blocks goes out from the staged copy.
+  // first ring stage's or the first tile column's dot products, before any
+  // global write; then this CTA's share of the q8_K blocks goes out from the
+  // staged copy.
   bool waited = !a.defer;
   auto finish_wait = [&]() {
     pdl_wait_primary();
@@ -358,6 +360,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
         if (!failed && tl < nt) group_dot<T, kGroupSums>(c[u], gs + tl, sq, sgsum, sdx, a, row, y);
       }
       if (++slot == S) { slot = 0; phase ^= 1u; }
+      if (!waited && a.defer == 2) finish_wait();
     }
     if (!waited) finish_wait();
     if (!kGroupSums) {
@@ -778,13 +781,23 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
   }
 }
 
-// Whether a launch the host allowed to defer its wait (a.defer) does so: only
-// for Y outputs, and only when every CTA has two or more tile columns, so the
-// wait after the first one leaves the rest of the stream to overlap the
-// previous kernel's end; with a single column per CTA the wait would come at
-// the end and hold back the next kernel's start (measured slower).
-inline int defer_wait(const GemvArgs& a, bool group_sums, int grid) {
-  return a.defer && !group_sums && a.nrb >= 2 * grid ? 1 : 0;
+// Where a launch the host allowed to defer its wait (a.defer) waits: never
+// for group sums (stored per group); after the first ring stage when a tile
+// column takes three or more stages (the dp4a loop only); else after the
+// first tile column when every CTA has two or more, so the rest of its stream
+// overlaps the previous kernel's end. With a single short column per CTA the
+// wait would come at its end and hold back the next kernel's start. Measured
+// on GB300 in graph chains at one token: 5120 x 17408 (five stages per
+// column, one column per CTA) 11.4 -> 8.2 us waiting after the first stage;
+// 32768 x 8192 13.5 us after the first column, 13.8 after the first stage;
+// 5120 x 5120 (two stages, one column) slower either way; the mma.sync
+// variant slower waiting after a stage.
+inline int defer_wait(const GemvArgs& a, bool group_sums, int grid, int stage_tiles,
+                      bool after_stage_ok) {
+  if (!a.defer || group_sums) return 0;
+  const int per_rb = (a.ngroups + stage_tiles - 1) / stage_tiles;
+  if (after_stage_ok && per_rb >= 3) return 2;
+  return a.nrb >= 2 * grid ? 1 : 0;
 }
 
 template <int T, bool G, int TPW>
@@ -814,7 +827,7 @@ cudaError_t launch_mma(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
   for (int g = grid; g >= grid - grid / 4 && g >= 1; --g)
     if (a.nrb % g == 0) { grid = g; break; }
 #endif
-  a.defer = defer_wait(a, G, grid);
+  a.defer = defer_wait(a, G, grid, MmaCfg<T, TPW>::kStageTiles, false);
   return launch_pdl(kernel, dim3(grid), dim3(MmaCfg<T, TPW>::kThreads), (size_t)smem, s, a);
 }
 
@@ -849,7 +862,7 @@ cudaError_t launch_t(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
   for (int g = grid; g >= grid - grid / 4 && g >= 1; --g)
     if (a.nrb % g == 0) { grid = g; break; }
 #endif
-  a.defer = defer_wait(a, G, grid);
+  a.defer = defer_wait(a, G, grid, Cfg<T>::kStageTiles, true);
   return launch_pdl(kernel, dim3(grid), dim3(Cfg<T>::kThreads), (size_t)smem, s, a);
 }
 

@@ -47,40 +47,45 @@ def _bits(t):
     return t.view(torch.int32) if t.dtype == torch.float32 else t
 
 
-@pytest.mark.parametrize("ntok", [1, 3, 4, 8])
-def test_graph_chain_of_independent_calls(ntok):
+@pytest.mark.parametrize("rows,cols,ntok", [(ROWS, 1024, 1), (ROWS, 1024, 3), (ROWS, 1024, 4),
+                                             (ROWS, 1024, 8), (5120, 17408, 1), (5120, 17408, 3),
+                                             (5120, 17408, 4)])
+def test_graph_chain_of_independent_calls(rows, cols, ntok):
     """Four fused calls and two tq_matmul calls, each on its own weights, all
     reading activations no call of the chain writes (the fused calls share
-    one q8_K output buffer): the early-read form runs from the second call on."""
+    one q8_K output buffer): the early-read form runs from the second call on.
+    With 1024 columns every CTA has several tile columns and waits after its
+    first; 5120 x 17408 gives one long tile column per CTA, and the one- and
+    three-token kernels wait after its first ring stage."""
     import bit_matvec_gb300 as tq
-    cols, n = 1024, 4
-    wpq = [synth.pq2_0_weights(ROWS, cols, 40 + i) for i in range(n + 2)]
-    Ws = [gpu_repack(w, ROWS, cols) for w in wpq]
+    n = 4
+    wpq = [synth.pq2_0_weights(rows, cols, 40 + i) for i in range(n + 2)]
+    Ws = [gpu_repack(w, rows, cols) for w in wpq]
     x = _acts(ntok, cols, 41)
     X = torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
     Xq_in = gpu_quantize(_acts(ntok, cols, 42))
-    ws = tq.workspace_empty(ROWS, cols, ntok, DEV)
+    ws = tq.workspace_empty(rows, cols, ntok, DEV)
 
     def run(s, Ys, Xq):
         for i in range(n):
-            tq.tq_quantize_matmul(Ws[i], X, Xq, Ys[i], ROWS, cols, ntok, ws, stream=s)
+            tq.tq_quantize_matmul(Ws[i], X, Xq, Ys[i], rows, cols, ntok, ws, stream=s)
         for i in range(2):
-            tq.tq_matmul(Ws[n + i], Xq_in, Ys[n + i], ROWS, cols, ntok, stream=s)
+            tq.tq_matmul(Ws[n + i], Xq_in, Ys[n + i], rows, cols, ntok, stream=s)
 
     # one call at a time
     refs = []
     Xq_ref = tq.q8K_empty(ntok, cols, DEV)
     for i in range(n + 2):
-        Y = torch.empty((ntok, ROWS), device=DEV)
+        Y = torch.empty((ntok, rows), device=DEV)
         if i < n:
-            tq.tq_quantize_matmul(Ws[i], X, Xq_ref, Y, ROWS, cols, ntok, ws)
+            tq.tq_quantize_matmul(Ws[i], X, Xq_ref, Y, rows, cols, ntok, ws)
         else:
-            tq.tq_matmul(Ws[i], Xq_in, Y, ROWS, cols, ntok)
+            tq.tq_matmul(Ws[i], Xq_in, Y, rows, cols, ntok)
         torch.cuda.synchronize()
         refs.append(Y)
     assert torch.equal(Xq_ref, gpu_quantize(x))
 
-    Ys = [torch.full((ntok, ROWS), float("nan"), device=DEV) for _ in range(n + 2)]
+    Ys = [torch.full((ntok, rows), float("nan"), device=DEV) for _ in range(n + 2)]
     Xq = torch.full_like(Xq_ref, 0xEE)
     g = _capture(lambda s: run(s, Ys, Xq))
     for _ in range(3):
@@ -97,8 +102,8 @@ def test_graph_chain_of_independent_calls(ntok):
     # and against the oracle, for the first and the last weights
     xq = oracle.quantize_q8K(x)
     for i in (0, n - 1):
-        rows_s = np.r_[0:64, ROWS - 64:ROWS]
-        y_ref, abs_sum = oracle.matmul(wpq[i].reshape(ROWS, -1)[rows_s].reshape(-1), xq,
+        rows_s = np.r_[0:64, rows - 64:rows]
+        y_ref, abs_sum = oracle.matmul(wpq[i].reshape(rows, -1)[rows_s].reshape(-1), xq,
                                        len(rows_s), cols)
         assert_close(refs[i].cpu().numpy()[:, rows_s], y_ref, abs_sum)
 
