@@ -943,16 +943,35 @@ cudaError_t launch_gemv(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t
   a.Xq_out = Xq_out;
   a.defer = inputs_final ? 1 : 0;
   const bool gsum = S != nullptr;
+  cudaError_t e;
   switch (ntok) {
-    case 1: return launch_tok<1>(a, cols, gsum, s);
-    case 2: return launch_tok<2>(a, cols, gsum, s);
-    case 3: return launch_tok<3>(a, cols, gsum, s);
-    case 4: return launch_tok<4>(a, cols, gsum, s);
-    case 5: return launch_tok<5>(a, cols, gsum, s);
-    case 6: return launch_tok<6>(a, cols, gsum, s);
-    case 7: return launch_tok<7>(a, cols, gsum, s);
-    default: return launch_tok<8>(a, cols, gsum, s);
+    case 1: e = launch_tok<1>(a, cols, gsum, s); break;
+    case 2: e = launch_tok<2>(a, cols, gsum, s); break;
+    case 3: e = launch_tok<3>(a, cols, gsum, s); break;
+    case 4: e = launch_tok<4>(a, cols, gsum, s); break;
+    case 5: e = launch_tok<5>(a, cols, gsum, s); break;
+    case 6: e = launch_tok<6>(a, cols, gsum, s); break;
+    case 7: e = launch_tok<7>(a, cols, gsum, s); break;
+    default: e = launch_tok<8>(a, cols, gsum, s); break;
   }
+  if (e != cudaErrorNotSupported || ntok == 1) return e;
+  // The activations of all tokens do not fit in shared memory (long rows:
+  // 8 tokens of 17408 columns): one launch per half of the tokens, each
+  // streaming the weights once, instead of the tensor-core path for a tile
+  // of 64 tokens. Every token's inputs and outputs are contiguous rows, and
+  // each half's arithmetic is that of a call with those tokens alone. The
+  // first half fits whenever the second does (fewer tokens need less shared
+  // memory), so either both launch or neither does.
+  const int n0 = (ntok + 1) / 2;
+  e = launch_gemv(Wtq, Xq, Y, S, rows, cols, n0, dev_status, early_weights, inputs_final, s, X,
+                  Xq_out);
+  if (e != cudaSuccess) return e;
+  // the first half's kernel writes no weights and none of the second half's inputs
+  return launch_gemv(Wtq, Xq ? Xq + (int64_t)n0 * a.nblk * kQ8KBytes : nullptr,
+                     Y ? Y + (int64_t)n0 * rows : nullptr,
+                     S ? S + (int64_t)n0 * rows * a.ngroups : nullptr, rows, cols, ntok - n0,
+                     dev_status, true, false, s, X ? X + (int64_t)n0 * cols : nullptr,
+                     Xq_out ? Xq_out + (int64_t)n0 * a.nblk * kQ8KBytes : nullptr);
 }
 
 }  // namespace tq

@@ -160,8 +160,11 @@ int tq_repack_ptq1_0(const void *Wpt, void *Wtq, int64_t rows, int64_t cols, voi
  * 1e-5 of sum_g |d_w d_x isum| of the exact value.
  * Routing by ntok (post, "the leftovers": never one weight pass per leftover
  * token): ntok <= 8 runs a bandwidth-bound GEMV that reads the weights once
- * for all tokens; larger ntok runs a tcgen05 tensor-core kernel with the
- * token dimension zero-padded to its tile, storing only the real outputs.
+ * for all tokens (once per half of them where the activations of all do not
+ * fit in shared memory, as 8 tokens of 17408 columns; the tensor-core path
+ * only where not even one token's do); larger ntok runs a tcgen05
+ * tensor-core kernel with the token dimension zero-padded to its tile,
+ * storing only the real outputs.
  *   Wtq [tq layout] repacked weights, 16-byte aligned.
  *   Xq  [ntok][cols/256] q8_K blocks, 16-byte aligned.
  *   Y   [ntok][rows] f32, 4-byte aligned, overwritten (not accumulated).

@@ -112,13 +112,15 @@ def test_gemv_groupsums_exact_matmul_close(rows, cols, ntok):
 
 
 @pytest.mark.parametrize("rows,cols,ntok", [(64, 8192, 4), (64, 8192, 8), (96, 16384, 6),
-                                             (64, 5120, 5), (100, 5120, 8), (40, 6144, 4)])
+                                             (64, 5120, 5), (100, 5120, 8), (40, 6144, 4),
+                                             (64, 17408, 8), (40, 32768, 5), (33, 65536, 3)])
 def test_gemv_wide_rows(rows, cols, ntok):
     """Long rows: from 4 tokens the tensor-core (mma.sync) variant runs while its
     f16 activations fit in shared memory (8 x 8192 do not: the dp4a loop takes
     over); 16384 columns at 6 tokens exercise the largest staged activations;
     5120 and 6144 columns (40 and 48 groups) take three tiles per warp and
-    stage, the others two."""
+    stage, the others two. Where no variant fits all tokens (8 x 17408,
+    5 x 32768, 3 x 65536) the GEMV runs once per half of the tokens."""
     _check_product(rows, cols, ntok)
 
 
@@ -240,7 +242,8 @@ def test_concurrent_streams():
 
 
 @pytest.mark.parametrize("rows,cols,ntok", [(300, 1024, 1), (100, 768, 3), (300, 1024, 4),
-                                             (64, 8192, 8), (32, 256, 8), (128, 1024, 9),
+                                             (64, 8192, 8), (32, 256, 8), (64, 17408, 8),
+                                             (128, 1024, 9),
                                              (100, 512, 64), (300, 1024, 65), (160, 2048, 130)])
 def test_quantize_matmul_equals_separate_calls(rows, cols, ntok):
     """The fused call gives the bits of tq_quantize_q8K + tq_matmul_ws: Xq and Y
