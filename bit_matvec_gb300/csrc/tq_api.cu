@@ -3,6 +3,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <unordered_map>
 #include <utility>
 
@@ -233,6 +234,50 @@ cudaError_t ensure_dynamic_smem(const void* kernel, int bytes) {
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
   if (e != cudaSuccess) return e;
   g_smem_optin[key] = optin;
+  return cudaSuccess;
+}
+
+cudaError_t device_limits(DeviceLimits* out) {
+  static DeviceLimits limits[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceLimits& l = limits[dev];
+  if (l.sms == 0) {
+    int optin = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+            cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
+    l.optin_smem = optin;
+    l.sms = sms;
+  }
+  *out = l;
+  return cudaSuccess;
+}
+
+cudaError_t resident_ctas(const void* kernel, int threads, size_t smem, int* out) {
+  static std::map<std::tuple<int, const void*, int, size_t>, int> cache;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const auto key = std::make_tuple(dev, kernel, threads, smem);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      *out = it->second;
+      return cudaSuccess;
+    }
+  }
+  int n = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_mu);
+  cache[key] = n;
+  *out = n;
   return cudaSuccess;
 }
 

@@ -24,8 +24,14 @@
 //     minus the sum of the group's activations from the q8_K partial sums turns
 //     u back into w (dot(w,y) = dot(u,y) - sum(y)), and one f32 FMA applies
 //     d_w * d_x;
-//   - launched as a programmatic dependent: when the previous kernel is the
-//     quantizer, the first weight stages are requested before waiting for it.
+//   - launched as a programmatic dependent: when the previous kernel writes no
+//     weights, the first weight stages are requested before waiting for it;
+//     a GEMV lets the next kernel start only after its own wait, so in a
+//     captured chain of GEMVs whose inputs the previous GEMV does not write,
+//     the host lets a launch read everything first and wait only before its
+//     first store (launch_gemv, defer_wait);
+//   - where the activations of all tokens do not fit in shared memory, one
+//     launch per half of the tokens.
 #include <algorithm>
 
 #include "tq_tcgen05.cuh"
@@ -804,13 +810,10 @@ template <int T, bool G, int TPW>
 cudaError_t launch_mma(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
   auto kernel = gemv_mma_kernel<T, G, TPW>;
   GemvArgs a = a0;
-  int dev = 0, optin = 0, nsm = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  DeviceLimits lim;
+  cudaError_t e = device_limits(&lim);
   if (e != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
-          cudaSuccess ||
-      (e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-    return e;
+  const int optin = lim.optin_smem, nsm = lim.sms;
   int stages = TQ_GEMV_MAX_STAGES;
   while (stages > 2 && plan_mma<T, TPW>(stages, cols).total > optin) --stages;
   const int64_t smem = plan_mma<T, TPW>(stages, cols).total;
@@ -819,7 +822,8 @@ cudaError_t launch_mma(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
   e = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), (int)smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, MmaCfg<T, TPW>::kThreads, (size_t)smem);
+  e = resident_ctas(reinterpret_cast<const void*>(kernel), MmaCfg<T, TPW>::kThreads, (size_t)smem,
+                    &per_sm);
   if (e != cudaSuccess) return e;
   per_sm = max(1, min(per_sm, TQ_GEMV_CTAS_PER_SM));
   int grid = (int)std::min<int64_t>(a.nrb, (int64_t)nsm * per_sm);
@@ -836,13 +840,10 @@ cudaError_t launch_t(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
   static_assert(T >= 1 && T <= kMaxTok, "token count");
   auto kernel = gemv_kernel<T, G>;
   GemvArgs a = a0;
-  int dev = 0, optin = 0, nsm = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  DeviceLimits lim;
+  cudaError_t e = device_limits(&lim);
   if (e != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
-          cudaSuccess ||
-      (e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-    return e;
+  const int optin = lim.optin_smem, nsm = lim.sms;
   // deepest ring that fits
   int stages = TQ_GEMV_MAX_STAGES;
   while (stages > 2 && plan_smem<T>(stages, cols).total > optin) --stages;
@@ -852,7 +853,7 @@ cudaError_t launch_t(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
   e = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), (int)smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, Cfg<T>::kThreads, (size_t)smem);
+  e = resident_ctas(reinterpret_cast<const void*>(kernel), Cfg<T>::kThreads, (size_t)smem, &per_sm);
   if (e != cudaSuccess) return e;
   per_sm = max(1, min(per_sm, TQ_GEMV_CTAS_PER_SM));
   int grid = (int)std::min<int64_t>(a.nrb, (int64_t)nsm * per_sm);

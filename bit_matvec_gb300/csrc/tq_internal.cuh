@@ -267,6 +267,19 @@ cudaError_t launch_quantize_gemm_tc_ws(const float* X, uint8_t* Xq, const uint8_
 // Opt a kernel in to `bytes` of dynamic shared memory on the current device
 // (cached per device and kernel).
 cudaError_t ensure_dynamic_smem(const void* kernel, int bytes);
+
+// The current device's opt-in shared memory per block and SM count, read from
+// the driver once per device.
+struct DeviceLimits {
+  int optin_smem;
+  int sms;
+};
+cudaError_t device_limits(DeviceLimits* out);
+
+// CTAs of kernel (threads per CTA, dynamic shared memory smem) that fit on one
+// SM of the current device, asked of the driver once per device, kernel,
+// block size and shared memory size (the answer never changes).
+cudaError_t resident_ctas(const void* kernel, int threads, size_t smem, int* out);
 // Record e as this host thread's tq_last_cuda_error.
 void record_cuda_error(cudaError_t e);
 
