@@ -71,6 +71,8 @@ def parse_args():
     p.add_argument("--workload", default="decode", choices=list(WORKLOADS))
     p.add_argument("--no-extra", action="store_true", help="skip the 4- and 64-token tiles")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--e2e-streams", type=int, default=4,
+                   help="streams the end-to-end steps alternate over (requests in flight)")
     p.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     p.add_argument("--no-replay", action="store_true",
                    help="skip the 64-block decode-step replay (ntok 1 and 512)")
@@ -433,20 +435,17 @@ def time_graph(wl: Workload, steps: int, warmup: int, world: int):
     return total_ms / steps, kern_ms, steps, how, serial_ms
 
 
-E2E_STREAMS = 2
-
-
-def time_e2e(wl: Workload, steps: int, warmup: int):
+def time_e2e(wl: Workload, steps: int, warmup: int, nstreams: int):
     """Through the C ABI with host buffers: one tq_matmul_host call per step
     (pinned host X -> device, quantize, matmul, device -> pinned host Y). Steps
-    alternate over E2E_STREAMS streams, each with its own host and device
+    alternate over nstreams streams, each with its own host and device
     buffers, as a server pipelines independent requests: one step's copies run
     while another step's kernels do; every step still copies its own input in
     and its own result out."""
     import torch
     import bit_matvec_gb300 as tq
     lanes = []
-    for _ in range(E2E_STREAMS):
+    for _ in range(nstreams):
         lanes.append({
             "stream": torch.cuda.Stream(wl.device),
             "x_pin": torch.from_numpy(wl.x_host).pin_memory(),
@@ -455,7 +454,7 @@ def time_e2e(wl: Workload, steps: int, warmup: int):
             "Y": torch.empty_like(wl.Y), "ws": torch.empty_like(wl.ws)})
 
     def one(i):
-        ln = lanes[i % E2E_STREAMS]
+        ln = lanes[i % nstreams]
         tq.tq_matmul_host(wl.W[i % wl.copies], ln["x_pin"], ln["X"], ln["Xq"], ln["Y"],
                           ln["y_pin"], wl.rows, wl.cols, wl.ntok, ln["ws"], ln["stream"])
 
@@ -696,15 +695,15 @@ def main():
     e2e = None
     if not args.no_e2e:
         e2e_steps = max(100, min(args.steps, 5000))
-        s_per_step, h2d, d2h = time_e2e(wl, e2e_steps, args.warmup)
+        s_per_step, h2d, d2h = time_e2e(wl, e2e_steps, args.warmup, args.e2e_streams)
         s_per_step = max_over_ranks(s_per_step, world, device)
         units = wl.weights() if wl.ntok == 1 else wl.macs()
         e2e = {"value": world * units / s_per_step / 1e9,
                "unit": "Gweights/s" if wl.ntok == 1 else "GMAC/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-               "ms_per_step": s_per_step * 1e3, "streams": E2E_STREAMS,
+               "ms_per_step": s_per_step * 1e3, "streams": args.e2e_streams,
                "how": "tq_matmul_host per step from pinned host X to pinned host Y; "
-                      f"steps alternate over {E2E_STREAMS} streams with their own buffers; "
+                      f"steps alternate over {args.e2e_streams} streams with their own buffers; "
                       "host wall clock around all steps"}
 
     cpu = None
