@@ -61,6 +61,8 @@ def header_functions() -> list[str]:
 
 def _load():
     global _lib
+    if _lib is not None:   # loaded: no lock on the per-call path
+        return _lib
     with _lock:
         if _lib is not None:
             return _lib
@@ -110,13 +112,13 @@ def _ptr(t: torch.Tensor | None):
         raise ValueError("tensor must live on a CUDA device")
     if not t.is_contiguous():
         raise ValueError("tensor must be contiguous")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()   # an int; the declared argtypes make it a void*
 
 
 def _stream(stream, device):
     if stream is None:
         stream = torch.cuda.current_stream(device)
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream
 
 
 def _call(name, device, *args):
@@ -239,7 +241,7 @@ def _host_ptr(t: torch.Tensor):
         raise ValueError("tensor must live in host memory")
     if not t.is_contiguous():
         raise ValueError("tensor must be contiguous")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
 def tq_matmul_host(Wtq: torch.Tensor, X_host: torch.Tensor, X: torch.Tensor, Xq: torch.Tensor,
