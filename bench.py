@@ -46,6 +46,8 @@ import synth  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
 PAGES_DECODE_GWEIGHTS = 390.5   # ciot README: t2x4 NEON, 32768 x 8192 matvec, 8 Oryon cores
+# GB300 HBM3e nominal bandwidth (GB/s): context beside the measured copy peak.
+HBM_NOMINAL_GBS = 7900.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # The tensor-core matmul runs e4m3 MMAs: its peak is the measured bf16 dense
 # rate times the nominal e4m3 : bf16 ratio (4.5 : 2.25 PFLOP/s dense). It
@@ -324,6 +326,7 @@ def measure_replay(ntok, steps, warmup, world, device, peaks, peak_kind):
         peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         res["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                            "frac": achieved / peak, "peak_source": peak_kind,
+                           "frac_of_nominal": achieved / HBM_NOMINAL_GBS,
                            "note": "whole step (quantize + matmul launches) over algorithmic bytes"}
     else:
         res["gmac_per_s"] = world * wl.weights() * ntok / (ms * 1e-3) / 1e9
@@ -600,6 +603,7 @@ def measure(name, args, rank, world, device, peaks, peak_kind, steps):
         traffic = profile_traffic(f"gemv_{name}_ncu.txt", GEMV_FILES)
         res["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                            "frac": achieved / peak, "traffic": traffic,
+                           "frac_of_nominal": achieved / HBM_NOMINAL_GBS,
                            "kernel": "gemv_kernel (quantize fused in)", "kernel_ms": kern_ms,
                            "kernel_timing": kern_how,
                            "kernel_ms_serialised": serial_ms,
