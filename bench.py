@@ -349,6 +349,15 @@ def measure_replay(ntok, steps, warmup, world, device, peaks, peak_kind):
 STEPS_PER_GRAPH = 40
 
 
+def graph_plan(steps: int, copies: int):
+    """(G, replays of the G-step graph, steps left for a second graph): G is the
+    largest multiple of `copies` up to STEPS_PER_GRAPH (at least `copies`), and
+    replays * G + rest == steps exactly."""
+    G = copies * max(1, STEPS_PER_GRAPH // copies)
+    reps, rest = divmod(steps, G)
+    return G, reps, rest
+
+
 def time_graph(wl: Workload, steps: int, warmup: int, world: int):
     """Device time per step, and the matmul kernel's average launch duration.
 
@@ -377,8 +386,7 @@ def time_graph(wl: Workload, steps: int, warmup: int, world: int):
 
     ev = [(timing_event(), timing_event()) for _ in range(n)]
 
-    G = n * max(1, STEPS_PER_GRAPH // n)
-    reps, rest = divmod(steps, G)
+    G, reps, rest = graph_plan(steps, n)
 
     def timed(graph, graph_rest):
         start = torch.cuda.Event(enable_timing=True)
@@ -731,7 +739,7 @@ def main():
                        "ntok": wl.ntok,
                        "l2": f"{wl.copies} rotating weight copies "
                              f"({wl.copies * wl.W[0].numel() / 1e6:.0f} MB > 2x 129 MB L2)",
-                       "timing": f"CUDA graphs of {wl.copies * max(1, STEPS_PER_GRAPH // wl.copies)} "
+                       "timing": f"CUDA graphs of {graph_plan(args.steps, wl.copies)[0]} "
                                  f"quantize+matmul steps each, CUDA events"},
             "hbm_gbs": main_res["hbm_gbs_step"],
             "roofline": main_res["roofline"],

@@ -88,3 +88,30 @@ def test_reference_arm_prints_one_json_line():
     sys.path.insert(0, ROOT)
     import bench
     assert d["metric"] == bench.metric_name("Gweights/s", "decode")   # the GPU arm's string
+
+
+def test_graph_plan_times_exactly_the_requested_steps():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.graph_plan(20000, 5) == (40, 500, 0)     # decode: 5 weight copies
+    assert bench.graph_plan(2002, 13) == (39, 51, 13)     # 13 copies of a 24 MB matrix
+    assert bench.graph_plan(20, 5) == (40, 0, 20)         # fewer steps than one graph
+    assert bench.graph_plan(7, 64) == (64, 0, 7)          # more copies than the graph size
+    for steps in range(1, 300, 7):
+        for copies in (2, 5, 13, 41, 64):
+            G, reps, rest = bench.graph_plan(steps, copies)
+            assert G % copies == 0 and G >= copies and 0 <= rest < G
+            assert reps * G + rest == steps
+
+
+def test_e2e_streams_option():
+    sys.path.insert(0, ROOT)
+    import bench
+    argv = sys.argv
+    try:
+        sys.argv = ["bench.py"]
+        assert bench.parse_args().e2e_streams == 4
+        sys.argv = ["bench.py", "--e2e-streams", "2"]
+        assert bench.parse_args().e2e_streams == 2
+    finally:
+        sys.argv = argv
