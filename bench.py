@@ -30,6 +30,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -563,11 +564,20 @@ def run_reference(args, rank, world):
 
 # ---------------------------------------------------------------- profile evidence
 
+def code_text(src: str) -> str:
+    """C/CUDA source without its comments (no string literal in the kernel
+    sources holds a comment marker): what the compiler sees of it."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return re.sub(r"//[^\n]*", "", src)
+
+
 def kernel_source_sha(files):
+    """Hash of the kernel sources' code (comments stripped), so a profile taken
+    on a kernel stays valid across comment-only edits."""
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "bit_matvec_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "bit_matvec_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(code_text(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

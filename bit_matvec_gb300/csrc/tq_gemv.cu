@@ -961,8 +961,9 @@ cudaError_t launch_gemv(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t
   // streaming the weights once, instead of the tensor-core path for a tile
   // of 64 tokens. Every token's inputs and outputs are contiguous rows, and
   // each half's arithmetic is that of a call with those tokens alone. The
-  // first half fits whenever the second does (fewer tokens need less shared
-  // memory), so either both launch or neither does.
+  // second half has no more tokens than the first, so it fits whenever the
+  // first does (fewer tokens need less shared memory): either both launch or
+  // neither does.
   const int n0 = (ntok + 1) / 2;
   e = launch_gemv(Wtq, Xq, Y, S, rows, cols, n0, dev_status, early_weights, inputs_final, s, X,
                   Xq_out);

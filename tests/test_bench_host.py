@@ -115,3 +115,14 @@ def test_e2e_streams_option():
         assert bench.parse_args().e2e_streams == 2
     finally:
         sys.argv = argv
+
+
+def test_source_hash_ignores_comments():
+    sys.path.insert(0, ROOT)
+    import bench
+    a = "int f(int x) {  // one\n  return x; /* two\n lines */ }\n"
+    b = "int f(int x) {  // other words\n  return x; /* x */ }\n"
+    c = "int f(int x) {\n  return x + 1; }\n"
+    assert bench.code_text(a) == bench.code_text(b)
+    assert bench.code_text(a) != bench.code_text(c)
+    assert "return x;" in bench.code_text(a) and "one" not in bench.code_text(a)
