@@ -181,11 +181,14 @@ int tq_repack_ptq1_0(const void *Wpt, void *Wtq, int64_t rows, int64_t cols, voi
  * the capture is the previous call's GEMV node (nothing else was captured
  * between them), and none of whose inputs (Wtq, Xq, or X for
  * tq_quantize_matmul) overlaps that GEMV's outputs (Y or S, and Xq it
- * wrote), reads its inputs before waiting, and waits only before its first
- * store, when every CTA has two or more 32-row tile columns (the one-token
- * decode matrices). Back-to-back decode matmuls in a graph then overlap
- * each other's start and end. Outside a capture the library cannot see what
- * else is on the stream and always waits first.
+ * wrote), reads its inputs before waiting and waits only before its first
+ * store: after its first ring stage where a 32-row tile column takes three
+ * or more stages (more than 8192 columns at 1 to 3 tokens), else after its
+ * first tile column where every CTA has two or more (the 32768 x 8192 decode
+ * matrix), else at its start as usual; the group-sum form always waits
+ * first. Back-to-back decode matmuls in a graph then overlap each other's
+ * start and end. Outside a capture the library cannot see what else is on
+ * the stream and always waits first.
  * Errors: TQ_ERR_SHAPE if cols % 256 != 0; TQ_ERR_ALIAS if Y overlaps an input.
  */
 int tq_matmul(const void *Wtq, const void *Xq, float *Y, int64_t rows, int64_t cols,
