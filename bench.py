@@ -79,6 +79,8 @@ def parse_args():
     p.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     p.add_argument("--no-replay", action="store_true",
                    help="skip the 64-block decode-step replay (ntok 1 and 512)")
+    p.add_argument("--no-read-ceiling", action="store_true",
+                   help="skip the read-ceiling probe beside the GEMV's roofline")
     p.add_argument("--tensor-rates", action="store_true",
                    help="only measure library int8 / bf16 / f16 GEMM rates (operand-type choice)")
     return p.parse_args()
@@ -344,6 +346,49 @@ def measure_replay(ntok, steps, warmup, world, device, peaks, peak_kind):
     return res
 
 
+def measure_read_ceiling(nbytes, device, warmup):
+    """Read rate of the probe kernel (tq_probe_read_sum: a streaming sum, no
+    other work) over buffers of nbytes rotating through more than twice the
+    L2, in graphs of back-to-back launches: 'chained' lets each launch read
+    before the previous one ends (as the independent GEMV chain does), and
+    'wait_first' makes each wait for it first."""
+    import torch
+    import bit_matvec_gb300 as tq
+    copies = max(2, -(-2 * L2_BYTES // nbytes) + 1)
+    bufs = [torch.full((nbytes // 4,), i + 1, dtype=torch.int32, device=device)
+            for i in range(copies)]
+    out = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.Stream(device=device)
+    stream.wait_stream(torch.cuda.current_stream(device))
+    G = copies * max(1, STEPS_PER_GRAPH // copies)
+    res = {"bytes": nbytes, "copies": copies}
+    with torch.cuda.stream(stream):
+        for early in (True, False):
+            for i in range(copies):
+                tq.tq_probe_read_sum(bufs[i], out, early, stream)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(G):
+                    tq.tq_probe_read_sum(bufs[i % copies], out, early, stream)
+            for _ in range(max(3, warmup // G + 1)):
+                g.replay()
+            stream.synchronize()
+            reps = max(5, int(2e9 // (nbytes * G)))
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+            stream.synchronize()
+            us = a.elapsed_time(b) / (reps * G) * 1e3
+            res["chained" if early else "wait_first"] = {"us": us, "gbs": nbytes / us / 1e3}
+    del bufs
+    torch.cuda.empty_cache()
+    return res
+
+
 # Steps per captured graph (a multiple of the weight copies): a decode graph
 # holds many matmuls back to back, and consecutive kernels overlap only within
 # one graph launch.
@@ -389,6 +434,24 @@ def time_graph(wl: Workload, steps: int, warmup: int, world: int):
 
     G, reps, rest = graph_plan(steps, n)
 
+    # Dependent chain: step k > 0 of a graph quantizes the previous step's
+    # output (its first ntok x cols values) instead of the seeded activations,
+    # so each launch must wait for the one before it before reading them (its
+    # weights, which no step writes, may still be requested first). Two output
+    # buffers alternate; every graph launch starts again from the seeded X.
+    import bit_matvec_gb300 as tq_mod
+    need = wl.ntok * wl.cols
+    if wl.ntok * wl.rows >= need:
+        Yd = [torch.empty_like(wl.Y) for _ in range(2)]
+
+        def dep_step(i, s):
+            k = i % G
+            X = wl.X if k == 0 else Yd[(k - 1) % 2].view(-1)[:need].view(wl.ntok, wl.cols)
+            tq_mod.tq_quantize_matmul(wl.W[i % wl.copies], X, wl.Xq, Yd[k % 2], wl.rows, wl.cols,
+                                      wl.ntok, wl.ws, s)
+    else:
+        dep_step = None
+
     def timed(graph, graph_rest):
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
@@ -416,6 +479,8 @@ def time_graph(wl: Workload, steps: int, warmup: int, world: int):
         stream.synchronize()
         ga, ga_rest = capture(wl.step, G), capture(wl.step, rest)
         gm, gm_rest = capture(wl.matmul_only, G), capture(wl.matmul_only, rest)
+        gd, gd_rest = ((capture(dep_step, G), capture(dep_step, rest)) if dep_step
+                       else (None, None))
         gb = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gb, stream=stream):
             for i in range(n):
@@ -424,10 +489,11 @@ def time_graph(wl: Workload, steps: int, warmup: int, world: int):
                 ev[i][0].record(stream)
                 wl.matmul_only(i, stream)
                 ev[i][1].record(stream)
-        for g in (ga, gm, gb):                          # graph warm-up replays
-            for _ in range(max(1, -(-warmup // G))):
-                g.replay()
-        for g in (ga_rest, gm_rest):
+        for g in (ga, gm, gb, gd):                      # graph warm-up replays
+            if g is not None:
+                for _ in range(max(1, -(-warmup // G))):
+                    g.replay()
+        for g in (ga_rest, gm_rest, gd_rest):
             if g is not None:
                 g.replay()
         stream.synchronize()
@@ -435,6 +501,7 @@ def time_graph(wl: Workload, steps: int, warmup: int, world: int):
         torch.cuda.synchronize(wl.device)
         total_ms = timed(ga, ga_rest)
         kern_ms = timed(gm, gm_rest) / steps
+        dep_ms = timed(gd, gd_rest) / steps if gd is not None else None
         gb.replay()
         stream.synchronize()
         try:
@@ -444,7 +511,7 @@ def time_graph(wl: Workload, steps: int, warmup: int, world: int):
         barrier(world)
     how = (f"timed graphs of back-to-back matmul launches ({G} per graph, events around "
            f"the region)")
-    return total_ms / steps, kern_ms, steps, how, serial_ms
+    return total_ms / steps, kern_ms, steps, how, serial_ms, dep_ms
 
 
 def time_e2e(wl: Workload, steps: int, warmup: int, nstreams: int):
@@ -483,33 +550,96 @@ def time_e2e(wl: Workload, steps: int, warmup: int, nstreams: int):
 
 # ---------------------------------------------------------------- oracle timing
 
-def oracle_rate(name: str, budget_s: float, rows_per_call: int | None = None):
-    """The C oracle (single-threaded) on a row sample of the workload.
+def cpu_info():
+    """Host cores and CPU model of the machine the oracle is timed on."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                             text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name:"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for ln in f:
+                    if ln.lower().startswith(("model name", "cpu part")):
+                        model = ln.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    import platform
+    return {"nproc": os.cpu_count(), "model": model, "machine": platform.machine()}
 
-    Returns (units per second, unit, sample description, cores)."""
+
+def _timed_loop(fn, budget_s):
+    """Seconds per call of fn, repeated until budget_s has passed (at least once)."""
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    return (time.perf_counter() - t0) / n, n
+
+
+def oracle_matrix_time(rows, cols, ntok, x, seed_index, budget_s):
+    """Estimated single-core seconds of the oracle for quantize + matmul of the
+    whole rows x cols matrix: the quantizer timed on all of x, the matmul on a
+    sample of rows scaled up by rows / sample (the matmul's time is linear in
+    the rows). Returns (seconds, description)."""
     import oracle
+    oracle.build()
+    rpc = max(1, min(rows, (1 << 22) // (cols * ntok)))
+    wsub = synth.pq2_0_weights(rpc, cols, seed_index)
+    t_q, n_q = _timed_loop(lambda: oracle.quantize_q8K(x), budget_s * 0.2)
+    xq = oracle.quantize_q8K(x)
+    t_m, n_m = _timed_loop(lambda: oracle.matmul(wsub, xq, rpc, cols), budget_s * 0.8)
+    est = t_q + t_m * rows / rpc
+    return est, (f"quantize {ntok}x{cols} timed whole ({n_q} calls); matmul timed on {rpc} of "
+                 f"{rows} rows ({n_m} calls) and scaled by {rows / rpc:.1f}")
+
+
+def oracle_rate(name: str, budget_s: float):
+    """The C oracle (single-threaded) on a workload: units per second,
+    estimated from a row sample (oracle_matrix_time). Returns (rate, unit,
+    sample description, cores used, seconds per full step)."""
     cfg = synth.CONFIGS[name]
     rows, cols, ntok = cfg["rows"], cfg["cols"], cfg["ntok"]
     s = synth.seeds(cfg["index"])
     x = synth.activations(ntok, cols, s["acts"], s["outliers"] if cfg["outliers"] else None)
-    if rows_per_call is None:
-        rows_per_call = max(1, min(rows, (1 << 22) // (cols * ntok)))
-    wsub = synth.pq2_0_weights(rows_per_call, cols, cfg["index"])
-    oracle.build()
-    n = 0
-    t0 = time.perf_counter()
-    while True:
-        xq = oracle.quantize_q8K(x)
-        oracle.matmul(wsub, xq, rows_per_call, cols)
-        n += 1
-        if time.perf_counter() - t0 >= budget_s:
-            break
-    dt = time.perf_counter() - t0
-    work = n * rows_per_call * cols * (ntok if ntok > 1 else 1)
+    est, how = oracle_matrix_time(rows, cols, ntok, x, cfg["index"], budget_s)
     unit = "Gweights/s" if ntok == 1 else "GMAC/s"
-    sample = (f"{n} calls x {rows_per_call} of {rows} rows, {cols} cols, ntok={ntok} "
-              f"(quantize + matmul each), {dt:.1f} s")
-    return work / dt / 1e9, unit, sample, 1, dt / n, rows_per_call
+    return rows * cols * ntok / est / 1e9, unit, how, 1, est
+
+
+def oracle_replay_rate(ntok: int, budget_s: float, blocks=None):
+    """The oracle on one decode-step replay: per matrix of a block, quantize +
+    matmul estimated from a row sample; times the blocks. Returns (rate, unit,
+    sample description, cores used, seconds per step)."""
+    blocks = blocks or synth.REPLAY_BLOCKS
+    total, weights, parts = 0.0, 0, []
+    for m in range(len(synth.REPLAY_BLOCK)):
+        _, x, rows, cols = synth.replay_matrix(m, ntok, rows=1)
+        est, how = oracle_matrix_time(rows, cols, ntok, x, 0x100 + m,
+                                      budget_s / len(synth.REPLAY_BLOCK))
+        total += est
+        weights += rows * cols
+        parts.append(f"{rows}x{cols}: {how}")
+    total *= blocks
+    weights *= blocks
+    unit = "Gweights/s" if ntok == 1 else "GMAC/s"
+    return (weights * ntok / total / 1e9, unit,
+            f"{blocks} blocks x 5 matrices, each estimated as: " + "; ".join(parts), 1, total)
+
+
+def cpu_baseline_entry(rate, unit, sample, cores, step_s):
+    return {"value": rate, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample,
+            "s_per_step": step_s, "host": cpu_info()}
 
 
 def metric_name(unit, name):
@@ -524,8 +654,7 @@ def run_reference(args, rank, world):
     name = args.workload
     cfg = synth.CONFIGS[name]
     # calibrate a per-step row sample so that warm-up + steps take about a minute
-    _, _, _, _, per_call, rpc = oracle_rate(name, 1.0)
-    per_row = per_call / rpc
+    per_row = oracle_rate(name, 1.0)[4] / cfg["rows"]
     total = max(1, args.steps + args.warmup)
     rows_step = int(max(1, min(cfg["rows"], 60.0 / total / per_row)))
     import oracle
@@ -555,7 +684,7 @@ def run_reference(args, rank, world):
         "config": {"workload": WORKLOADS[name], "rows": cfg["rows"], "cols": cfg["cols"],
                    "ntok": ntok, "sample_rows": rows_step},
         "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "host": cpu_info()},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -605,7 +734,8 @@ TC_FILES = ("tq_gemm_tc_ws.cu", "tq_tcgen05.cuh", "tq_internal.cuh")
 
 def measure(name, args, rank, world, device, peaks, peak_kind, steps):
     wl = Workload(name, device)
-    step_ms, kern_ms, done, kern_how, serial_ms = time_graph(wl, steps, args.warmup, world)
+    step_ms, kern_ms, done, kern_how, serial_ms, dep_ms = time_graph(wl, steps, args.warmup,
+                                                                      world)
     step_ms = max_over_ranks(step_ms, world, device)
     abytes = algorithmic_bytes(wl.rows, wl.cols, wl.ntok)
     res = {"workload": WORKLOADS[name], "rows": wl.rows, "cols": wl.cols, "ntok": wl.ntok,
@@ -619,12 +749,26 @@ def measure(name, args, rank, world, device, peaks, peak_kind, steps):
         achieved = abytes / (kern_ms * 1e-3) / 1e9
         peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         traffic = profile_traffic(f"gemv_{name}_ncu.txt", GEMV_FILES)
+
+        def frac_at(ms):
+            return None if ms is None else abytes / (ms * 1e-3) / 1e9 / peak
+
         res["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                            "frac": achieved / peak, "traffic": traffic,
                            "frac_of_nominal": achieved / HBM_NOMINAL_GBS,
                            "kernel": "gemv_kernel (quantize fused in)", "kernel_ms": kern_ms,
                            "kernel_timing": kern_how,
+                           "frac_meaning": "frac: independent launches back to back in a graph "
+                                           "(each reads nothing the one before writes, so it "
+                                           "streams its weights and activations before that one "
+                                           "ends); frac_dependent: each launch quantizes the "
+                                           "previous launch's output, so it waits for it before "
+                                           "reading activations (weights are still requested "
+                                           "first); frac_serialised: events between launches, "
+                                           "no overlap at all",
+                           "kernel_ms_dependent": dep_ms, "frac_dependent": frac_at(dep_ms),
                            "kernel_ms_serialised": serial_ms,
+                           "frac_serialised": frac_at(serial_ms),
                            "algorithmic_bytes": abytes, "peak_source": peak_kind}
     else:
         flops = 2.0 * wl.macs()
@@ -636,6 +780,7 @@ def measure(name, args, rank, world, device, peaks, peak_kind, steps):
                            "mma_busy_frac": achieved * MMA_FLOPS_PER_FLOP / peak,
                            "kernel": "act_pack + gemm_tc_ws_kernel (tcgen05 kind::f8f6f4, exact)",
                            "kernel_ms": kern_ms, "kernel_timing": kern_how,
+                           "kernel_ms_dependent": dep_ms,
                            "kernel_ms_serialised": serial_ms, "algorithmic_flops": flops,
                            "peak_source": f"{peak_kind} bf16 dense x {E4M3_PER_BF16:g} "
                                           f"(e4m3 : bf16 nominal)"}
@@ -702,17 +847,26 @@ def main():
     wl, main_res = measure(args.workload, args, rank, world, device, peaks, peak_kind, args.steps)
     clocks.stop()
 
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu
     extra = {}
     if not args.no_extra:
         for name in ("small_batch", "prefill"):
             if name != args.workload:
                 _, r = measure(name, args, rank, world, device, peaks, peak_kind,
                                max(64, args.steps // 10))
+                if want_cpu:
+                    r["cpu_baseline"] = cpu_baseline_entry(*oracle_rate(name, 5.0))
                 extra[name] = r
     if not args.no_replay:
         for ntok, rsteps in ((1, 30), (512, 3)):
-            extra[f"replay_ntok{ntok}"] = measure_replay(ntok, rsteps, args.warmup // 100 + 1, world,
-                                                         device, peaks, peak_kind)
+            r = measure_replay(ntok, rsteps, args.warmup // 100 + 1, world, device, peaks,
+                               peak_kind)
+            if want_cpu:
+                r["cpu_baseline"] = cpu_baseline_entry(*oracle_replay_rate(ntok, 5.0))
+            extra[f"replay_ntok{ntok}"] = r
+    if wl.ntok <= 8 and not args.no_read_ceiling:
+        main_res["roofline"]["read_ceiling"] = measure_read_ceiling(
+            main_res["roofline"]["algorithmic_bytes"] // 16 * 16, device, args.warmup)
 
     e2e = None
     if not args.no_e2e:
@@ -725,13 +879,19 @@ def main():
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                "ms_per_step": s_per_step * 1e3, "streams": args.e2e_streams,
                "how": "tq_matmul_host per step from pinned host X to pinned host Y; "
-                      f"steps alternate over {args.e2e_streams} streams with their own buffers; "
-                      "host wall clock around all steps"}
+                      f"steps alternate over {args.e2e_streams} streams with their own buffers "
+                      "(independent requests in flight); host wall clock around all steps"}
+        if args.e2e_streams != 1:
+            s1, _, _ = time_e2e(wl, e2e_steps, args.warmup, 1)
+            s1 = max_over_ranks(s1, world, device)
+            e2e["one_stream"] = {"value": world * units / s1 / 1e9, "ms_per_step": s1 * 1e3,
+                                 "how": "the same calls on one stream: each step's copy in, "
+                                        "kernel and copy out run one after another (the "
+                                        "latency of a single request)"}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu:
-        v, unit, sample, cores, _, _ = oracle_rate(args.workload, 10.0)
-        cpu = {"value": v, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample}
+    if want_cpu:
+        cpu = cpu_baseline_entry(*oracle_rate(args.workload, 10.0))
 
     if rank == 0:
         unit = "Gweights/s" if wl.ntok == 1 else "GMAC/s"

@@ -91,6 +91,8 @@ def _load():
             "tq_last_cuda_error": ([], I),
             "tq_device_status": ([], I),
             "tq_version": ([], ctypes.c_char_p),
+            "tq_debug_stall_next_launch": ([I64], I),
+            "tq_probe_read_sum": ([P, I64, P, I, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -268,6 +270,22 @@ def tq_device_status(device=None) -> int:
     lib = _load()
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
         return int(lib.tq_device_status())
+
+
+def tq_probe_read_sum(buf: torch.Tensor, out: torch.Tensor, early: bool = False, stream=None):
+    """Adds buf's 32-bit words (mod 2^32) to out[0] (an int32 tensor) with the
+    read-ceiling probe kernel: one streaming pass over buf and nothing else."""
+    _call("tq_probe_read_sum", buf.device, _ptr(buf), buf.numel() * buf.element_size(), _ptr(out),
+          1 if early else 0, _stream(stream, buf.device))
+
+
+def tq_debug_stall_next_launch(wait_limit_ns: int):
+    """Test facility: the next matmul kernel's first thread block requests no
+    input copies, so its waits expire after wait_limit_ns and it reports
+    TQ_ERR_TIMEOUT through tq_device_status (0 cancels)."""
+    rc = _load().tq_debug_stall_next_launch(wait_limit_ns)
+    if rc != TQ_OK:
+        raise TQError(rc, "tq_debug_stall_next_launch")
 
 
 def tq_version() -> str:

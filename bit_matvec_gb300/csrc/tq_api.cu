@@ -1,5 +1,6 @@
 // tq_api.cu -- the C ABI declared in include/tq.h: argument checks, routing by
 // token count, error reporting. Kernels live in the other files of csrc/.
+#include <atomic>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -27,22 +28,23 @@ bool overlap(const void* a, int64_t na, const void* b, int64_t nb) {
   return na > 0 && nb > 0 && x < y + (uintptr_t)nb && y < x + (uintptr_t)na;
 }
 
-// What this library last enqueued on each stream. A GEMV may read weights
-// before the preceding kernel finishes when that kernel writes none (the
-// quantizer, a matmul, a GEMV whose outputs miss them). After a GEMV it may
-// also read its activations early, but only inside a stream capture whose one
-// dependency is that GEMV's node: then nothing else sits between the two
-// kernels, and since a GEMV lets its successor start only after its own wait,
-// that GEMV is the only kernel that can still be running; its outputs must
-// miss every input of the new one. Outside a capture the library cannot see
-// other work on the stream, so it does not read activations early there.
+// What this library last enqueued on each stream, and, inside a stream
+// capture, that kernel's graph node. A kernel of this library may read its
+// weights (or all its inputs) before waiting for the kernel before it only
+// when the host can prove what that kernel is: inside a capture whose one
+// dependency is the node this library recorded for its own last kernel on the
+// stream (so nothing else was captured between the two), and whose outputs
+// miss the new kernel's inputs. Outside a capture the library cannot see
+// other work on the stream (a caller's kernel between two calls could write
+// the weights), so its kernels always wait first there.
 enum LastOp { kOpOther = 0, kOpQuantize = 1, kOpMatmul = 2, kOpGemv = 3 };
+constexpr int kMaxOuts = 3;
 struct StreamLast {
   int op = kOpOther;
-  unsigned long long capture_id = 0;   // kOpGemv inside a capture: its id and
-  cudaGraphNode_t node = nullptr;      // the GEMV's node (else 0, null)
-  const void* out[2] = {nullptr, nullptr};
-  int64_t out_bytes[2] = {0, 0};
+  unsigned long long capture_id = 0;   // inside a capture: its id and the
+  cudaGraphNode_t node = nullptr;      // kernel's node (else 0, null)
+  const void* out[kMaxOuts] = {};
+  int64_t out_bytes[kMaxOuts] = {};
 };
 std::mutex g_stream_mu;
 std::unordered_map<cudaStream_t, StreamLast> g_last_op;
@@ -70,11 +72,14 @@ bool capture_tail(cudaStream_t s, unsigned long long* id, cudaGraphNode_t* node)
   return true;
 }
 
-// Called right after a GEMV launch on s, with the ranges it writes.
-void note_gemv(cudaStream_t s, const void* out0, int64_t bytes0, const void* out1,
-               int64_t bytes1) {
+// Called right after this library launched a kernel of kind `op` on s, with
+// the ranges that kernel (or a kernel before it that may still be running)
+// writes.
+void note_kernel(cudaStream_t s, int op, const void* out0, int64_t bytes0,
+                 const void* out1 = nullptr, int64_t bytes1 = 0, const void* out2 = nullptr,
+                 int64_t bytes2 = 0) {
   StreamLast l;
-  l.op = kOpGemv;
+  l.op = op;
   if (!capture_tail(s, &l.capture_id, &l.node)) {
     l.capture_id = 0;
     l.node = nullptr;
@@ -83,45 +88,50 @@ void note_gemv(cudaStream_t s, const void* out0, int64_t bytes0, const void* out
   l.out_bytes[0] = bytes0;
   l.out[1] = out1;
   l.out_bytes[1] = bytes1;
+  l.out[2] = out2;
+  l.out_bytes[2] = bytes2;
   std::lock_guard<std::mutex> lk(g_stream_mu);
   g_last_op[s] = l;
 }
 
 bool misses_outputs(const StreamLast& l, const void* p, int64_t n) {
-  return !overlap(p, n, l.out[0], l.out_bytes[0]) && !overlap(p, n, l.out[1], l.out_bytes[1]);
+  for (int i = 0; i < kMaxOuts; ++i)
+    if (overlap(p, n, l.out[i], l.out_bytes[i])) return false;
+  return true;
 }
 
-bool last_op_is_quantize(cudaStream_t s) {
-  std::lock_guard<std::mutex> lk(g_stream_mu);
-  auto it = g_last_op.find(s);
-  return it != g_last_op.end() && it->second.op == kOpQuantize;
-}
-
-// The last call on the stream enqueued kernels that do not write the weights.
-bool last_op_keeps_weights(cudaStream_t s, const void* W, int64_t w_bytes) {
-  std::lock_guard<std::mutex> lk(g_stream_mu);
-  auto it = g_last_op.find(s);
-  if (it == g_last_op.end()) return false;
-  const StreamLast& l = it->second;
-  return l.op == kOpQuantize || l.op == kOpMatmul || (l.op == kOpGemv && misses_outputs(l, W, w_bytes));
-}
-
-// The GEMV about to be enqueued on s may read all its inputs (the activations
-// in0 and the weights in1) before waiting for the kernel before it.
-bool gemv_inputs_final(cudaStream_t s, const void* in0, int64_t bytes0, const void* in1,
-                       int64_t bytes1) {
-  StreamLast l;
+// The kernel enqueued just before on s is, provably, this library's last
+// kernel there (see StreamLast); its record is returned in *l.
+bool proven_predecessor(cudaStream_t s, StreamLast* l) {
   {
     std::lock_guard<std::mutex> lk(g_stream_mu);
     auto it = g_last_op.find(s);
     if (it == g_last_op.end()) return false;
-    l = it->second;
+    *l = it->second;
   }
-  if (l.op != kOpGemv || !l.node) return false;
+  if (l->op == kOpOther || !l->node) return false;
   unsigned long long id = 0;
   cudaGraphNode_t node = nullptr;
-  if (!capture_tail(s, &id, &node) || id != l.capture_id || node != l.node) return false;
-  return misses_outputs(l, in0, bytes0) && misses_outputs(l, in1, bytes1);
+  return capture_tail(s, &id, &node) && id == l->capture_id && node == l->node;
+}
+
+// The GEMV about to be enqueued on s may request its weights W before waiting
+// for the kernel before it: that kernel is this library's and writes no part
+// of W.
+bool early_weights_ok(cudaStream_t s, const void* W, int64_t w_bytes) {
+  StreamLast l;
+  return proven_predecessor(s, &l) && misses_outputs(l, W, w_bytes);
+}
+
+// The GEMV about to be enqueued on s may read all its inputs (the activations
+// in0 and the weights in1) before waiting: the kernel before it is this
+// library's GEMV, which lets its successor start only after its own wait (so
+// nothing older can still run), and none of its outputs overlaps them.
+bool gemv_inputs_final(cudaStream_t s, const void* in0, int64_t bytes0, const void* in1,
+                       int64_t bytes1) {
+  StreamLast l;
+  return proven_predecessor(s, &l) && l.op == kOpGemv && misses_outputs(l, in0, bytes0) &&
+         misses_outputs(l, in1, bytes1);
 }
 
 int fail_cuda(cudaError_t e) {
@@ -193,15 +203,15 @@ int matmul_impl(const void* Wtq, const void* Xq, float* Y, int32_t* S, int64_t r
   int* status = nullptr;
   cudaError_t e = device_status_ptr(&status);
   if (e != cudaSuccess) return fail_cuda(e);
-  const bool after_quantize = last_op_is_quantize(s);
+  const int64_t w_bytes = tq_repacked_bytes(rows, cols);
+  const bool early = early_weights_ok(s, Wtq, w_bytes);
   const bool inputs_final =
-      ntok <= gemv_max_tokens() &&
-      gemv_inputs_final(s, Xq, q8K_bytes(ntok, cols), Wtq, tq_repacked_bytes(rows, cols));
+      ntok <= gemv_max_tokens() && gemv_inputs_final(s, Xq, q8K_bytes(ntok, cols), Wtq, w_bytes);
   note_op(s, kOpOther);
   if (ntok <= gemv_max_tokens()) {
-    e = launch_gemv(W, X, Y, S, rows, cols, (int)ntok, status, after_quantize, inputs_final, s);
+    e = launch_gemv(W, X, Y, S, rows, cols, (int)ntok, status, early, inputs_final, s);
     if (e == cudaSuccess) {
-      note_gemv(s, out, out_bytes, nullptr, 0);
+      note_kernel(s, kOpGemv, out, out_bytes);
       return TQ_OK;
     }
     if (e != cudaErrorNotSupported) return fail_cuda(e);
@@ -211,12 +221,23 @@ int matmul_impl(const void* Wtq, const void* Xq, float* Y, int32_t* S, int64_t r
     e = launch_gemm_tc_ws(W, X, Y, S, rows, cols, ntok, static_cast<uint8_t*>(ws), status, s);
   else
     e = launch_gemm_tc(W, X, Y, S, rows, cols, ntok, status, s);
-  return e == cudaSuccess ? TQ_OK : fail_cuda(e);
+  if (e != cudaSuccess) return fail_cuda(e);
+  note_kernel(s, kOpMatmul, out, out_bytes, ws, need);
+  return TQ_OK;
 }
 
 }  // namespace
 
 void record_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
+
+namespace {
+std::atomic<int64_t> g_debug_stall_ns{0};
+}  // namespace
+
+int64_t take_debug_stall() {
+  if (g_debug_stall_ns.load(std::memory_order_relaxed) == 0) return 0;   // the usual case
+  return g_debug_stall_ns.exchange(0);
+}
 
 cudaError_t ensure_dynamic_smem(const void* kernel, int bytes) {
   if (bytes <= 48 * 1024) return cudaSuccess;
@@ -294,9 +315,11 @@ int tq_quantize_q8K(const float* X, void* Xq, int64_t ntok, int64_t cols, void* 
   if (!aligned16(X) || !aligned16(Xq)) return TQ_ERR_ALIGN;
   if (overlap(X, ntok * cols * 4, Xq, q8K_bytes(ntok, cols))) return TQ_ERR_ALIAS;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  note_op(s, kOpOther);
   cudaError_t e = launch_quantize_q8K(X, static_cast<uint8_t*>(Xq), ntok * (cols / kQK), s);
-  note_op(s, e == cudaSuccess ? kOpQuantize : kOpOther);
-  return e == cudaSuccess ? TQ_OK : fail_cuda(e);
+  if (e != cudaSuccess) return fail_cuda(e);
+  note_kernel(s, kOpQuantize, Xq, q8K_bytes(ntok, cols));
+  return TQ_OK;
 }
 
 int64_t tq_repacked_bytes(int64_t rows, int64_t cols) {
@@ -405,12 +428,13 @@ int tq_quantize_matmul(const void* Wtq, const float* X, void* Xq, float* Y, int6
     int* status = nullptr;
     cudaError_t e = device_status_ptr(&status);
     if (e != cudaSuccess) return fail_cuda(e);
-    const bool early = last_op_keeps_weights(s, Wtq, w_bytes);
+    const bool early = early_weights_ok(s, Wtq, w_bytes);
     const bool inputs_final = gemv_inputs_final(s, X, x_bytes, Wtq, w_bytes);
+    note_op(s, kOpOther);
     e = launch_gemv(static_cast<const uint8_t*>(Wtq), nullptr, Y, nullptr, rows, cols, (int)ntok,
                     status, early, inputs_final, s, X, static_cast<uint8_t*>(Xq));
     if (e == cudaSuccess) {
-      note_gemv(s, Y, y_bytes, Xq, xq_bytes);
+      note_kernel(s, kOpGemv, Y, y_bytes, Xq, xq_bytes);
       return TQ_OK;
     }
     if (e != cudaErrorNotSupported) {
@@ -428,14 +452,12 @@ int tq_quantize_matmul(const void* Wtq, const float* X, void* Xq, float* Y, int6
     e = launch_quantize_gemm_tc_ws(X, static_cast<uint8_t*>(Xq), static_cast<const uint8_t*>(Wtq),
                                    Y, rows, cols, ntok, static_cast<uint8_t*>(workspace), status, s);
     if (e != cudaSuccess) return fail_cuda(e);
-    note_op(s, kOpMatmul);
+    note_kernel(s, kOpMatmul, Y, y_bytes, Xq, xq_bytes, workspace, need);
     return TQ_OK;
   }
   int rc = tq_quantize_q8K(X, Xq, ntok, cols, stream);
   if (rc != TQ_OK) return rc;
-  rc = tq_matmul_ws(Wtq, Xq, Y, rows, cols, ntok, workspace, workspace_bytes, stream);
-  if (rc == TQ_OK) note_op(s, kOpMatmul);
-  return rc;
+  return tq_matmul_ws(Wtq, Xq, Y, rows, cols, ntok, workspace, workspace_bytes, stream);
 }
 
 int tq_matmul_host(const void* Wtq, const float* X_host, float* X, void* Xq, float* Y,
@@ -504,6 +526,25 @@ int tq_device_status(void) {
   return v == kDevTimeout ? TQ_ERR_TIMEOUT : TQ_OK;
 }
 
-const char* tq_version(void) { return "0.1.0"; }
+int tq_probe_read_sum(const void* buf, int64_t bytes, uint32_t* out, int early, void* stream) {
+  if (bytes < 0 || bytes % 16 != 0) return TQ_ERR_SHAPE;
+  if (!out) return TQ_ERR_NULL;
+  if (bytes == 0) return TQ_OK;
+  if (!buf) return TQ_ERR_NULL;
+  if (!aligned16(buf) || !aligned4(out)) return TQ_ERR_ALIGN;
+  if (overlap(buf, bytes, out, 4)) return TQ_ERR_ALIAS;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  note_op(s, kOpOther);
+  const cudaError_t e = launch_read_sum(buf, bytes, out, early != 0, s);
+  return e == cudaSuccess ? TQ_OK : fail_cuda(e);
+}
+
+int tq_debug_stall_next_launch(int64_t wait_limit_ns) {
+  if (wait_limit_ns < 0) return TQ_ERR_SHAPE;
+  g_debug_stall_ns.store(wait_limit_ns);
+  return TQ_OK;
+}
+
+const char* tq_version(void) { return "0.2.0"; }
 
 }  // extern "C"

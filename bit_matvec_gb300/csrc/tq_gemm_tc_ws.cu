@@ -114,7 +114,7 @@ static_assert(kInBytes % 16 == 0 && kWRun % 16 == 0 && kInW % 16 == 0,
               "bulk copies need 16-byte multiples");
 // scale ring stage: d_w * 2^9 per group and row, then the block's d_x
 constexpr int kScaleFloats = kGPB * kM + kN;
-constexpr int kNumBars = 2 * kInStages + 3 * kStages;
+constexpr int kNumBars = 2 * kInStages + 3 * kStages + 1;   // + the failure drain
 constexpr int kSmemUsed = kInStages * kInBytes + kStages * kBSumBytes +
                           kScaleStages * kScaleFloats * 4 + kNumBars * 8 + 16;
 // Enough shared memory that only one CTA fits on an SM: each CTA allocates
@@ -264,6 +264,8 @@ struct WsArgs {
   int ngroups;
   int nblk;
   int nrb;
+  int stall;          // test facility: CTA (0, 0) requests no input, so its waits
+  uint64_t stall_ns;  // expire after stall_ns (tq_debug_stall_next_launch)
 };
 
 // One group's codes (this thread: one row, the 64 weights of one k half) ->
@@ -298,7 +300,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
   uint64_t* mma_ready = in_empty + kInStages;                                  // [stage]
   uint64_t* a_free = mma_ready + kStages;                                      // [stage]
   uint64_t* mma_done = a_free + kStages;                                       // [stage]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + kStages);
+  uint64_t* drain_bar = mma_done + kStages;   // after a failure: the MMAs issued are done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  // Set by a role that gave up a wait (before its next arrival): the producer
+  // then requests no more input, so a slot is never refilled while a copy into
+  // it may still be in flight.
+  volatile int* s_failed = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.ngroups;
@@ -306,6 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
   const int64_t rb0 = (int64_t)blockIdx.x * kTilesPerCta;
   const int64_t nt = blockIdx.y;
   const int64_t tok0 = nt * kN;
+  const bool stalled = a.stall && blockIdx.x == 0 && blockIdx.y == 0;
+  const uint64_t lim = stalled ? a.stall_ns : kWaitLimitNs;   // bound of the pipeline's waits
+  int issued[kInStages] = {};   // producer: copies requested per input slot
 
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -328,6 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
       mbarrier_init(smem_u32(a_free + s), 1);
       mbarrier_init(smem_u32(mma_done + s), 1);
     }
+    mbarrier_init(smem_u32(drain_bar), 1);
+    *s_failed = 0;
     mbarrier_init_fence();
   }
   tc_fence_before();
@@ -355,13 +367,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
       pdl_wait_primary();   // the workspace is written by the previous kernel (the pre-pass)
       int i = 0;
       uint32_t ph = 0;
-      for (int j = 0; j < nb; ++j) {
+      for (int j = 0; j < (stalled ? 0 : nb); ++j) {
         // the slot is free once the converters and the MMAs of block j - kInStages are done
-        if (j >= kInStages &&
-            !mbarrier_wait_bounded(smem_u32(in_empty + i), ph ^ 1u, kWaitLimitNs)) {
-          failed = true;
-          break;
+        if (j >= kInStages) {
+          if (!mbarrier_wait_bounded(smem_u32(in_empty + i), ph ^ 1u, lim)) {
+            failed = true;
+            break;
+          }
+          if (*s_failed) break;
         }
+        ++issued[i];
         uint8_t* st = sIn + i * kInBytes;
         const uint32_t full = smem_u32(in_full + i);
         const int g0 = j * kGPB;
@@ -387,7 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
     int i = 0, sa = 0, ss = 0, g = 0;
     uint32_t pin = 0, pa = 0;
     for (int b = 0; b < nb; ++b) {
-      if (!failed && !mbarrier_wait_bounded(smem_u32(in_full + i), pin, kWaitLimitNs)) failed = true;
+      if (!failed && !mbarrier_wait_bounded(smem_u32(in_full + i), pin, lim)) failed = true;
+      failed = __any_sync(0xffffffffu, failed);
+      if (failed && lane == 0) *s_failed = 1;   // before this warp's arrival below
       const uint8_t* st = sIn + i * kInBytes;
       const uint8_t* tile = st + kInW + q4 * kWRun;
       uint4 cw[kGPB];
@@ -416,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
       for (int gi = 0; gi < kGPB; ++gi) {
         // A stage sa is free once the MMAs of group g - kStages have finished
         if (g >= kStages && !failed &&
-            !mbarrier_wait_bounded(smem_u32(a_free + sa), pa ^ 1u, kWaitLimitNs))
+            !mbarrier_wait_bounded(smem_u32(a_free + sa), pa ^ 1u, lim))
           failed = true;
         failed = __any_sync(0xffffffffu, failed);   // tcgen05.st below is warp-wide
         tc_fence_after();
@@ -468,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
       const float4* dx4 = reinterpret_cast<const float4*>(sst + kGPB * kM + n0);
 #pragma unroll
       for (int gi = 0; gi < kGPB; ++gi) {
-        if (!failed && !mbarrier_wait_bounded(smem_u32(mma_done + sa), pa, kWaitLimitNs))
+        if (!failed && !mbarrier_wait_bounded(smem_u32(mma_done + sa), pa, lim))
           failed = true;
         failed = __any_sync(0xffffffffu, failed);   // tcgen05.ld below is warp-wide
         tc_fence_after();
@@ -537,8 +554,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
 #pragma unroll
       for (int gi = 0; gi < kGPB; ++gi) {
         // A(g) written and the accumulator of group g - 3 read
-        if (!failed && !mbarrier_wait_bounded(smem_u32(mma_ready + sa), pa, kWaitLimitNs))
+        if (!failed && !mbarrier_wait_bounded(smem_u32(mma_ready + sa), pa, lim)) {
           failed = true;
+          *s_failed = 1;
+        }
         tc_fence_after();
         if (!failed) {
           const uint32_t d = tmem + kAccCol + (uint32_t)sa * kAccCols;
@@ -561,12 +580,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
   }
 
   if (failed) atomicExch(a.status, kDevTimeout);
-  // After a failure, staged copies may still be in flight: let the last use of
-  // each input slot land before shared memory is released.
-  if (__syncthreads_or(failed) && warp == kProdWarp && lane == 0) {
-    for (int i = 0; i < kInStages && i < nb; ++i) {
-      const int last = i + (nb - 1 - i) / kInStages * kInStages;
-      mbarrier_wait_bounded(smem_u32(in_full + i), (uint32_t)((last / kInStages) & 1), kWaitLimitNs);
+  // After a failure, copies and MMAs may still be in flight: before shared
+  // and tensor memory are released, let the last copy requested into each
+  // input slot land (the producer refills a slot only after every converter
+  // saw its previous copy land, so at most that one is pending; it completes
+  // phase issued - 1 of the slot's barrier), and let every MMA issued finish
+  // (a commit tracks all of the issuing thread's earlier MMAs).
+  if (__syncthreads_or(failed)) {
+    if (warp == kProdWarp && lane == 0) {
+      for (int i = 0; i < kInStages; ++i)
+        if (issued[i] > 0)
+          mbarrier_wait_bounded(smem_u32(in_full + i), (uint32_t)((issued[i] - 1) & 1),
+                                kWaitLimitNs);
+    } else if (warp == kMmaWarp && lane == 0) {
+      mma_commit(smem_u32(drain_bar));
+      mbarrier_wait_bounded(smem_u32(drain_bar), 0u, kWaitLimitNs);
     }
   }
   tc_fence_before();
@@ -607,6 +635,9 @@ cudaError_t launch_main(const uint8_t* Wtq, float* Y, int32_t* S, int64_t rows, 
   a.ngroups = G;
   a.nblk = nblk;
   a.nrb = (int)((rows + kTileRows - 1) / kTileRows);
+  const int64_t stall_ns = take_debug_stall();
+  a.stall = stall_ns > 0 ? 1 : 0;
+  a.stall_ns = stall_ns > 0 ? (uint64_t)stall_ns : 0;
   const int64_t gx = (rows + kM - 1) / kM;
   if (gx > 0x7fffffff) return cudaErrorInvalidConfiguration;
   const dim3 grid((unsigned)gx, (unsigned)l.ntile);

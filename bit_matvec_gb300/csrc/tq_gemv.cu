@@ -96,6 +96,9 @@ struct GemvArgs {
   int defer;          // the inputs are final when the kernel starts: wait for the
                       // previous kernel only after the first tile column (1) or
                       // after the first ring stage (2), before any global write
+  int stall;          // test facility: CTA 0 requests no weight stage, so its
+                      // waits expire after stall_ns (tq_debug_stall_next_launch)
+  uint64_t stall_ns;
 };
 
 // Fused form: quantizes the T x cols f32 activations block by block (warp per
@@ -191,8 +194,8 @@ __host__ __device__ inline SmemPlan plan_smem(int stages, int64_t cols) {
   const int64_t g = cols / kGroup, b = cols / kQK;
   p.ring = 0;
   p.bars = (int64_t)stages * Cfg<T>::kStageBytes;        // full[S], redfull[2], redempty[2]
-  p.counters = p.bars + (stages + 4) * 8;                  // int[S]
-  p.sq = (p.counters + stages * 4 + 15) / 16 * 16;
+  p.counters = p.bars + (stages + 4) * 8;                  // int[S] released, int[S] issued
+  p.sq = (p.counters + stages * 8 + 15) / 16 * 16;
   p.sgsum = p.sq + T * cols;
   p.sdx = p.sgsum + T * g * 4;
   p.red = p.sdx + T * b * 4;
@@ -214,6 +217,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
   uint64_t* redfull = full + S;                                   // [2]
   uint64_t* redempty = redfull + 2;                               // [2]
   int* released = reinterpret_cast<int*>(smem + pl.counters);    // [S]
+  int* issued = released + S;                                    // [S] copies per slot
   int8_t* sq = reinterpret_cast<int8_t*>(smem + pl.sq);           // [T][cols]
   int* sgsum = reinterpret_cast<int*>(smem + pl.sgsum);           // [T][ngroups]
   float* sdx = reinterpret_cast<float*>(smem + pl.sdx);           // [T][nblk]
@@ -226,6 +230,8 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
   const int per_rb = (a.ngroups + kStageTiles - 1) / kStageTiles;
   const int nstage = (rb1 - rb0) * per_rb;
   const uint64_t policy = l2_evict_first_policy();
+  const bool stalled = a.stall && blockIdx.x == 0;
+  const uint64_t lim = stalled ? a.stall_ns : kWaitLimitNs;   // bound of the stream's waits
 
   // Stage j of this CTA covers tile column rb0 + j / per_rb, groups from
   // (j % per_rb) * kStageTiles; it lands in ring slot j % S. Counters below
@@ -234,11 +240,13 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
     const int gs = st * kStageTiles;
     const uint32_t bytes = (uint32_t)(min(kStageTiles, a.ngroups - gs) * kTileBytes);
     const uint32_t bar = smem_u32(full + slot);
+    ++issued[slot];   // one thread at a time per slot: the ring protocol orders them
     mbarrier_arrive_expect_tx(bar, bytes);
     bulk_copy_g2s(smem_u32(ring + (size_t)slot * kStageBytes),
                   a.Wtq + ((int64_t)rb * a.ngroups + gs) * kTileBytes, bytes, bar, policy);
   };
   auto issue_first = [&]() {
+    if (stalled) return;
     int rb = rb0, st = 0;
     for (int j = 0; j < min(S, nstage); ++j) {
       issue(j, rb, st);
@@ -250,6 +258,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
     for (int i = 0; i < S; ++i) {
       mbarrier_init(smem_u32(full + i), 1);
       released[i] = 0;
+      issued[i] = 0;
     }
     for (int i = 0; i < 2; ++i) {
       mbarrier_init(smem_u32(redfull + i), kConsumers);
@@ -332,7 +341,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
     for (int st = 0; st < per_rb; ++st, ++j) {
       const int gs = st * kStageTiles;
       const int nt = min(kStageTiles, a.ngroups - gs);
-      if (!failed && !mbarrier_wait_bounded(smem_u32(full + slot), phase, kWaitLimitNs))
+      if (!failed && !mbarrier_wait_bounded(smem_u32(full + slot), phase, lim))
         failed = true;
       // this warp's tiles of the stage: warp, warp + 16, ... (spread for short stages)
       GroupCodes c[Cfg<T>::kTilesPerWarp];
@@ -378,7 +387,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
       float* r = red + p * (kConsumers * T * 32);
       if (i >= 2 && !failed &&
           !mbarrier_wait_bounded(smem_u32(redempty + p), (uint32_t)(((i >> 1) - 1) & 1),
-                                 kWaitLimitNs))
+                                 lim))
         failed = true;
 #pragma unroll
       for (int t = 0; t < T; ++t) r[(warp * T + t) * 32 + lane] = y[t];
@@ -387,7 +396,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
       const int t = (warp - i * T) & (kConsumers - 1);
       if (t < T) {
         if (!failed && !mbarrier_wait_bounded(smem_u32(redfull + p), (uint32_t)((i >> 1) & 1),
-                                              kWaitLimitNs))
+                                              lim))
           failed = true;
         float s = 0.0f;
 #pragma unroll
@@ -401,12 +410,14 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
   if (!waited) finish_wait();   // a CTA without tile columns
   if (failed && lane == 0) atomicExch(a.status, kDevTimeout);
   // Copies can still be in flight only after a failed wait: then let the last
-  // stage of each slot land before the CTA's shared memory is released.
+  // copy requested into each slot land before the CTA's shared memory is
+  // released. A slot is refilled only by a warp that saw its previous copy
+  // land, so at most that last one can be in flight; it completes phase
+  // issued - 1 of the slot's barrier.
   if (__syncthreads_or(failed) && threadIdx.x == 0) {
-    for (int sl = 0; sl < S && sl < nstage; ++sl) {
-      const int last = sl + (nstage - 1 - sl) / S * S;
-      mbarrier_wait_bounded(smem_u32(full + sl), (uint32_t)((last / S) & 1), kWaitLimitNs);
-    }
+    for (int sl = 0; sl < S; ++sl)
+      if (issued[sl] > 0)
+        mbarrier_wait_bounded(smem_u32(full + sl), (uint32_t)((issued[sl] - 1) & 1), kWaitLimitNs);
   }
 }
 
@@ -458,8 +469,8 @@ __host__ __device__ inline MmaPlan plan_mma(int stages, int64_t cols) {
   p.sb_stride = cols * 2 + 8;
   p.ring = 0;
   p.bars = (int64_t)stages * MmaCfg<T, TPW>::kStageBytes;
-  p.counters = p.bars + (stages + 4) * 8;
-  p.sb = (p.counters + stages * 4 + 15) / 16 * 16;
+  p.counters = p.bars + (stages + 4) * 8;                  // int[S] released, int[S] issued
+  p.sb = (p.counters + stages * 8 + 15) / 16 * 16;
   p.sgsum = p.sb + T * p.sb_stride;
   p.sdx = p.sgsum + T * g * 4;
   p.red = (p.sdx + T * b * 4 + 15) / 16 * 16;
@@ -588,6 +599,7 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
   uint64_t* redfull = full + S;                                   // [2]
   uint64_t* redempty = redfull + 2;                               // [2]
   int* released = reinterpret_cast<int*>(smem + pl.counters);    // [S]
+  int* issued = released + S;                                    // [S] copies per slot
   uint8_t* sb = smem + pl.sb;                                     // [T][cols] f16 (+8 B)
   int* sgsum = reinterpret_cast<int*>(smem + pl.sgsum);           // [T][ngroups]
   float* sdx = reinterpret_cast<float*>(smem + pl.sdx);           // [T][nblk]
@@ -599,16 +611,20 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
   const int per_rb = (a.ngroups + kStageTiles - 1) / kStageTiles;
   const int nstage = (rb1 - rb0) * per_rb;
   const uint64_t policy = l2_evict_first_policy();
+  const bool stalled = a.stall && blockIdx.x == 0;
+  const uint64_t lim = stalled ? a.stall_ns : kWaitLimitNs;   // bound of the stream's waits
 
   auto issue = [&](int slot, int rb, int st) {
     const int gs = st * kStageTiles;
     const uint32_t bytes = (uint32_t)(min(kStageTiles, a.ngroups - gs) * kTileBytes);
     const uint32_t bar = smem_u32(full + slot);
+    ++issued[slot];   // one thread at a time per slot: the ring protocol orders them
     mbarrier_arrive_expect_tx(bar, bytes);
     bulk_copy_g2s(smem_u32(ring + (size_t)slot * kStageBytes),
                   a.Wtq + ((int64_t)rb * a.ngroups + gs) * kTileBytes, bytes, bar, policy);
   };
   auto issue_first = [&]() {
+    if (stalled) return;
     int rb = rb0, st = 0;
     for (int j = 0; j < min(S, nstage); ++j) {
       issue(j, rb, st);
@@ -620,6 +636,7 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
     for (int i = 0; i < S; ++i) {
       mbarrier_init(smem_u32(full + i), 1);
       released[i] = 0;
+      issued[i] = 0;
     }
     for (int i = 0; i < 2; ++i) {
       mbarrier_init(smem_u32(redfull + i), kConsumers);
@@ -716,7 +733,7 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
     for (int st = 0; st < per_rb; ++st, ++j) {
       const int gs = st * kStageTiles;
       const int nt = min(kStageTiles, a.ngroups - gs);
-      if (!failed && !mbarrier_wait_bounded(smem_u32(full + slot), phase, kWaitLimitNs))
+      if (!failed && !mbarrier_wait_bounded(smem_u32(full + slot), phase, lim))
         failed = true;
       failed = __any_sync(0xffffffffu, failed);   // mma.sync below is warp-wide
       const uint8_t* stage = ring + (size_t)slot * kStageBytes;
@@ -755,7 +772,7 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
       float* r = red + p * (kConsumers * 8 * 32);
       if (i >= 2 && !failed &&
           !mbarrier_wait_bounded(smem_u32(redempty + p), (uint32_t)(((i >> 1) - 1) & 1),
-                                 kWaitLimitNs))
+                                 lim))
         failed = true;
 #pragma unroll
       for (int e = 0; e < 8; ++e) r[(warp * 8 + e) * 32 + lane] = y[e];
@@ -764,7 +781,7 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
       const int e = (warp - i * kMmaReducers) & (kConsumers - 1);
       if (e < kMmaReducers) {
         if (!failed && !mbarrier_wait_bounded(smem_u32(redfull + p), (uint32_t)((i >> 1) & 1),
-                                              kWaitLimitNs))
+                                              lim))
           failed = true;
         float sum = 0.0f;
 #pragma unroll
@@ -779,11 +796,10 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
   }
   if (!waited) finish_wait();   // a CTA without tile columns
   if (failed && lane == 0) atomicExch(a.status, kDevTimeout);
-  if (__syncthreads_or(failed) && threadIdx.x == 0) {
-    for (int sl = 0; sl < S && sl < nstage; ++sl) {
-      const int last = sl + (nstage - 1 - sl) / S * S;
-      mbarrier_wait_bounded(smem_u32(full + sl), (uint32_t)((last / S) & 1), kWaitLimitNs);
-    }
+  if (__syncthreads_or(failed) && threadIdx.x == 0) {   // as in the one-token kernel
+    for (int sl = 0; sl < S; ++sl)
+      if (issued[sl] > 0)
+        mbarrier_wait_bounded(smem_u32(full + sl), (uint32_t)((issued[sl] - 1) & 1), kWaitLimitNs);
   }
 }
 
@@ -804,6 +820,13 @@ inline int defer_wait(const GemvArgs& a, bool group_sums, int grid, int stage_ti
   const int per_rb = (a.ngroups + stage_tiles - 1) / stage_tiles;
   if (after_stage_ok && per_rb >= 3) return 2;
   return a.nrb >= 2 * grid ? 1 : 0;
+}
+
+// A launch about to go takes a pending test stall (tq_debug_stall_next_launch).
+inline void take_stall(GemvArgs& a) {
+  const int64_t ns = take_debug_stall();
+  a.stall = ns > 0 ? 1 : 0;
+  a.stall_ns = ns > 0 ? (uint64_t)ns : 0;
 }
 
 template <int T, bool G, int TPW>
@@ -832,6 +855,7 @@ cudaError_t launch_mma(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
     if (a.nrb % g == 0) { grid = g; break; }
 #endif
   a.defer = defer_wait(a, G, grid, MmaCfg<T, TPW>::kStageTiles, false);
+  take_stall(a);
   return launch_pdl(kernel, dim3(grid), dim3(MmaCfg<T, TPW>::kThreads), (size_t)smem, s, a);
 }
 
@@ -864,6 +888,7 @@ cudaError_t launch_t(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
     if (a.nrb % g == 0) { grid = g; break; }
 #endif
   a.defer = defer_wait(a, G, grid, Cfg<T>::kStageTiles, true);
+  take_stall(a);
   return launch_pdl(kernel, dim3(grid), dim3(Cfg<T>::kThreads), (size_t)smem, s, a);
 }
 
@@ -943,6 +968,8 @@ cudaError_t launch_gemv(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t
   a.X = X;
   a.Xq_out = Xq_out;
   a.defer = inputs_final ? 1 : 0;
+  a.stall = 0;
+  a.stall_ns = 0;
   const bool gsum = S != nullptr;
   cudaError_t e;
   switch (ntok) {

@@ -283,4 +283,13 @@ cudaError_t resident_ctas(const void* kernel, int threads, size_t smem, int* out
 // Record e as this host thread's tq_last_cuda_error.
 void record_cuda_error(cudaError_t e);
 
+// Read-ceiling probe: adds the buffer's 32-bit words (wrapping) to *out.
+cudaError_t launch_read_sum(const void* buf, int64_t bytes, uint32_t* out, bool early,
+                            cudaStream_t s);
+
+// Test facility (tq_debug_stall_next_launch): the wait limit in ns that the
+// next matmul kernel launched takes for its stalled first CTA, or 0 if none is
+// pending; taking it clears it.
+int64_t take_debug_stall();
+
 }  // namespace tq

@@ -58,7 +58,8 @@ extern "C" int tq_matmul_static_ws(const void* Wtq, const void* Xq, float* Y, in
   // tokens and per 128 columns) exceeds the array; rejecting them first also
   // keeps the size product below from overflowing.
   constexpr int64_t kMaxFactor = TQ_STATIC_WS_BYTES / 16384;
-  if (ntok > 8 && cols > 0 && (cols / TQ_GROUP > kMaxFactor || (ntok + 63) / 64 > kMaxFactor))
+  if (ntok > tq::gemv_max_tokens() && cols > 0 &&
+      (cols / TQ_GROUP > kMaxFactor || (ntok + 63) / 64 > kMaxFactor))
     return TQ_ERR_WORKSPACE;
   const int64_t need = tq_matmul_workspace_bytes(rows, cols, ntok);
   if (need < 0) return TQ_ERR_SHAPE;

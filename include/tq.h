@@ -306,7 +306,10 @@ int tq_matmul_host(const void *Wtq, const float *X_host, float *X, void *Xq, flo
  *   library's code for the array onto that device; make that first call
  *   before any stream capture. TQ_ERR_CUDA if the look-up fails.
  *   Memory: the array occupies TQ_STATIC_WS_BYTES on every GPU where it has
- *   been loaded, until the process exits.
+ *   been loaded, until the process exits. The looked-up address is kept for
+ *   the life of the process: do not use the library on a device after
+ *   cudaDeviceReset (or any reset of its primary context) there, since the
+ *   array then moves and the kept address is stale.
  *   Sharing: every call uses the same array, which keeps the last call's
  *   contents (nothing in it needs to start at zero: the pre-pass rewrites all
  *   of it that the matmul reads). Calls whose kernels overlap on the GPU
@@ -330,6 +333,39 @@ int tq_last_cuda_error(void);
  * synchronizes the device (it copies the word to the host).
  */
 int tq_device_status(void);
+
+/*
+ * tq_probe_read_sum -- measurement aid: the memory-read ceiling the GEMV is
+ * judged against (the post measures its DRAM read ceiling the same way, in
+ * "the ceiling": a sum over a large buffer). Adds every 32-bit word of buf,
+ * as unsigned integers modulo 2^32, to *out, reading buf once with 128-bit
+ * streaming loads and nothing else; time it to get the read rate.
+ *   buf    bytes of device memory, 16-byte aligned; bytes a multiple of 16.
+ *   out    one uint32 in device memory, 4-byte aligned; added to (atomically).
+ *   early  nonzero: the loads may start before the kernel enqueued just
+ *          before on the stream finishes (the caller promises that kernel
+ *          does not write buf); the store into out still waits for it.
+ * Errors: TQ_ERR_SHAPE if bytes < 0 or bytes % 16 != 0; TQ_ERR_NULL;
+ * TQ_ERR_ALIGN; TQ_ERR_ALIAS if out lies in buf.
+ */
+int tq_probe_read_sum(const void *buf, int64_t bytes, uint32_t *out, int early, void *stream);
+
+/*
+ * tq_debug_stall_next_launch -- test facility for the timeout path (the pages
+ * have no counterpart). The next matmul kernel this library launches, from
+ * any host thread and on any stream, runs with its first thread block
+ * requesting none of its input copies, as if they never arrived: that block's
+ * waits on them expire after wait_limit_ns (instead of the usual 2 s), it
+ * sets the device status word and returns; the other blocks finish normally.
+ * Its outputs are then undefined, and tq_device_status() reports
+ * TQ_ERR_TIMEOUT (and clears the word). The block still waits for any copy
+ * it did request before it exits, so no copy outlives it. Nothing faults and
+ * nothing waits without bound. Kernels that take it: the GEMV (ntok <= 8) and
+ * the tensor-core kernel of the workspace forms. wait_limit_ns = 0 cancels a
+ * pending stall.
+ * Errors: TQ_ERR_SHAPE if wait_limit_ns < 0.
+ */
+int tq_debug_stall_next_launch(int64_t wait_limit_ns);
 
 /* Library version as "major.minor.patch". */
 const char *tq_version(void);

@@ -17,7 +17,7 @@
  *  - "Quantization and the CPU", section *Quantizing the weights and
  *    activations* (symmetric int8: largest magnitude divided by 127).
  *
- * Readings where the pages are silent (each also listed in the design doc):
+ * Readings where the pages are silent:
  *  - pq2_0 block = { uint16 fp16 scale; uint8 codes[32] }, 34 bytes; weight k
  *    of the block in code byte k >> 2, bits 2*(k & 3).
  *  - q8_K block = { float d; int8 qs[256]; int16 bsums[16] }, 292 bytes.

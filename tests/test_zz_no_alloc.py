@@ -61,9 +61,13 @@ def test_static_workspace_matches_caller_workspace(tq):
         pytest.skip("no CUDA device")
     from gpu_util import DEV, assert_close, gpu_quantize, gpu_repack
 
-    # two shapes in a row: 3 token tiles with a ragged tail, then 1 tile
-    # with other columns, so the second call reads over the first one's data
-    cases = [(300, 1024, 130, 2), (128, 768, 64, 3)]
+    # Two calls in a row on the shared array. The first fills whole token
+    # tiles (192 = 3 x 64 tokens, no padding), so its data sits where the
+    # second call's padded token slots fall: the second (130 tokens, a ragged
+    # third tile) must not read any of it. Each result must equal the caller
+    # workspace form bit for bit (same kernels, same inputs) and the oracle
+    # within the matmul tolerance.
+    cases = [(128, 1024, 192, 2), (300, 1024, 130, 3)]
     ins, outs = [], []
     for rows, cols, ntok, seed in cases:
         wpq, x = _case(rows, cols, ntok, seed)
@@ -74,9 +78,13 @@ def test_static_workspace_matches_caller_workspace(tq):
         outs.append(Y)
     for (rows, cols, ntok, _), (wpq, x, Wtq, Xq), Y in zip(cases, ins, outs):
         ws = tq.workspace_empty(rows, cols, ntok, DEV)
+        ws.fill_(0x5A)
         Yws = torch.full((ntok, rows), float("nan"), dtype=torch.float32, device=DEV)
         tq.tq_matmul_ws(Wtq, Xq, Yws, rows, cols, ntok, ws)
-        _, abs_sum = oracle.matmul(wpq, oracle.quantize_q8K(x), rows, cols)
-        y_static = Y.cpu().numpy()
-        assert_close(y_static, Yws.cpu().numpy(), abs_sum)
+        y_static, y_ws = Y.cpu().numpy(), Yws.cpu().numpy()
+        y_ref, abs_sum = oracle.matmul(wpq, oracle.quantize_q8K(x), rows, cols)
+        assert np.array_equal(y_static.view(np.uint32), y_ws.view(np.uint32)), \
+            f"static and caller workspaces differ at {(rows, cols, ntok)}"
+        assert_close(y_static, y_ws, abs_sum)
+        assert_close(y_static, y_ref, abs_sum)
     assert tq.tq_device_status() == tq.TQ_OK
