@@ -52,11 +52,10 @@ HBM_NOMINAL_GBS = 7900.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # The tensor-core matmul runs e4m3 MMAs: its peak is the measured bf16 dense
 # rate times the nominal e4m3 : bf16 ratio (4.5 : 2.25 PFLOP/s dense). It
-# executes 2.5 MMA flops per algorithmic flop: each int8 activation is split
-# exactly into two e4m3 parts (two MMA columns), and one sum MMA per four
-# main MMAs applies w = u - 1.
+# executes 2 MMA flops per algorithmic flop: each int8 activation is split
+# exactly into two e4m3 parts (two MMA columns).
 E4M3_PER_BF16 = 2.0
-MMA_FLOPS_PER_FLOP = 2.5
+MMA_FLOPS_PER_FLOP = 2.0
 
 WORKLOADS = {
     "decode": "decode GEMV 32768x8192 pq2_0 x q8_K, ntok=1",

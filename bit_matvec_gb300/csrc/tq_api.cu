@@ -115,9 +115,11 @@ bool proven_predecessor(cudaStream_t s, StreamLast* l) {
   return capture_tail(s, &id, &node) && id == l->capture_id && node == l->node;
 }
 
-// The GEMV about to be enqueued on s may request its weights W before waiting
-// for the kernel before it: that kernel is this library's and writes no part
-// of W.
+// The GEMV about to be enqueued on s may request its weights W before
+// waiting for the kernel before it: that kernel is this library's and writes
+// no part of W, and, like every kernel of this library that is recorded
+// here, it lets its successor start only after its own wait (or at its end),
+// so no older kernel can still be running.
 bool early_weights_ok(cudaStream_t s, const void* W, int64_t w_bytes) {
   StreamLast l;
   return proven_predecessor(s, &l) && misses_outputs(l, W, w_bytes);

@@ -19,13 +19,12 @@
 // give the subnormal u * 2^-9, bits 2-3 give u * 4 * 2^-9 (u = 2 sets the
 // lowest exponent bit, 2^-6 = 8 * 2^-9). The pre-pass divides B by 4 at the
 // k whose A carries the factor 4, so every product is u * lo * 2^-9 or
-// u * 16 hi * 2^-9 exactly. For w = u - 1 a fifth MMA per group adds
-// -2^-9 * sum_k q (the group's sum from the q8_K bsums): B holds the sum's
-// four base-16 digits d0..d3 (d3 signed, all exact in e4m3) at k = 0..3 of
-// the low columns, A the constants -2^-9 * 16^i. Every partial sum is an
-// integer multiple of 2^-9 below 2^15 in magnitude, so the accumulation is
-// exact and ends at isum * 2^-9 (low plus high columns); the epilogue scales
-// by d_w * 2^9 * d_x.
+// u * 16 hi * 2^-9 exactly. Every partial sum is an integer multiple of 2^-9
+// below 2^15 in magnitude, so the accumulation is exact and the low plus high
+// columns end at sum_k u q * 2^-9. The epilogue turns u back into w = u - 1
+// with the group's activation sum from the q8_K bsums (dot(w, q) = dot(u, q) -
+// sum(q), post "the trick with 4 and 16"): isum = 2^9 * acc - sum(q), one
+// exact f32 FMA, then adds d_x * d_w * isum.
 //
 // Per CTA (128 weight rows x 64 tokens) the work goes one q8_K block (two
 // 128-weight groups) at a time:
@@ -36,15 +35,18 @@
 //   - 8 converter warps mask the codes of each group into A and store them
 //     into tensor memory (tcgen05.st), 64 weights per thread and group;
 //   - one thread issues per group 4 tcgen05.mma (K = 32 each) with A in
-//     tensor memory and B read from the staged slot, and the sum MMA, into one
-//     accumulator of 128 columns per group;
+//     tensor memory and B read from the staged slot into one accumulator of
+//     128 columns per group, and one commit;
 //   - 8 epilogue warps tcgen05.ld each accumulator and add
-//     d_x * d_w * (acc_lo + acc_hi) in packed f32x2 arithmetic.
-// The A operands, the sum operands and the accumulators form one ring of three
-// group stages (3 x 128 accumulator and 3 x 32 A columns of tensor memory, 3 x
-// 4 KB of shared memory for the digits). The MMAs of group g wait on a single
-// barrier: the converters have written A(g) and the digits of g, and the
-// epilogue has read the accumulator of g - 3.
+//     d_x * d_w * (2^9 (acc_lo + acc_hi) - sum(q)) in packed f32x2 arithmetic.
+// The A operands and the accumulators form one ring of three group stages
+// (3 x 128 accumulator and 3 x 32 A columns of tensor memory). The MMAs of
+// group g wait on a single barrier: the converters have written A(g) and the
+// epilogue has read the accumulator of g - 3. One commit per group tells both
+// the epilogue (accumulator g is complete) and the converters (A stage g is
+// free again). Measured on GB300 with clock stamps, the issuing thread sets
+// the pace: each commit and each wait costs it more than an MMA does, so the
+// group's path has one of each.
 #include "tq_tcgen05.cuh"
 
 namespace tq {
@@ -70,7 +72,14 @@ constexpr int kScaleStages = kStages + 1;
 #endif
 constexpr int kInStages = TQ_TC_IN_STAGES;  // staged-input ring in shared memory
 constexpr int kConvWarps = 8;    // converters: warp w -> rows 32*(w%4).., k half w/4
-constexpr int kEpiWarps = 8;     // epilogue: warp w -> rows 32*(w%4).., tokens 32*(w/4)..
+#ifndef TQ_TC_EPI_WARPS
+#define TQ_TC_EPI_WARPS 16
+#endif
+// epilogue: warp w -> rows 32*(w%4).., tokens kEpiTok*(w/4).. (a warp reaches
+// only the tensor-memory lanes of its warp index mod 4)
+constexpr int kEpiWarps = TQ_TC_EPI_WARPS;
+constexpr int kEpiTok = kN / (kEpiWarps / 4);   // tokens per epilogue warp
+static_assert(kEpiWarps % 4 == 0 && kEpiTok % 16 == 0, "epilogue split");
 constexpr int kMmaWarp = kConvWarps + kEpiWarps;
 constexpr int kProdWarp = kMmaWarp + 1;
 constexpr int kThreads = (kProdWarp + 1) * 32;
@@ -80,10 +89,7 @@ constexpr uint32_t kAccCols = kNB;                   // 128 per group
 constexpr uint32_t kACols = kGroup / 4;              // 32 per group: four e4m3 per column
 constexpr uint32_t kAccCol = 0;                      // accumulator stage s: s * 128
 constexpr uint32_t kACol = kStages * kAccCols;       // A stage s: kACol + s * 32
-constexpr uint32_t kASumCol = kACol + kStages * kACols;   // constant A of the sum MMA (16)
-static_assert(kASumCol + 16 <= kTmemCols, "tensor memory overflow");
-// A of the sum MMA, k = 0..3 of every row: e4m3 -2^-9, -2^-5, -2^-1, -2^3.
-constexpr uint32_t kASumWord = 0xD0B09081u;
+static_assert(kACol + kStages * kACols <= kTmemCols, "tensor memory overflow");
 
 // B operand per (token tile, group) in UMMA canonical K-major layout without
 // swizzle: 128 rows (row n < 64: lo of token n; row 64 + n: 16 * hi of token
@@ -93,14 +99,10 @@ constexpr uint32_t kASumWord = 0xD0B09081u;
 constexpr uint32_t kLBO = 128;
 constexpr uint32_t kSBO = 8 * 128;
 constexpr int kBTile = kNB * kGroup;                   // 16384
-// B of the sum MMA per group stage: 128 rows x 32 k, the digits of row n < 64
-// at k = 0..3, zeros elsewhere; LBO = 128, SBO = 256.
-constexpr uint32_t kSBOs = 2 * 128;
-constexpr int kBSumBytes = kNB * kK;                   // 4096
 constexpr float kProdScale = 512.0f;                   // products carry 2^-9
-// per (token tile, block): d_x of 64 tokens (f32), then per group the four
-// e4m3 digits of each token's sum as one 32-bit word
-constexpr int kSumOff = kN;                            // words
+// per (token tile, block): d_x of 64 tokens (f32), then per group minus each
+// token's activation sum (an integer of magnitude at most 16256, exact in f32)
+constexpr int kSumOff = kN;                            // floats
 constexpr int kDxFloats = kN + kGPB * kN;              // 192
 constexpr int kDxBytes = kDxFloats * 4;                // 768
 // one staged slot: the block's B tiles, its weight tiles (per 32-row tile both
@@ -112,11 +114,12 @@ constexpr int kInDx = kInW + kTilesPerCta * kWRun;
 constexpr int kInBytes = kInDx + kDxBytes;
 static_assert(kInBytes % 16 == 0 && kWRun % 16 == 0 && kInW % 16 == 0,
               "bulk copies need 16-byte multiples");
-// scale ring stage: d_w * 2^9 per group and row, then the block's d_x
-constexpr int kScaleFloats = kGPB * kM + kN;
-constexpr int kNumBars = 2 * kInStages + 3 * kStages + 1;   // + the failure drain
-constexpr int kSmemUsed = kInStages * kInBytes + kStages * kBSumBytes +
-                          kScaleStages * kScaleFloats * 4 + kNumBars * 8 + 16;
+// scale ring stage: d_w per group and row, then the block's record (d_x and
+// minus the sums of each group)
+constexpr int kScaleFloats = kGPB * kM + kDxFloats;
+constexpr int kNumBars = 2 * kInStages + 2 * kStages + 1;   // + the failure drain
+constexpr int kSmemUsed = kInStages * kInBytes + kScaleStages * kScaleFloats * 4 +
+                          kNumBars * 8 + 16;
 // Enough shared memory that only one CTA fits on an SM: each CTA allocates
 // all 512 tensor-memory columns.
 constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
@@ -139,17 +142,10 @@ __host__ __device__ inline Layout ws_layout(int64_t cols, int64_t ntok) {
 
 // ---------------------------------------------------------------- pre-pass
 
-// A group's activation sum as the four e4m3 digits the sum MMA reads: sq = d0 + 16 d1 + 256 d2 + 4096 d3, d0..d2 in [0, 15], d3 in
-// [-4, 3].
-__device__ __forceinline__ uint32_t sum_digits(int sq) {
-  return e4m3x2((float)(sq & 15), (float)((sq >> 4) & 15)) |
-         (e4m3x2((float)((sq >> 8) & 15), (float)(sq >> 12)) << 16);
-}
-
 // One CTA per (group g, token tile): thread t takes token t % 64 and k
 // quarter t / 64 (32 activations) and writes two 16-byte core-matrix rows of
 // the low part and two of the high part; the k-quarter-0 threads also write
-// the token's group sum and (for even g) its block scale.
+// minus the token's group sum and (for even g) its block scale.
 __global__ void __launch_bounds__(256) act_pack_kernel(const uint8_t* __restrict__ Xq,
                                                        uint8_t* __restrict__ Bt,
                                                        float* __restrict__ Dx, int64_t ntok,
@@ -197,7 +193,7 @@ __global__ void __launch_bounds__(256) act_pack_kernel(const uint8_t* __restrict
   }
   if (kq == 0) {
     float* rec = Dx + (nt * nblk + (g >> 1)) * kDxFloats;
-    reinterpret_cast<uint32_t*>(rec)[kSumOff + (g & 1) * kN + n] = sum_digits(sq);
+    rec[kSumOff + (g & 1) * kN + n] = (float)(-sq);
     if ((g & 1) == 0) rec[n] = d;
   }
 }
@@ -205,7 +201,7 @@ __global__ void __launch_bounds__(256) act_pack_kernel(const uint8_t* __restrict
 // Fused form of the quantizer and the pre-pass (tq_quantize_matmul): one warp
 // per (token slot, q8_K block) quantizes the f32 activations exactly as the
 // quantizer kernel does (q8K_warp), writes the q8_K block, and writes the
-// token's e4m3 rows of both groups' B tiles, the group sums' digits and the
+// token's e4m3 rows of both groups' B tiles, minus the group sums and the
 // block scale. Token slots past ntok (the last tile's padding) get zeros.
 // Lane l holds values 8l .. 8l + 7: group l / 16, k = 8 (l % 16) .. + 7 of it,
 // bit 2 of k clear for the first four and set for the last four.
@@ -245,9 +241,9 @@ __global__ void __launch_bounds__(kPackWarps * 32) quantize_pack_kernel(
   const int off = (kl >> 4) * kLBO + (kl & 15);
   *reinterpret_cast<uint2*>(tile + (n >> 3) * kSBO + (n & 7) * 16 + off) = make_uint2(l0, l1);
   *reinterpret_cast<uint2*>(tile + ((kN + n) >> 3) * kSBO + (n & 7) * 16 + off) = make_uint2(h0, h1);
-  uint32_t* rec = reinterpret_cast<uint32_t*>(Dx + (nt * nblk + b) * kDxFloats);
-  if ((lane & 15) == 0) rec[kSumOff + gi * kN + n] = sum_digits(sq);
-  if (lane == 0) rec[n] = __float_as_uint(d);
+  float* rec = Dx + (nt * nblk + b) * kDxFloats;
+  if ((lane & 15) == 0) rec[kSumOff + gi * kN + n] = (float)(-sq);
+  if (lane == 0) rec[n] = d;
 }
 
 // ---------------------------------------------------------------- tensor cores
@@ -290,16 +286,16 @@ template <bool kGroupSums>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sIn = smem;                                                         // [in][slot]
-  uint8_t* sBSum = smem + kInStages * kInBytes;                                // [stage][4096]
-  float* sScale = reinterpret_cast<float*>(sBSum + kStages * kBSumBytes);      // [scale][320]
+  float* sScale = reinterpret_cast<float*>(smem + kInStages * kInBytes);       // [scale][448]
   uint64_t* in_full = reinterpret_cast<uint64_t*>(sScale + kScaleStages * kScaleFloats);  // [in]
   uint64_t* in_empty = in_full + kInStages;                                    // [in]
   // mma_ready[s]: the MMAs of group g (stage s = g % 3) may go: the converters
-  // have written A(g) and its digits, and the epilogue has read the
-  // accumulator of g - 3 (the epilogue pre-arrives for groups 0..2).
+  // have written A(g), and the epilogue has read the accumulator of g - 3
+  // (the epilogue pre-arrives for groups 0..2).
   uint64_t* mma_ready = in_empty + kInStages;                                  // [stage]
-  uint64_t* a_free = mma_ready + kStages;                                      // [stage]
-  uint64_t* mma_done = a_free + kStages;                                       // [stage]
+  // mma_done[s]: the MMAs of group g are complete: its accumulator is ready
+  // for the epilogue, and A stage s is free for the converters' group g + 3.
+  uint64_t* mma_done = mma_ready + kStages;                                    // [stage]
   uint64_t* drain_bar = mma_done + kStages;   // after a failure: the MMAs issued are done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
   // Set by a role that gave up a wait (before its next arrival): the producer
@@ -322,20 +318,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
                  ::"r"(smem_u32(tmem_slot)), "r"(kTmemCols) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // the digit tiles are zero outside k = 0..3 of rows 0..63
-  for (int i = tid; i < kStages * kBSumBytes / 16; i += kThreads)
-    reinterpret_cast<uint4*>(sBSum)[i] = make_uint4(0u, 0u, 0u, 0u);
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   if (tid == 0) {
     // Consumer warps arrive once per warp (lane 0, after __syncwarp).
     for (int i = 0; i < kInStages; ++i) {
       mbarrier_init(smem_u32(in_full + i), 1);
-      // converters have read the slot's weights and scales, the MMAs its B
+      // the converters have read the slot's weights and scales, and the MMAs
+      // that read its B are complete (a commit)
       mbarrier_init(smem_u32(in_empty + i), kConvWarps + 1);
     }
     for (int s = 0; s < kStages; ++s) {
       mbarrier_init(smem_u32(mma_ready + s), kConvWarps + kEpiWarps);
-      mbarrier_init(smem_u32(a_free + s), 1);
       mbarrier_init(smem_u32(mma_done + s), 1);
     }
     mbarrier_init(smem_u32(drain_bar), 1);
@@ -347,16 +339,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool failed = false;
-  if (warp < 4) {   // constant A of the sum MMA, one warp per lane quarter
-    uint32_t r[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) r[j] = j == 0 ? kASumWord : 0u;
-    tmem_st16(tmem + ((uint32_t)(warp * 32) << 16) + kASumCol, r);
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
 
   if (warp == kProdWarp) {
     // ---------------- producer: stage block j into slot j % kInStages
@@ -380,6 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
         uint8_t* st = sIn + i * kInBytes;
         const uint32_t full = smem_u32(in_full + i);
         const int g0 = j * kGPB;
+        // the activations first (from L2), then the weights (from HBM)
         mbarrier_arrive_expect_tx(full, (uint32_t)(kInW + nvalid * kWRun + kDxBytes));
         bulk_copy_g2s(smem_u32(st + kInB), a.Bt + (nt * G + g0) * (int64_t)kBTile, kInW, full,
                       policy);
@@ -395,8 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
     // ---------------- converters
     const int q4 = warp & 3, khalf = warp >> 2;          // row quarter, k half of A
     const bool row_ok = rb0 + q4 < a.nrb;
-    // ct < 64 copies d_x of token ct; 64 <= ct < 192 the digits of group
-    // (ct - 64) / 64, token ct % 64
+    // thread ct < 192 copies word ct of the block's record (d_x of 64 tokens,
+    // then minus the sums of each group's 64 tokens) into the scale ring
     const int ct = warp * 32 + lane;
     const uint32_t a_base = tmem + ((uint32_t)(q4 * 32) << 16) + kACol + (uint32_t)khalf * 16;
     int i = 0, sa = 0, ss = 0, g = 0;
@@ -433,27 +416,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
       for (int gi = 0; gi < kGPB; ++gi) {
         // A stage sa is free once the MMAs of group g - kStages have finished
         if (g >= kStages && !failed &&
-            !mbarrier_wait_bounded(smem_u32(a_free + sa), pa ^ 1u, lim))
+            !mbarrier_wait_bounded(smem_u32(mma_done + sa), pa ^ 1u, lim))
           failed = true;
         failed = __any_sync(0xffffffffu, failed);   // tcgen05.st below is warp-wide
         tc_fence_after();
         if (!failed) {
           convert_store(cw[gi], a_base + (uint32_t)sa * kACols);
-          if (ct >= kSumOff + gi * kN && ct < kSumOff + (gi + 1) * kN) {
-            const int n = ct - kSumOff - gi * kN;
-            *reinterpret_cast<uint32_t*>(sBSum + sa * kBSumBytes + (n >> 3) * kSBOs + (n & 7) * 16) =
-                rec;
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          }
           if (gi == 0) {
             float* sst = sScale + ss * kScaleFloats;
             if (khalf == 0) {
 #pragma unroll
               for (int gj = 0; gj < kGPB; ++gj)
-                sst[gj * kM + q4 * 32 + lane] =
-                    __half2float(__ushort_as_half((unsigned short)sc[gj])) * kProdScale;
+                sst[gj * kM + q4 * 32 + lane] = __half2float(__ushort_as_half((unsigned short)sc[gj]));
             }
-            if (ct < kN) sst[kGPB * kM + ct] = __uint_as_float(rec);
+            if (ct < kDxFloats) sst[kGPB * kM + ct] = __uint_as_float(rec);
           }
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         }
@@ -468,13 +444,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
   } else if (warp < kMmaWarp) {
     // ---------------- epilogue
     const int ew = warp - kConvWarps;
-    const int q4 = ew & 3, nhalf = ew >> 2;               // row quarter, token half
+    const int q4 = ew & 3;                                // row quarter
     const int64_t row = (rb0 + q4) * kTileRows + lane;
-    const int n0 = nhalf * 32;
+    const int n0 = (ew >> 2) * kEpiTok;                   // first token
     const uint32_t acc_base = tmem + ((uint32_t)(q4 * 32) << 16) + kAccCol + (uint32_t)n0;
-    uint64_t y2[16];                                      // tokens n0 + 2p, +1
+    const uint64_t k512 = f2_packf(kProdScale, kProdScale);
+    uint64_t y2[kEpiTok / 2];                             // tokens n0 + 2p, +1
 #pragma unroll
-    for (int p = 0; p < 16; ++p) y2[p] = 0ull;
+    for (int p = 0; p < kEpiTok / 2; ++p) y2[p] = 0ull;
     int sa = 0, ss = 0;
     uint32_t pa = 0;
     if (lane == 0) {   // all accumulator stages start free (groups 0..kStages-1)
@@ -493,34 +470,36 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
           const uint32_t tc0 = acc_base + (uint32_t)sa * kAccCols;
           const float dw = sst[gi * kM + q4 * 32 + lane];
           const uint64_t w2 = f2_packf(dw, dw);
+          const float4* nsq4 = reinterpret_cast<const float4*>(sst + kGPB * kM + kSumOff + gi * kN + n0);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < kEpiTok / 16; ++h) {
             uint32_t lo[16], hi[16];
             tmem_ld16_nowait(tc0 + (uint32_t)h * 16, lo);
             tmem_ld16_nowait(tc0 + kN + (uint32_t)h * 16, hi);
             tmem_wait_ld();
 #pragma unroll
             for (int j4 = 0; j4 < 4; ++j4) {
+              const float4 d = dx4[h * 4 + j4];
+              const float4 m = nsq4[h * 4 + j4];          // minus the tokens' sums
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
                 const int j = 4 * j4 + 2 * e;             // token pair n0 + 16h + j, +1
-                // isum * 2^-9 for the two tokens, exact
-                const uint64_t z = f2_add(f2_pack(lo[j], lo[j + 1]), f2_pack(hi[j], hi[j + 1]));
+                const uint64_t z = f2_add(f2_pack(lo[j], lo[j + 1]),
+                                          f2_pack(hi[j], hi[j + 1]));   // sum u q * 2^-9
+                const uint64_t nsq = e == 0 ? f2_packf(m.x, m.y) : f2_packf(m.z, m.w);
+                const uint64_t is = f2_fma(z, k512, nsq);                      // isum, exact
                 if (kGroupSums) {
                   if (row < a.rows) {
-                    const float2 zz = f2_unpack(z);
+                    const float2 ii = f2_unpack(is);
                     const int64_t t = tok0 + n0 + 16 * h + j;
                     if (t < a.ntok)
-                      a.S[(t * a.rows + row) * G + b * kGPB + gi] =
-                          __float2int_rn(zz.x * kProdScale);
+                      a.S[(t * a.rows + row) * G + b * kGPB + gi] = __float2int_rn(ii.x);
                     if (t + 1 < a.ntok)
-                      a.S[((t + 1) * a.rows + row) * G + b * kGPB + gi] =
-                          __float2int_rn(zz.y * kProdScale);
+                      a.S[((t + 1) * a.rows + row) * G + b * kGPB + gi] = __float2int_rn(ii.y);
                   }
                 } else {
-                  const float4 d = dx4[h * 4 + j4];
                   const uint64_t dxp = e == 0 ? f2_packf(d.x, d.y) : f2_packf(d.z, d.w);
-                  y2[8 * h + j / 2] = f2_fma(f2_mul(dxp, w2), z, y2[8 * h + j / 2]);
+                  y2[8 * h + j / 2] = f2_fma(f2_mul(dxp, w2), is, y2[8 * h + j / 2]);
                 }
               }
             }
@@ -535,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
     }
     if (!kGroupSums && !failed && row < a.rows) {
 #pragma unroll
-      for (int p = 0; p < 16; ++p) {
+      for (int p = 0; p < kEpiTok / 2; ++p) {
         const float2 v = f2_unpack(y2[p]);
         const int64_t t = tok0 + n0 + 2 * p;
         if (t < a.ntok) a.Y[t * a.rows + row] = v.x;
@@ -544,7 +523,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
     }
   } else if (lane == 0) {
     // ---------------- MMA issuer
-    const uint64_t sd0 = smem_desc(smem_u32(sBSum), kLBO, kSBOs);
     int i = 0, sa = 0;
     uint32_t pa = 0;
     for (int b = 0; b < nb; ++b) {
@@ -554,7 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
 #pragma unroll
       for (int gi = 0; gi < kGPB; ++gi) {
         // A(g) written and the accumulator of group g - 3 read
-        if (!failed && !mbarrier_wait_bounded(smem_u32(mma_ready + sa), pa, lim)) {
+        if (!failed && !mbarrier_test_wait(smem_u32(mma_ready + sa), pa) &&
+            !mbarrier_wait_bounded(smem_u32(mma_ready + sa), pa, lim)) {
           failed = true;
           *s_failed = 1;
         }
@@ -567,13 +546,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
             mma_e4m3_tmem_a(d, at + (uint32_t)(kK / 4) * kk,
                             bd0 + (uint64_t)((gi * kBTile + kk * 2 * kLBO) >> 4), kIdesc,
                             kk > 0 ? 1u : 0u);
-          mma_e4m3_tmem_a(d, tmem + kASumCol, sd0 + (uint64_t)((sa * kBSumBytes) >> 4), kIdesc, 1u);
         }
-        // the commits fire when these MMAs are done (at once if none were issued)
+        // the commit fires when these MMAs are done (at once if none were issued)
         mma_commit(smem_u32(mma_done + sa));
-        mma_commit(smem_u32(a_free + sa));
         if (++sa == kStages) { sa = 0; pa ^= 1u; }
       }
+      // the slot's B is read once these MMAs are complete
       mma_commit(smem_u32(in_empty + i));
       if (++i == kInStages) i = 0;
     }

@@ -89,6 +89,20 @@ __device__ __forceinline__ bool mbarrier_try_wait(uint32_t bar, uint32_t parity,
   return ok != 0;
 }
 
+// Non-blocking check that phase `parity` of an mbarrier has completed: cheaper
+// than a suspending try_wait when the phase is usually complete already.
+__device__ __forceinline__ bool mbarrier_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for phase `parity` of an mbarrier, giving up after `limit_ns` of global
 // time (checked every 16 polls, with a cap of 2^28 polls). Returns false on
 // giving up; the caller records the failure and stops using the barrier.

@@ -20,9 +20,12 @@ constexpr int kWarpsPerCta = 8;
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
 quantize_q8K_kernel(const float* __restrict__ X, uint8_t* __restrict__ Xq, int64_t nblocks) {
   // Launched as a programmatic dependent: start early, but touch no memory
-  // before the previous kernel in the stream has finished.
-  pdl_launch_dependents();
+  // before the previous kernel in the stream has finished; let the next kernel
+  // start only after that wait, so that when it starts this kernel is the only
+  // one before it that can still run (the matmuls rely on that to request
+  // their weights early).
   pdl_wait_primary();
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t blk = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   if (blk >= nblocks) return;  // whole warp leaves together

@@ -8,9 +8,11 @@ subnormal, m * 2^-9) represents v exactly when v = M * 2^E with an integer
   - activation q in [-127, 127]: lo = q & 15 and 16 * (q >> 4), and both / 4;
   - weight code u in {0, 1, 2} at bits 0-1 of a byte: the byte is u * 2^-9;
     at bits 2-3: u * 4 * 2^-9 (u = 2 sets the lowest exponent bit);
-  - a group's activation sum s in [-16256, 16256] as four base-16 digits with
-    weights -2^-9 * 16^i: d0..d2 in [0, 15], d3 = s >> 12 in [-4, 3].
+  - the epilogue's return from u to w = u - 1: isum = 2^9 * acc - s, with acc
+    the accumulator (a multiple of 2^-9) and s the group's activation sum in
+    [-16256, 16256], one f32 FMA that must be exact.
 """
+import numpy as np
 from fractions import Fraction
 
 
@@ -55,19 +57,22 @@ def test_products_are_multiples_of_two_to_minus_nine():
                     == Fraction(u * q, 512))
 
 
-def test_sum_digits():
-    weights = [Fraction(-1, 512) * 16 ** i for i in range(4)]
-    assert all(w in E4M3 for w in weights)
-    for s in range(-16256, 16257):
-        d = [s & 15, (s >> 4) & 15, (s >> 8) & 15, s >> 12]
-        assert 0 <= min(d[:3]) and max(d[:3]) <= 15 and -4 <= d[3] <= 3
-        assert all(Fraction(x) in E4M3 for x in d)
-        assert sum(w * x for w, x in zip(weights, d)) == Fraction(-s, 512)
+def test_epilogue_correction_exact_in_f32():
+    # acc = N * 2^-9 with |N| <= 128 * 2 * 127 (every u = 2, every |q| = 127);
+    # 2^9 * acc is a power-of-two scaling, and N - s is an integer below 2^24
+    # in magnitude, so f32 gives both exactly: isum = N - s.
+    n = np.arange(-128 * 2 * 127, 128 * 2 * 127 + 1, dtype=np.int64)
+    acc = (n.astype(np.float64) / 512).astype(np.float32)
+    assert np.array_equal(acc.astype(np.float64) * 512, n.astype(np.float64))   # acc exact
+    for sq in (-16256, -12345, -1, 0, 1, 9999, 16256):
+        isum = acc * np.float32(512) + np.float32(-sq)                           # f32 ops
+        assert isum.dtype == np.float32
+        assert np.array_equal(isum.astype(np.int64), n - sq)
 
 
 def test_accumulator_stays_exact_in_f32():
     # Every partial sum of a group (up to 128 products u * q * 2^-9 with
-    # |u * q| <= 254, plus the sum term) is N * 2^-9 with |N| below 2^16: at
-    # most 16 significant bits, so f32 (24) holds every one exactly.
-    bound = 128 * 2 * 127 + 16256
-    assert bound < 2 ** 16
+    # |u * q| <= 254) is N * 2^-9 with |N| below 2^15: at most 15 significant
+    # bits, so f32 (24) holds every one exactly.
+    bound = 128 * 2 * 127
+    assert bound < 2 ** 15

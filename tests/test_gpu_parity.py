@@ -159,8 +159,8 @@ def test_exact_integer_mode(ntok):
 def test_extremes(ntok):
     """All u = 2 (w = +1) or all u = 0 against q = +-127: the largest group sums,
     and activation sums of -16256, 0 and +16256 (the e4m3 path splits each q
-    into q & 15 and 16 (q >> 4) and the sum into four base-16 digits; these are
-    the extremes of both), on the plain and the workspace forms."""
+    into q & 15 and 16 (q >> 4) and subtracts the sum in its epilogue; these
+    are the extremes of both), on the plain and the workspace forms."""
     rows, cols = 64, 512
     for code in (0, 2):
         wpq = synth.pack_pq2_0(np.full((rows, cols), code, np.uint8),
