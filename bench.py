@@ -56,6 +56,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # exactly into two e4m3 parts (two MMA columns).
 E4M3_PER_BF16 = 2.0
 MMA_FLOPS_PER_FLOP = 2.0
+# Token counts the library runs as a GEMV (one weight pass, one fused launch)
+GEMV_MAX_TOKENS = 16
 
 WORKLOADS = {
     "decode": "decode GEMV 32768x8192 pq2_0 x q8_K, ntok=1",
@@ -219,16 +221,16 @@ class Workload:
         self.device = device
 
     def step(self, i, stream=None):
-        """quantize + matmul: one fused launch for ntok <= 8."""
+        """quantize + matmul: one fused launch for ntok <= GEMV_MAX_TOKENS."""
         import bit_matvec_gb300 as tq
         tq.tq_quantize_matmul(self.W[i % self.copies], self.X, self.Xq, self.Y, self.rows,
                               self.cols, self.ntok, self.ws, stream)
 
     def matmul_only(self, i, stream=None):
-        """The dominant kernel alone: the fused GEMV for ntok <= 8 (it is the
+        """The dominant kernel alone: the fused GEMV for ntok <= GEMV_MAX_TOKENS (it is the
         whole step), the workspace tensor-core matmul otherwise."""
         import bit_matvec_gb300 as tq
-        if self.ntok <= 8:
+        if self.ntok <= GEMV_MAX_TOKENS:
             self.step(i, stream)
         else:
             tq.tq_matmul_ws(self.W[i % self.copies], self.Xq, self.Y, self.rows, self.cols,
@@ -237,7 +239,7 @@ class Workload:
     def launches(self):
         # tq_quantize_matmul: one fused GEMV launch up to 8 tokens; above, the
         # quantize-and-pack kernel and the tensor-core kernel
-        return 1 if self.ntok <= 8 else 2
+        return 1 if self.ntok <= GEMV_MAX_TOKENS else 2
 
     def weights(self):
         return self.rows * self.cols
@@ -282,7 +284,7 @@ class ReplayWorkload:
                                       self.ntok, self.ws, stream)
 
     def launches(self):
-        return (1 if self.ntok <= 8 else 2) * self.blocks * len(self.mats)
+        return (1 if self.ntok <= GEMV_MAX_TOKENS else 2) * self.blocks * len(self.mats)
 
     def weights(self):
         return self.blocks * sum(m["rows"] * m["cols"] for m in self.mats)
@@ -483,7 +485,7 @@ def time_graph(wl: Workload, steps: int, warmup: int, world: int):
         gb = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gb, stream=stream):
             for i in range(n):
-                if wl.ntok > 8:
+                if wl.ntok > GEMV_MAX_TOKENS:
                     tq.tq_quantize_q8K(wl.X, wl.Xq, wl.ntok, wl.cols, stream)
                 ev[i][0].record(stream)
                 wl.matmul_only(i, stream)
@@ -744,7 +746,7 @@ def measure(name, args, rank, world, device, peaks, peak_kind, steps):
         res["gweights_per_s"] = world * wl.weights() / (step_ms * 1e-3) / 1e9
     res["gmac_per_s"] = world * wl.macs() / (step_ms * 1e-3) / 1e9
     res["hbm_gbs_step"] = (abytes + quantize_bytes(wl.ntok, wl.cols)) / (step_ms * 1e-3) / 1e9
-    if wl.ntok <= 8:
+    if wl.ntok <= GEMV_MAX_TOKENS:
         achieved = abytes / (kern_ms * 1e-3) / 1e9
         peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         traffic = profile_traffic(f"gemv_{name}_ncu.txt", GEMV_FILES)
@@ -863,7 +865,7 @@ def main():
             if want_cpu:
                 r["cpu_baseline"] = cpu_baseline_entry(*oracle_replay_rate(ntok, 5.0))
             extra[f"replay_ntok{ntok}"] = r
-    if wl.ntok <= 8 and not args.no_read_ceiling:
+    if wl.ntok <= GEMV_MAX_TOKENS and not args.no_read_ceiling:
         main_res["roofline"]["read_ceiling"] = measure_read_ceiling(
             main_res["roofline"]["algorithmic_bytes"] // 16 * 16, device, args.warmup)
 
@@ -902,7 +904,7 @@ def main():
             "higher_is_better": True, "scaling": "weak",
             "vs_baseline": (value / PAGES_DECODE_GWEIGHTS
                             if args.workload == "decode" else None),
-            "dtype": "int8" if wl.ntok <= 8 else "e4m3 (exact integer sums)",
+            "dtype": "int8" if wl.ntok <= GEMV_MAX_TOKENS else "e4m3 (exact integer sums)",
             "data": "synthetic (seeded splitmix64; no model weights)",
             "config": {"workload": WORKLOADS[args.workload], "rows": wl.rows, "cols": wl.cols,
                        "ntok": wl.ntok,

@@ -162,8 +162,12 @@ cudaError_t device_status_ptr(int** out) {
 
 int64_t q8K_bytes(int64_t ntok, int64_t cols) { return ntok * (cols / kQK) * kQ8KBytes; }
 
+// With a workspace, tokens beyond this many go to the tensor cores (a token
+// tile of 16, 32 or 64); without one the GEMV takes up to gemv_max_tokens().
+constexpr int kWsGemvMaxTok = 8;
+
 int64_t workspace_bytes(int64_t rows, int64_t cols, int64_t ntok) {
-  if (rows <= 0 || cols <= 0 || ntok <= gemv_max_tokens()) return 0;
+  if (rows <= 0 || cols <= 0 || ntok <= kWsGemvMaxTok) return 0;
   return tc_workspace_bytes(cols, ntok);
 }
 
@@ -207,10 +211,11 @@ int matmul_impl(const void* Wtq, const void* Xq, float* Y, int32_t* S, int64_t r
   if (e != cudaSuccess) return fail_cuda(e);
   const int64_t w_bytes = tq_repacked_bytes(rows, cols);
   const bool early = early_weights_ok(s, Wtq, w_bytes);
+  const bool gemv = ntok <= (use_ws ? kWsGemvMaxTok : gemv_max_tokens());
   const bool inputs_final =
-      ntok <= gemv_max_tokens() && gemv_inputs_final(s, Xq, q8K_bytes(ntok, cols), Wtq, w_bytes);
+      gemv && gemv_inputs_final(s, Xq, q8K_bytes(ntok, cols), Wtq, w_bytes);
   note_op(s, kOpOther);
-  if (ntok <= gemv_max_tokens()) {
+  if (gemv) {
     e = launch_gemv(W, X, Y, S, rows, cols, (int)ntok, status, early, inputs_final, s);
     if (e == cudaSuccess) {
       note_kernel(s, kOpGemv, out, out_bytes);
@@ -231,6 +236,8 @@ int matmul_impl(const void* Wtq, const void* Xq, float* Y, int32_t* S, int64_t r
 }  // namespace
 
 void record_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
+
+int ws_gemv_max_tokens() { return kWsGemvMaxTok; }
 
 namespace {
 std::atomic<int64_t> g_debug_stall_ns{0};
@@ -426,7 +433,7 @@ int tq_quantize_matmul(const void* Wtq, const float* X, void* Xq, float* Y, int6
       return TQ_ERR_ALIAS;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (ntok <= gemv_max_tokens()) {
+  if (ntok <= kWsGemvMaxTok) {
     int* status = nullptr;
     cudaError_t e = device_status_ptr(&status);
     if (e != cudaSuccess) return fail_cuda(e);

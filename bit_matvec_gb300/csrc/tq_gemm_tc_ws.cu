@@ -55,106 +55,140 @@ namespace {
 using namespace tc;
 
 constexpr int kM = 128;            // weight rows per CTA (UMMA M)
-constexpr int kN = 64;             // tokens per CTA
-constexpr int kNB = 2 * kN;        // UMMA N: low and high parts of 64 tokens
 constexpr int kK = 32;             // UMMA K of kind::f8f6f4
 constexpr int kGPB = kQK / kGroup;     // groups per q8_K block (2)
 constexpr int kMmaPerGroup = kGroup / kK;   // 4
-constexpr int kStages = 3;         // A + accumulator ring in tensor memory, one group each
-// d_w, d_x and the group sums per block, written by the converters and read by
-// the epilogue. A converter writing block b has seen the MMAs of group
-// 2b - kStages finish, which were issued after the epilogue released group
-// 2b - 2 kStages; the epilogue then is past block b - kStages, so a ring of
-// kStages + 1 blocks is never overwritten while read.
-constexpr int kScaleStages = kStages + 1;
-#ifndef TQ_TC_IN_STAGES
-#define TQ_TC_IN_STAGES 3
-#endif
-constexpr int kInStages = TQ_TC_IN_STAGES;  // staged-input ring in shared memory
 constexpr int kConvWarps = 8;    // converters: warp w -> rows 32*(w%4).., k half w/4
-#ifndef TQ_TC_EPI_WARPS
-#define TQ_TC_EPI_WARPS 16
-#endif
-// epilogue: warp w -> rows 32*(w%4).., tokens kEpiTok*(w/4).. (a warp reaches
-// only the tensor-memory lanes of its warp index mod 4)
-constexpr int kEpiWarps = TQ_TC_EPI_WARPS;
-constexpr int kEpiTok = kN / (kEpiWarps / 4);   // tokens per epilogue warp
-static_assert(kEpiWarps % 4 == 0 && kEpiTok % 16 == 0, "epilogue split");
-constexpr int kMmaWarp = kConvWarps + kEpiWarps;
-constexpr int kProdWarp = kMmaWarp + 1;
-constexpr int kThreads = (kProdWarp + 1) * 32;
+constexpr int kEpiTok = 16;      // tokens per epilogue warp
 constexpr int kTilesPerCta = kM / kTileRows;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCols = kNB;                   // 128 per group
 constexpr uint32_t kACols = kGroup / 4;              // 32 per group: four e4m3 per column
-constexpr uint32_t kAccCol = 0;                      // accumulator stage s: s * 128
-constexpr uint32_t kACol = kStages * kAccCols;       // A stage s: kACol + s * 32
-static_assert(kACol + kStages * kACols <= kTmemCols, "tensor memory overflow");
-
+constexpr uint32_t kAccCol = 0;                      // accumulator stage s: s * kNB
 // B operand per (token tile, group) in UMMA canonical K-major layout without
-// swizzle: 128 rows (row n < 64: lo of token n; row 64 + n: 16 * hi of token
-// n) x 128 k, one byte each. A core matrix is 8 rows x 16 bytes stored as 128
+// swizzle: 2N rows (row n < N: lo of token n; row N + n: 16 * hi of token n)
+// x 128 k, one byte each. A core matrix is 8 rows x 16 bytes stored as 128
 // contiguous bytes; LBO = 128 (next 16 k), SBO = 1024 (next 8 rows). The MMA
 // for k = 32 kk.. starts kk * 256 bytes in.
 constexpr uint32_t kLBO = 128;
 constexpr uint32_t kSBO = 8 * 128;
-constexpr int kBTile = kNB * kGroup;                   // 16384
 constexpr float kProdScale = 512.0f;                   // products carry 2^-9
-// per (token tile, block): d_x of 64 tokens (f32), then per group minus each
-// token's activation sum (an integer of magnitude at most 16256, exact in f32)
-constexpr int kSumOff = kN;                            // floats
-constexpr int kDxFloats = kN + kGPB * kN;              // 192
-constexpr int kDxBytes = kDxFloats * 4;                // 768
-// one staged slot: the block's B tiles, its weight tiles (per 32-row tile both
-// groups, adjacent), its scales and sums
-constexpr int kInB = 0;
-constexpr int kInW = kGPB * kBTile;
 constexpr int kWRun = kGPB * kTileBytes;               // one 32-row tile, both groups
-constexpr int kInDx = kInW + kTilesPerCta * kWRun;
-constexpr int kInBytes = kInDx + kDxBytes;
-static_assert(kInBytes % 16 == 0 && kWRun % 16 == 0 && kInW % 16 == 0,
-              "bulk copies need 16-byte multiples");
-// scale ring stage: d_w per group and row, then the block's record (d_x and
-// minus the sums of each group)
-constexpr int kScaleFloats = kGPB * kM + kDxFloats;
-constexpr int kNumBars = 2 * kInStages + 2 * kStages + 1;   // + the failure drain
-constexpr int kSmemUsed = kInStages * kInBytes + kScaleStages * kScaleFloats * 4 +
-                          kNumBars * 8 + 16;
-// Enough shared memory that only one CTA fits on an SM: each CTA allocates
-// all 512 tensor-memory columns.
-constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
-constexpr uint32_t kIdesc = idesc_e4m3(kM, kNB);
+constexpr int kInB = 0;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-struct Layout {
-  int64_t ntile;      // 64-token tiles
-  int64_t b_bytes;    // ntile * G * 16 KB
-  int64_t dx_bytes;   // ntile * nblk * 768
+// Everything that depends on the token tile N (16, 32 or 64 tokens per CTA).
+// A smaller tile for fewer tokens: a smaller B per group (less to stage and
+// to read from L2), fewer accumulator columns for the epilogue to read, and
+// room in tensor memory for more group stages.
+template <int N>
+struct TcCfg {
+  static_assert(N == 16 || N == 32 || N == 64, "token tile");
+  static constexpr int kN = N;                         // tokens per CTA
+  static constexpr int kNB = 2 * N;                    // UMMA N: low and high parts
+  // A + accumulator ring in tensor memory, one group per stage
+  static constexpr int kStages = (int)(kTmemCols / (kNB + kACols));
+  // d_w, d_x and the group sums per block, written by the converters and
+  // read by the epilogue. A converter writing block b has seen the MMAs of
+  // group 2b - kStages finish, which were issued after the epilogue released
+  // group 2b - 2 kStages; the epilogue then is past block b - kStages - 1, so
+  // a ring of kStages + 1 blocks is never overwritten while read.
+  static constexpr int kScaleStages = kStages + 1;
+  static constexpr int kInStages = N == 64 ? 3 : N == 32 ? 4 : 6;   // staged-input ring
+  // epilogue: warp w -> rows 32*(w%4).., tokens kEpiTok*(w/4).. (a warp reaches
+  // only the tensor-memory lanes of its warp index mod 4)
+  static constexpr int kEpiWarps = 4 * (N / kEpiTok);
+  static constexpr int kMmaWarp = kConvWarps + kEpiWarps;
+  static constexpr int kProdWarp = kMmaWarp + 1;
+  static constexpr int kThreads = (kProdWarp + 1) * 32;
+  static constexpr uint32_t kAccCols = kNB;
+  static constexpr uint32_t kACol = kStages * kAccCols;   // A stage s: kACol + s * 32
+  static_assert(kACol + kStages * kACols <= kTmemCols, "tensor memory overflow");
+  static constexpr int kBTile = kNB * kGroup;
+  // per (token tile, block): d_x of N tokens (f32), then per group minus each
+  // token's activation sum (an integer of magnitude at most 16256, exact in f32)
+  static constexpr int kSumOff = N;                    // floats
+  static constexpr int kDxFloats = N + kGPB * N;
+  static constexpr int kDxBytes = kDxFloats * 4;
+  // one staged slot: the block's B tiles, its weight tiles (per 32-row tile
+  // both groups, adjacent), its scales and sums
+  static constexpr int kInW = kGPB * kBTile;
+  static constexpr int kInDx = kInW + kTilesPerCta * kWRun;
+  static constexpr int kInBytes = kInDx + kDxBytes;
+  static_assert(kInBytes % 16 == 0 && kWRun % 16 == 0 && kInW % 16 == 0 && kDxBytes % 16 == 0,
+                "bulk copies need 16-byte multiples");
+  // scale ring stage: d_w per group and row, then the block's record (d_x and
+  // minus the sums of each group)
+  static constexpr int kScaleFloats = kGPB * kM + kDxFloats;
+  static constexpr int kNumBars = 2 * kInStages + 2 * kStages + 1;   // + the failure drain
+  static constexpr int kSmemUsed = kInStages * kInBytes + kScaleStages * kScaleFloats * 4 +
+                                   kNumBars * 8 + 16;
+  // Enough shared memory that only one CTA fits on an SM: each CTA allocates
+  // all 512 tensor-memory columns.
+  static constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
+  static constexpr uint32_t kIdesc = idesc_e4m3(kM, kNB);
 };
 
+// Local names for the token tile's constants inside a function templated on N.
+#define TQ_TC_CFG(N)                                                        \
+  using Cfg_ = TcCfg<N>;                                                    \
+  constexpr int kN = Cfg_::kN;                                              \
+  constexpr int kNB = Cfg_::kNB;                                            \
+  constexpr int kStages = Cfg_::kStages;                                    \
+  constexpr int kScaleStages = Cfg_::kScaleStages;                          \
+  constexpr int kInStages = Cfg_::kInStages;                                \
+  constexpr int kEpiWarps = Cfg_::kEpiWarps;                                \
+  constexpr int kMmaWarp = Cfg_::kMmaWarp;                                  \
+  constexpr int kProdWarp = Cfg_::kProdWarp;                                \
+  constexpr int kThreads = Cfg_::kThreads;                                  \
+  constexpr uint32_t kAccCols = Cfg_::kAccCols;                             \
+  constexpr uint32_t kACol = Cfg_::kACol;                                   \
+  constexpr int kBTile = Cfg_::kBTile;                                      \
+  constexpr int kSumOff = Cfg_::kSumOff;                                    \
+  constexpr int kDxFloats = Cfg_::kDxFloats;                                \
+  constexpr int kDxBytes = Cfg_::kDxBytes;                                  \
+  constexpr int kInW = Cfg_::kInW;                                          \
+  constexpr int kInDx = Cfg_::kInDx;                                        \
+  constexpr int kInBytes = Cfg_::kInBytes;                                  \
+  constexpr int kScaleFloats = Cfg_::kScaleFloats;                          \
+  constexpr uint32_t kIdesc = Cfg_::kIdesc;                                 \
+  (void)kN; (void)kNB; (void)kStages; (void)kScaleStages; (void)kInStages;  \
+  (void)kEpiWarps; (void)kMmaWarp; (void)kProdWarp; (void)kThreads;          \
+  (void)kAccCols; (void)kACol; (void)kBTile; (void)kSumOff; (void)kDxFloats; \
+  (void)kDxBytes; (void)kInW; (void)kInDx; (void)kInBytes; (void)kScaleFloats; \
+  (void)kIdesc
+
+struct Layout {
+  int64_t ntile;      // N-token tiles
+  int64_t b_bytes;    // ntile * G * kBTile
+  int64_t dx_bytes;   // ntile * nblk * kDxBytes
+};
+
+template <int N>
 __host__ __device__ inline Layout ws_layout(int64_t cols, int64_t ntok) {
   Layout l;
-  l.ntile = (ntok + kN - 1) / kN;
-  l.b_bytes = l.ntile * (cols / kGroup) * kBTile;
-  l.dx_bytes = l.ntile * (cols / kQK) * kDxBytes;
+  l.ntile = (ntok + N - 1) / N;
+  l.b_bytes = l.ntile * (cols / kGroup) * TcCfg<N>::kBTile;
+  l.dx_bytes = l.ntile * (cols / kQK) * TcCfg<N>::kDxBytes;
   return l;
 }
 
 // ---------------------------------------------------------------- pre-pass
 
-// One CTA per (group g, token tile): thread t takes token t % 64 and k
-// quarter t / 64 (32 activations) and writes two 16-byte core-matrix rows of
-// the low part and two of the high part; the k-quarter-0 threads also write
-// minus the token's group sum and (for even g) its block scale.
-__global__ void __launch_bounds__(256) act_pack_kernel(const uint8_t* __restrict__ Xq,
-                                                       uint8_t* __restrict__ Bt,
-                                                       float* __restrict__ Dx, int64_t ntok,
-                                                       int ngroups, int nblk) {
+// One CTA of 4N threads per (group g, token tile): thread t takes token t % N
+// and k quarter t / N (32 activations) and writes two 16-byte core-matrix rows
+// of the low part and two of the high part; the k-quarter-0 threads also
+// write minus the token's group sum and (for even g) its block scale.
+template <int N>
+__global__ void __launch_bounds__(4 * N) act_pack_kernel(const uint8_t* __restrict__ Xq,
+                                                         uint8_t* __restrict__ Bt,
+                                                         float* __restrict__ Dx, int64_t ntok,
+                                                         int ngroups, int nblk) {
+  TQ_TC_CFG(N);
   pdl_launch_dependents();
   pdl_wait_primary();   // the q8_K activations come from the previous kernel
   const int g = blockIdx.x;
   const int64_t nt = blockIdx.y;
-  const int n = threadIdx.x & (kN - 1), kq = threadIdx.x >> 6;
+  const int n = threadIdx.x % kN, kq = threadIdx.x / kN;
   const int64_t tok = nt * kN + n;
   uint32_t q[8];
   float d = 0.0f;
@@ -207,9 +241,11 @@ __global__ void __launch_bounds__(256) act_pack_kernel(const uint8_t* __restrict
 // bit 2 of k clear for the first four and set for the last four.
 constexpr int kPackWarps = 8;
 
+template <int N>
 __global__ void __launch_bounds__(kPackWarps * 32) quantize_pack_kernel(
     const float* __restrict__ X, uint8_t* __restrict__ Xq, uint8_t* __restrict__ Bt,
     float* __restrict__ Dx, int64_t ntok, int ngroups, int nblk, int64_t nslots) {
+  TQ_TC_CFG(N);
   pdl_launch_dependents();
   // the workspace and Xq may still be read by the previous kernel in the stream
   pdl_wait_primary();
@@ -282,8 +318,9 @@ __device__ __forceinline__ void convert_store(const uint4 codes, uint32_t taddr)
   tmem_st16(taddr, wa);
 }
 
-template <bool kGroupSums>
-__global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a) {
+template <int N, bool kGroupSums>
+__global__ void __launch_bounds__(TcCfg<N>::kThreads, 1) gemm_tc_ws_kernel(const WsArgs a) {
+  TQ_TC_CFG(N);
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sIn = smem;                                                         // [in][slot]
   float* sScale = reinterpret_cast<float*>(smem + kInStages * kInBytes);       // [scale][448]
@@ -584,34 +621,41 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_ws_kernel(const WsArgs a)
   }
 }
 
+// The token tile for ntok tokens: the smallest of 16, 32, 64 that holds them
+// all, 64 above.
+inline int tile_tokens(int64_t ntok) { return ntok <= 16 ? 16 : ntok <= 32 ? 32 : 64; }
+
 }  // namespace
 
 int64_t tc_workspace_bytes(int64_t cols, int64_t ntok) {
-  const Layout l = ws_layout(cols, ntok);
+  Layout l;
+  switch (tile_tokens(ntok)) {
+    case 16: l = ws_layout<16>(cols, ntok); break;
+    case 32: l = ws_layout<32>(cols, ntok); break;
+    default: l = ws_layout<64>(cols, ntok); break;
+  }
   return l.b_bytes + l.dx_bytes;
 }
 
 namespace {
 
 // The tensor-core kernel over a workspace already packed.
+template <int N>
 cudaError_t launch_main(const uint8_t* Wtq, float* Y, int32_t* S, int64_t rows, int64_t cols,
                         int64_t ntok, uint8_t* ws, int* dev_status, cudaStream_t s) {
-  const Layout l = ws_layout(cols, ntok);
-  const int G = (int)(cols / kGroup), nblk = (int)(cols / kQK);
-  uint8_t* Bt = ws;
-  float* Dx = reinterpret_cast<float*>(ws + l.b_bytes);
-  cudaError_t e;
+  using C = TcCfg<N>;
+  const Layout l = ws_layout<N>(cols, ntok);
   WsArgs a;
   a.Wtq = Wtq;
-  a.Bt = Bt;
-  a.Dx = Dx;
+  a.Bt = ws;
+  a.Dx = reinterpret_cast<float*>(ws + l.b_bytes);
   a.Y = Y;
   a.S = S;
   a.status = dev_status;
   a.rows = rows;
   a.ntok = ntok;
-  a.ngroups = G;
-  a.nblk = nblk;
+  a.ngroups = (int)(cols / kGroup);
+  a.nblk = (int)(cols / kQK);
   a.nrb = (int)((rows + kTileRows - 1) / kTileRows);
   const int64_t stall_ns = take_debug_stall();
   a.stall = stall_ns > 0 ? 1 : 0;
@@ -619,14 +663,40 @@ cudaError_t launch_main(const uint8_t* Wtq, float* Y, int32_t* S, int64_t rows, 
   const int64_t gx = (rows + kM - 1) / kM;
   if (gx > 0x7fffffff) return cudaErrorInvalidConfiguration;
   const dim3 grid((unsigned)gx, (unsigned)l.ntile);
-  if (S) {
-    e = ensure_dynamic_smem(reinterpret_cast<const void*>(&gemm_tc_ws_kernel<true>), kSmemBytes);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(gemm_tc_ws_kernel<true>, grid, dim3(kThreads), kSmemBytes, s, a);
-  }
-  e = ensure_dynamic_smem(reinterpret_cast<const void*>(&gemm_tc_ws_kernel<false>), kSmemBytes);
+  auto kernel = S ? gemm_tc_ws_kernel<N, true> : gemm_tc_ws_kernel<N, false>;
+  const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  return launch_pdl(gemm_tc_ws_kernel<false>, grid, dim3(kThreads), kSmemBytes, s, a);
+  return launch_pdl(kernel, grid, dim3(C::kThreads), (size_t)C::kSmemBytes, s, a);
+}
+
+template <int N>
+cudaError_t launch_ws(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t* S, int64_t rows,
+                      int64_t cols, int64_t ntok, uint8_t* ws, int* dev_status, cudaStream_t s) {
+  const Layout l = ws_layout<N>(cols, ntok);
+  const int G = (int)(cols / kGroup), nblk = (int)(cols / kQK);
+  if (l.ntile > 65535) return cudaErrorInvalidConfiguration;
+  cudaError_t e = launch_pdl(act_pack_kernel<N>, dim3((unsigned)G, (unsigned)l.ntile),
+                             dim3(4 * N), 0, s, Xq, ws, reinterpret_cast<float*>(ws + l.b_bytes),
+                             ntok, G, nblk);
+  if (e != cudaSuccess) return e;
+  return launch_main<N>(Wtq, Y, S, rows, cols, ntok, ws, dev_status, s);
+}
+
+template <int N>
+cudaError_t launch_quantize_ws(const float* X, uint8_t* Xq, const uint8_t* Wtq, float* Y,
+                               int64_t rows, int64_t cols, int64_t ntok, uint8_t* ws,
+                               int* dev_status, cudaStream_t s) {
+  const Layout l = ws_layout<N>(cols, ntok);
+  const int nblk = (int)(cols / kQK);
+  if (l.ntile > 65535) return cudaErrorInvalidConfiguration;
+  const int64_t warps = l.ntile * N * nblk;
+  const int64_t grid = (warps + kPackWarps - 1) / kPackWarps;
+  if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  cudaError_t e = launch_pdl(quantize_pack_kernel<N>, dim3((unsigned)grid), dim3(kPackWarps * 32),
+                             0, s, X, Xq, ws, reinterpret_cast<float*>(ws + l.b_bytes), ntok,
+                             (int)(cols / kGroup), nblk, l.ntile * N);
+  if (e != cudaSuccess) return e;
+  return launch_main<N>(Wtq, Y, nullptr, rows, cols, ntok, ws, dev_status, s);
 }
 
 }  // namespace
@@ -635,30 +705,22 @@ cudaError_t launch_gemm_tc_ws(const uint8_t* Wtq, const uint8_t* Xq, float* Y, i
                               int64_t rows, int64_t cols, int64_t ntok, uint8_t* ws,
                               int* dev_status, cudaStream_t s) {
   if (rows <= 0 || ntok <= 0 || cols <= 0) return cudaSuccess;
-  const Layout l = ws_layout(cols, ntok);
-  const int G = (int)(cols / kGroup), nblk = (int)(cols / kQK);
-  if (l.ntile > 65535) return cudaErrorInvalidConfiguration;
-  cudaError_t e = launch_pdl(act_pack_kernel, dim3((unsigned)G, (unsigned)l.ntile), dim3(256), 0,
-                             s, Xq, ws, reinterpret_cast<float*>(ws + l.b_bytes), ntok, G, nblk);
-  if (e != cudaSuccess) return e;
-  return launch_main(Wtq, Y, S, rows, cols, ntok, ws, dev_status, s);
+  switch (tile_tokens(ntok)) {
+    case 16: return launch_ws<16>(Wtq, Xq, Y, S, rows, cols, ntok, ws, dev_status, s);
+    case 32: return launch_ws<32>(Wtq, Xq, Y, S, rows, cols, ntok, ws, dev_status, s);
+    default: return launch_ws<64>(Wtq, Xq, Y, S, rows, cols, ntok, ws, dev_status, s);
+  }
 }
 
 cudaError_t launch_quantize_gemm_tc_ws(const float* X, uint8_t* Xq, const uint8_t* Wtq, float* Y,
                                        int64_t rows, int64_t cols, int64_t ntok, uint8_t* ws,
                                        int* dev_status, cudaStream_t s) {
   if (rows <= 0 || ntok <= 0 || cols <= 0) return cudaSuccess;
-  const Layout l = ws_layout(cols, ntok);
-  const int nblk = (int)(cols / kQK);
-  if (l.ntile > 65535) return cudaErrorInvalidConfiguration;
-  const int64_t warps = l.ntile * kN * nblk;
-  const int64_t grid = (warps + kPackWarps - 1) / kPackWarps;
-  if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  cudaError_t e = launch_pdl(quantize_pack_kernel, dim3((unsigned)grid), dim3(kPackWarps * 32), 0,
-                             s, X, Xq, ws, reinterpret_cast<float*>(ws + l.b_bytes), ntok,
-                             (int)(cols / kGroup), nblk, l.ntile * kN);
-  if (e != cudaSuccess) return e;
-  return launch_main(Wtq, Y, nullptr, rows, cols, ntok, ws, dev_status, s);
+  switch (tile_tokens(ntok)) {
+    case 16: return launch_quantize_ws<16>(X, Xq, Wtq, Y, rows, cols, ntok, ws, dev_status, s);
+    case 32: return launch_quantize_ws<32>(X, Xq, Wtq, Y, rows, cols, ntok, ws, dev_status, s);
+    default: return launch_quantize_ws<64>(X, Xq, Wtq, Y, rows, cols, ntok, ws, dev_status, s);
+  }
 }
 
 }  // namespace tq

@@ -1,4 +1,4 @@
-// tq_gemv.cu -- ternary x q8_K product for 1..8 tokens, bound by the weight
+// tq_gemv.cu -- ternary x q8_K product for 1..16 tokens, bound by the weight
 // stream from HBM.
 //
 // Decode reads every weight once per token batch, so the bus is the limit
@@ -64,7 +64,8 @@ namespace {
 #define TQ_GEMV_EVEN_GRID 1
 #endif
 
-constexpr int kMaxTok = 8;
+constexpr int kMaxTok = 16;         // tokens the GEMV takes (in one launch up to 8 with dp4a)
+constexpr int kMaxDp4aTok = 8;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // Per token count: warps (each owns tiles of every stage), stage size, and
@@ -421,7 +422,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
   }
 }
 
-// ---------------------------------------------------------------- 2..8 tokens
+// ---------------------------------------------------------------- 4..16 tokens
 //
 // With several tokens the dp4a loop pays one dot instruction per 4 weights
 // per token. From TQ_GEMV_MMA_MIN_TOK tokens up this variant runs the group
@@ -443,18 +444,25 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
 // 16q + 4s + {2,3} (a2, a3) of code word q of a 64-weight half c; B token g8,
 // the same four activations; C rows g8, g8 + 8, tokens 2q, 2q + 1.
 
-constexpr int kMmaReducers = 8;   // warps that add one of the 8 C positions per lane
-
 // The tensor-core variant's shape: T's warps, and TPW tiles per warp and stage
-// (two, or one where the larger ring and T rows of f16 activations do not fit
-// in shared memory).
+// (two, or one where the larger ring and the activations do not fit in
+// shared memory). Up to 8 tokens fill the 8 columns of one MMA and the
+// activations sit in shared memory as f16 already scaled for their slot;
+// 9 to 16 tokens take two MMAs of 8 columns per weight fragment (the weights
+// stream once for all of them), and, since 16 rows of f16 activations would
+// leave no room for the weight ring, the activations sit there as int8 and
+// each B fragment is converted when it is used (exactly).
 template <int T, int TPW>
 struct MmaCfg {
-  static constexpr int kWarps = Cfg<T>::kWarps;
+  static constexpr int kWarps = Cfg<(T > 8 ? 8 : T)>::kWarps;
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kTilesPerWarp = TPW;
   static constexpr int kStageTiles = kWarps * TPW;
   static constexpr int kStageBytes = kStageTiles * kTileBytes;
+  static constexpr int kNB = (T + 7) / 8;        // 8-column token blocks
+  static constexpr bool kI8 = T > 8;             // int8 activations in shared memory
+  static constexpr int kReducers = 8 * kNB;      // C positions per lane, one reducing warp each
+  static_assert(kReducers <= kWarps, "one reducing warp per C position");
 };
 
 struct MmaPlan {
@@ -466,15 +474,16 @@ template <int T, int TPW>
 __host__ __device__ inline MmaPlan plan_mma(int stages, int64_t cols) {
   MmaPlan p;
   const int64_t g = cols / kGroup, b = cols / kQK;
-  p.sb_stride = cols * 2 + 8;
+  // bytes per token row; the pad spreads the rows' fragments over the banks
+  p.sb_stride = MmaCfg<T, TPW>::kI8 ? cols + 4 : cols * 2 + 8;
   p.ring = 0;
   p.bars = (int64_t)stages * MmaCfg<T, TPW>::kStageBytes;
   p.counters = p.bars + (stages + 4) * 8;                  // int[S] released, int[S] issued
   p.sb = (p.counters + stages * 8 + 15) / 16 * 16;
-  p.sgsum = p.sb + T * p.sb_stride;
+  p.sgsum = (p.sb + T * p.sb_stride + 15) / 16 * 16;
   p.sdx = p.sgsum + T * g * 4;
   p.red = (p.sdx + T * b * 4 + 15) / 16 * 16;
-  p.total = p.red + (int64_t)2 * MmaCfg<T, TPW>::kWarps * 8 * 32 * 4;
+  p.total = p.red + (int64_t)2 * MmaCfg<T, TPW>::kWarps * MmaCfg<T, TPW>::kReducers * 32 * 4;
   return p;
 }
 
@@ -525,16 +534,28 @@ __device__ __forceinline__ void load_mma_codes(const uint8_t* tile, int lane, Mm
 }
 
 // One 32-row tile and group on the tensor cores: adds d_w d_x isum into y
-// (y[4h + 2r + j]: half h, row g8 + 8r, token 2q + j) or stores isum.
+// (y[8nb + 4h + 2r + j]: token block nb, half h, row g8 + 8r, token
+// 8nb + 2q + j) or stores isum.
 template <int T, bool kGroupSums>
 __device__ __forceinline__ void group_mma(const MmaCodes& m, int g, const uint8_t* sb,
                                           int64_t sb_stride, const int* sgsum, const float* sdx,
-                                          const GemvArgs& a, int row_base, int lane, float (&y)[8]) {
+                                          const GemvArgs& a, int row_base, int lane,
+                                          float (&y)[8 * ((T + 7) / 8)]) {
+  constexpr int NB = (T + 7) / 8;
+  constexpr bool kI8 = T > 8;
   const int g8 = lane >> 2, q = lane & 3;
-  // B: token g8's activations of this group, rows of f16 in natural k order
-  const bool tok_ok = g8 < T;
-  const uint8_t* brow = sb + (tok_ok ? g8 : 0) * sb_stride + (int64_t)g * kGroup * 2 + q * 32;
-  float c[2][4] = {};
+  // B: token 8nb + g8's activations of this group, as f16 rows in natural k
+  // order (up to 8 tokens) or int8 (more)
+  const uint8_t* brow[NB];
+  bool tok_ok[NB];
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb) {
+    const int tok = 8 * nb + g8;
+    tok_ok[nb] = tok < T;
+    brow[nb] = sb + (tok_ok[nb] ? tok : 0) * sb_stride +
+               (kI8 ? (int64_t)g * kGroup + q * 16 : (int64_t)g * kGroup * 2 + q * 32);
+  }
+  float c[NB][2][4] = {};
 #pragma unroll
   for (int ch = 0; ch < 2; ++ch) {   // 64-weight half of the group (code half)
     uint32_t x01[2][2], x23[2][2];   // [tile half][row g8 / g8 + 8]
@@ -547,47 +568,67 @@ __device__ __forceinline__ void group_mma(const MmaCodes& m, int g, const uint8_
       }
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
-      uint2 bv = make_uint2(0u, 0u);
-      if (tok_ok) bv = *reinterpret_cast<const uint2*>(brow + ch * 128 + s * 8);
       const uint32_t mk = 0x00030003u << (2 * s);
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
-        mma16816(c[h], x01[h][0] & mk, x01[h][1] & mk, x23[h][0] & mk, x23[h][1] & mk, bv.x, bv.y);
-    }
-  }
-  // tokens 2q, 2q + 1 of this lane
-  const int t0 = 2 * q;
-  int sq[2];
-  float dx[2];
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const bool ok = t0 + j < T;
-    sq[j] = ok ? sgsum[(t0 + j) * a.ngroups + g] : 0;
-    dx[j] = ok ? sdx[(t0 + j) * a.nblk + (g >> 1)] : 0.0f;
-  }
-#pragma unroll
-  for (int h = 0; h < 2; ++h)
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int row = row_base + 16 * h + g8 + 8 * r;
-      const float dw = kGroupSums ? 0.0f : __half2float(__ushort_as_half((unsigned short)m.sc[h][r]));
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const float isum = fmaf(c[h][2 * r + j], 32768.0f, (float)(-sq[j]));   // exact
-        if (kGroupSums) {
-          if (t0 + j < T && row < a.rows)
-            a.S[((int64_t)(t0 + j) * a.rows + row) * a.ngroups + g] = __float2int_rn(isum);
-        } else {
-          y[4 * h + 2 * r + j] = fmaf(dw * dx[j], isum, y[4 * h + 2 * r + j]);
+      for (int nb = 0; nb < NB; ++nb) {
+        uint2 bv = make_uint2(0u, 0u);
+        if (tok_ok[nb]) {
+          if (kI8) {
+            // four int8 activations -> two exact f16 pairs, times 2^(9 - 2s)
+            uint32_t lo, hi;
+            tc::s8x4_to_h2x2(*reinterpret_cast<const uint32_t*>(brow[nb] + ch * 64 + s * 4), lo, hi);
+            const uint32_t sc = mma_slot_scale(s);
+            bv = make_uint2(h2_mul_rn(lo, sc), h2_mul_rn(hi, sc));
+          } else {
+            bv = *reinterpret_cast<const uint2*>(brow[nb] + ch * 128 + s * 8);
+          }
         }
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          mma16816(c[nb][h], x01[h][0] & mk, x01[h][1] & mk, x23[h][0] & mk, x23[h][1] & mk, bv.x,
+                   bv.y);
       }
     }
+  }
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb) {
+    // tokens 8nb + 2q, 8nb + 2q + 1 of this lane
+    const int t0 = 8 * nb + 2 * q;
+    int sq[2];
+    float dx[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const bool ok = t0 + j < T;
+      sq[j] = ok ? sgsum[(t0 + j) * a.ngroups + g] : 0;
+      dx[j] = ok ? sdx[(t0 + j) * a.nblk + (g >> 1)] : 0.0f;
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int row = row_base + 16 * h + g8 + 8 * r;
+        const float dw =
+            kGroupSums ? 0.0f : __half2float(__ushort_as_half((unsigned short)m.sc[h][r]));
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float isum = fmaf(c[nb][h][2 * r + j], 32768.0f, (float)(-sq[j]));   // exact
+          if (kGroupSums) {
+            if (t0 + j < T && row < a.rows)
+              a.S[((int64_t)(t0 + j) * a.rows + row) * a.ngroups + g] = __float2int_rn(isum);
+          } else {
+            float& yy = y[8 * nb + 4 * h + 2 * r + j];
+            yy = fmaf(dw * dx[j], isum, yy);
+          }
+        }
+      }
+  }
 }
 
 template <int T, bool kGroupSums, int TPW>
 __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(const GemvArgs a) {
   using Mc = MmaCfg<T, TPW>;
   constexpr int kConsumers = Mc::kWarps;
+  constexpr int kReducers = Mc::kReducers;
   constexpr int kStageTiles = Mc::kStageTiles;
   constexpr int kStageBytes = Mc::kStageBytes;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -640,7 +681,7 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
     }
     for (int i = 0; i < 2; ++i) {
       mbarrier_init(smem_u32(redfull + i), kConsumers);
-      mbarrier_init(smem_u32(redempty + i), kMmaReducers);
+      mbarrier_init(smem_u32(redempty + i), kReducers);
     }
     mbarrier_init_fence();
     if (a.early_weights) issue_first();
@@ -651,11 +692,18 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
   }
   if (threadIdx.x == 0 && !a.early_weights) issue_first();
 
-  // Stage the activations: f16 q * 2^(9 - 2s) per token row, the sum of each
-  // 128-value half-block (8 partial sums), and the block scales. Lane l takes
-  // values 8l .. 8l + 7 of a block (slots 2(l & 1) and 2(l & 1) + 1).
+  // Stage the activations: f16 q * 2^(9 - 2s) (up to 8 tokens) or the int8 q
+  // (more) per token row, the sum of each 128-value half-block (8 partial
+  // sums), and the block scales. Lane l takes values 8l .. 8l + 7 of a block
+  // (slots 2(l & 1) and 2(l & 1) + 1).
   auto put_f16 = [&](int tb, uint32_t v0, uint32_t v1) {
     const int t = tb / a.nblk, b = tb - t * a.nblk;
+    if (Mc::kI8) {
+      uint32_t* dst = reinterpret_cast<uint32_t*>(sb + t * pl.sb_stride + (int64_t)b * kQK + 8 * lane);
+      dst[0] = v0;
+      dst[1] = v1;
+      return;
+    }
     uint32_t h[4];
     tc::s8x4_to_h2x2(v0, h[0], h[1]);
     tc::s8x4_to_h2x2(v1, h[2], h[3]);
@@ -698,6 +746,14 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
       const float inv1 = (lane & 1) ? 0.125f : 0.0078125f;       // 2^-3 : 2^-7
       for (int tb = blockIdx.x + warp * gridDim.x; tb < T * a.nblk; tb += gridDim.x * kConsumers) {
         const int t = tb / a.nblk, b = tb - t * a.nblk;
+        if (Mc::kI8) {   // the int8 values as staged
+          const uint32_t* src =
+              reinterpret_cast<const uint32_t*>(sb + t * pl.sb_stride + (int64_t)b * kQK + 8 * lane);
+          const uint32_t w0 = src[0], w1 = src[1];
+          const int s8 = __dp4a((int)w0, 0x01010101, 0) + __dp4a((int)w1, 0x01010101, 0);
+          q8K_store(a.Xq_out + (int64_t)tb * kQ8KBytes, lane, w0, w1, s8, sdx[tb]);
+          continue;
+        }
         const uint2* src =
             reinterpret_cast<const uint2*>(sb + t * pl.sb_stride + ((int64_t)b * kQK + 8 * lane) * 2);
         int q[8];
@@ -727,9 +783,9 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
   uint32_t phase = 0;
   for (int rb = rb0, i = 0; rb < rb1; ++rb, ++i) {
     const int row_base = rb * kTileRows;
-    float y[8];
+    float y[kReducers];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) y[e] = 0.0f;
+    for (int e = 0; e < kReducers; ++e) y[e] = 0.0f;
     for (int st = 0; st < per_rb; ++st, ++j) {
       const int gs = st * kStageTiles;
       const int nt = min(kStageTiles, a.ngroups - gs);
@@ -767,27 +823,29 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
     if (!waited) finish_wait();
     if (!kGroupSums) {
       // The warps' partial sums of this tile column meet in shared memory;
-      // warp (i*8 + e) % 16 adds C position e over the warps in warp order.
+      // warp (i*R + e) % warps adds C position e (of R = 8 per token block)
+      // over the warps in warp order.
       const int p = i & 1;
-      float* r = red + p * (kConsumers * 8 * 32);
+      float* r = red + p * (kConsumers * kReducers * 32);
       if (i >= 2 && !failed &&
           !mbarrier_wait_bounded(smem_u32(redempty + p), (uint32_t)(((i >> 1) - 1) & 1),
                                  lim))
         failed = true;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) r[(warp * 8 + e) * 32 + lane] = y[e];
+      for (int e = 0; e < kReducers; ++e) r[(warp * kReducers + e) * 32 + lane] = y[e];
       __syncwarp();
       if (lane == 0) mbarrier_arrive(smem_u32(redfull + p));
-      const int e = (warp - i * kMmaReducers) & (kConsumers - 1);
-      if (e < kMmaReducers) {
+      const int e = (warp - i * kReducers) & (kConsumers - 1);
+      if (e < kReducers) {
         if (!failed && !mbarrier_wait_bounded(smem_u32(redfull + p), (uint32_t)((i >> 1) & 1),
                                               lim))
           failed = true;
         float sum = 0.0f;
 #pragma unroll
-        for (int k = 0; k < kConsumers; ++k) sum += r[(k * 8 + e) * 32 + lane];
-        const int row = row_base + 16 * (e >> 2) + (lane >> 2) + 8 * ((e >> 1) & 1);
-        const int t = 2 * (lane & 3) + (e & 1);
+        for (int k = 0; k < kConsumers; ++k) sum += r[(k * kReducers + e) * 32 + lane];
+        // e = 8nb + 4h + 2r + j: token block nb, half h, row g8 + 8r, token 2q + j
+        const int row = row_base + 16 * ((e >> 2) & 1) + (lane >> 2) + 8 * ((e >> 1) & 1);
+        const int t = 8 * (e >> 3) + 2 * (lane & 3) + (e & 1);
         if (!failed && t < T && row < a.rows) a.Y[(int64_t)t * a.rows + row] = sum;
         __syncwarp();
         if (lane == 0) mbarrier_arrive(smem_u32(redempty + p));
@@ -861,7 +919,7 @@ cudaError_t launch_mma(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
 
 template <int T, bool G>
 cudaError_t launch_t(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
-  static_assert(T >= 1 && T <= kMaxTok, "token count");
+  static_assert(T >= 1 && T <= kMaxDp4aTok, "token count");
   auto kernel = gemv_kernel<T, G>;
   GemvArgs a = a0;
   DeviceLimits lim;
@@ -930,7 +988,10 @@ cudaError_t launch_mma_tpw(int tpw, const GemvArgs& a, int64_t cols, cudaStream_
 template <int T>
 cudaError_t launch_tok(const GemvArgs& a, int64_t cols, bool gsum, cudaStream_t s) {
   if constexpr (T >= TQ_GEMV_MMA_MIN_TOK) {
-    const int tpw = mma_tiles_per_warp(a.ngroups);
+    // above 8 tokens the int8 activations and the wider reduction leave room
+    // for two tiles per warp and stage at most
+    const int tpw = T > kMaxDp4aTok ? min(2, mma_tiles_per_warp(a.ngroups))
+                                    : mma_tiles_per_warp(a.ngroups);
     cudaError_t e = gsum ? launch_mma_tpw<T, true>(tpw, a, cols, s)
                          : launch_mma_tpw<T, false>(tpw, a, cols, s);
     // the ring and the f16 activations did not fit in shared memory: one
@@ -939,7 +1000,10 @@ cudaError_t launch_tok(const GemvArgs& a, int64_t cols, bool gsum, cudaStream_t 
       e = gsum ? launch_mma<T, true, 1>(a, cols, s) : launch_mma<T, false, 1>(a, cols, s);
     if (e != cudaErrorNotSupported) return e;
   }
-  return gsum ? launch_t<T, true>(a, cols, s) : launch_t<T, false>(a, cols, s);
+  if constexpr (T <= kMaxDp4aTok)
+    return gsum ? launch_t<T, true>(a, cols, s) : launch_t<T, false>(a, cols, s);
+  else
+    return cudaErrorNotSupported;
 }
 
 }  // namespace
@@ -980,11 +1044,19 @@ cudaError_t launch_gemv(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t
     case 5: e = launch_tok<5>(a, cols, gsum, s); break;
     case 6: e = launch_tok<6>(a, cols, gsum, s); break;
     case 7: e = launch_tok<7>(a, cols, gsum, s); break;
-    default: e = launch_tok<8>(a, cols, gsum, s); break;
+    case 8: e = launch_tok<8>(a, cols, gsum, s); break;
+    case 9: e = launch_tok<9>(a, cols, gsum, s); break;
+    case 10: e = launch_tok<10>(a, cols, gsum, s); break;
+    case 11: e = launch_tok<11>(a, cols, gsum, s); break;
+    case 12: e = launch_tok<12>(a, cols, gsum, s); break;
+    case 13: e = launch_tok<13>(a, cols, gsum, s); break;
+    case 14: e = launch_tok<14>(a, cols, gsum, s); break;
+    case 15: e = launch_tok<15>(a, cols, gsum, s); break;
+    default: e = launch_tok<16>(a, cols, gsum, s); break;
   }
   if (e != cudaErrorNotSupported || ntok == 1) return e;
   // The activations of all tokens do not fit in shared memory (long rows:
-  // 8 tokens of 17408 columns): one launch per half of the tokens, each
+  // 8 tokens of 17408 columns, 16 of 8192): one launch per half of the tokens, each
   // streaming the weights once, instead of the tensor-core path for a tile
   // of 64 tokens. Every token's inputs and outputs are contiguous rows, and
   // each half's arithmetic is that of a call with those tokens alone. The

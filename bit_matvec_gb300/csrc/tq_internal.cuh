@@ -243,7 +243,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-// GEMV for 1..8 tokens. Returns cudaErrorNotSupported (without launching)
+// GEMV for 1..16 tokens. Returns cudaErrorNotSupported (without launching)
 // when the activations of all tokens do not fit in shared memory.
 // early_weights: the kernel enqueued just before on the stream does not write
 // Wtq, so weight reads may start before waiting for it.
@@ -260,6 +260,9 @@ cudaError_t launch_gemv(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t
                         bool inputs_final, cudaStream_t s, const float* X = nullptr,
                         uint8_t* Xq_out = nullptr);
 int gemv_max_tokens();
+// Token counts up to which the workspace forms also run the GEMV (beyond, the
+// tensor cores, which need the workspace).
+int ws_gemv_max_tokens();
 
 // Tensor-core path for any ntok >= 1 (used for ntok > gemv_max_tokens()).
 cudaError_t launch_gemm_tc(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t* S,

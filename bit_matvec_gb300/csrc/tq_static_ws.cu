@@ -54,12 +54,12 @@ cudaError_t static_ws_ptr(void** out) {
 extern "C" int tq_matmul_static_ws(const void* Wtq, const void* Xq, float* Y, int64_t rows,
                                    int64_t cols, int64_t ntok, void* stream) {
   if (rows < 0 || cols < 0 || ntok < 0 || cols % TQ_QK_K != 0) return TQ_ERR_SHAPE;
-  // Beyond these, the tensor-core path's workspace (at least 16 KB per 64
-  // tokens and per 128 columns) exceeds the array; rejecting them first also
-  // keeps the size product below from overflowing.
-  constexpr int64_t kMaxFactor = TQ_STATIC_WS_BYTES / 16384;
-  if (ntok > tq::gemv_max_tokens() && cols > 0 &&
-      (cols / TQ_GROUP > kMaxFactor || (ntok + 63) / 64 > kMaxFactor))
+  // Beyond these, the tensor-core path's workspace (at least 4 KB per 128
+  // columns, and 16 KB per 64 tokens and 128 columns) exceeds the array;
+  // rejecting them first also keeps the size product below from overflowing.
+  constexpr int64_t kMaxFactor = TQ_STATIC_WS_BYTES / 4096;
+  if (ntok > tq::ws_gemv_max_tokens() && cols > 0 &&
+      (cols / TQ_GROUP > kMaxFactor || ntok / 64 > kMaxFactor))
     return TQ_ERR_WORKSPACE;
   const int64_t need = tq_matmul_workspace_bytes(rows, cols, ntok);
   if (need < 0) return TQ_ERR_SHAPE;

@@ -146,6 +146,12 @@ def test_workspace_bytes(lib):
     # none for the GEMV route; B tiles + block scales per 64-token tile otherwise
     assert lib.tq_matmul_workspace_bytes(32768, 8192, 1) == 0
     assert lib.tq_matmul_workspace_bytes(17408, 5120, 8) == 0
+    # token tiles of 16, 32 and 64: per group 2 x 16 x 128 bytes of B (and per
+    # block 3 x 16 floats of scales and sums), 2 x 32 x 128, 2 x 64 x 128
+    assert lib.tq_matmul_workspace_bytes(17408, 5120, 9) == 40 * 4096 + 20 * 192
+    assert lib.tq_matmul_workspace_bytes(17408, 5120, 16) == 40 * 4096 + 20 * 192
+    assert lib.tq_matmul_workspace_bytes(17408, 5120, 17) == 40 * 8192 + 20 * 384
+    assert lib.tq_matmul_workspace_bytes(17408, 5120, 33) == 40 * 16384 + 20 * 768
     assert lib.tq_matmul_workspace_bytes(17408, 5120, 64) == 40 * 16384 + 20 * 768
     assert lib.tq_matmul_workspace_bytes(100, 512, 65) == 2 * (4 * 16384 + 2 * 768)
     assert lib.tq_matmul_workspace_bytes(0, 512, 65) == 0
@@ -156,17 +162,17 @@ def test_workspace_bytes(lib):
 def test_workspace_errors(lib):
     import bit_matvec_gb300 as tq
     D = 0x7F3000000000
-    need = lib.tq_matmul_workspace_bytes(64, 512, 16)
+    need = lib.tq_matmul_workspace_bytes(64, 512, 32)
     ws = lib.tq_matmul_ws
-    assert ws(P(A), P(B), P(C), 64, 512, 16, None, need, None) == tq.TQ_ERR_NULL
-    assert ws(P(A), P(B), P(C), 64, 512, 16, P(D + 8), need, None) == tq.TQ_ERR_ALIGN
-    assert ws(P(A), P(B), P(C), 64, 512, 16, P(D), need - 16, None) == tq.TQ_ERR_WORKSPACE
-    assert ws(P(A), P(B), P(C), 64, 512, 16, P(C + 64), need, None) == tq.TQ_ERR_ALIAS
-    assert ws(P(A), P(B), P(C), 64, 512, 16, P(B), need, None) == tq.TQ_ERR_ALIAS
-    assert ws(P(A), P(B), P(C), 64, 300, 16, P(D), need, None) == tq.TQ_ERR_SHAPE
+    assert ws(P(A), P(B), P(C), 64, 512, 32, None, need, None) == tq.TQ_ERR_NULL
+    assert ws(P(A), P(B), P(C), 64, 512, 32, P(D + 8), need, None) == tq.TQ_ERR_ALIGN
+    assert ws(P(A), P(B), P(C), 64, 512, 32, P(D), need - 16, None) == tq.TQ_ERR_WORKSPACE
+    assert ws(P(A), P(B), P(C), 64, 512, 32, P(C + 64), need, None) == tq.TQ_ERR_ALIAS
+    assert ws(P(A), P(B), P(C), 64, 512, 32, P(B), need, None) == tq.TQ_ERR_ALIAS
+    assert ws(P(A), P(B), P(C), 64, 300, 32, P(D), need, None) == tq.TQ_ERR_SHAPE
     assert ws(None, None, None, 64, 512, 0, None, 0, None) == tq.TQ_OK
     gs = lib.tq_matmul_groupsums_ws
-    assert gs(P(A), P(B), P(C), 64, 512, 16, P(D), need - 1, None) == tq.TQ_ERR_WORKSPACE
+    assert gs(P(A), P(B), P(C), 64, 512, 32, P(D), need - 1, None) == tq.TQ_ERR_WORKSPACE
 
 
 def test_matmul_host_errors_before_any_work(lib):
@@ -175,10 +181,10 @@ def test_matmul_host_errors_before_any_work(lib):
     import bit_matvec_gb300 as tq
     H, X, D = 0x10000000, 0x7F4000000000, 0x7F3000000000
     f = lib.tq_matmul_host
-    need = lib.tq_matmul_workspace_bytes(64, 512, 16)
+    need = lib.tq_matmul_workspace_bytes(64, 512, 32)
     args = lambda **k: [P(k.get("w", A)), P(k.get("xh", H)), P(k.get("x", X)), P(k.get("xq", B)),
                         P(k.get("y", C)), P(k.get("yh", H + (1 << 20))), k.get("rows", 64),
-                        k.get("cols", 512), k.get("ntok", 16), P(k.get("ws", D)),
+                        k.get("cols", 512), k.get("ntok", 32), P(k.get("ws", D)),
                         k.get("wsb", need), None]
     assert f(*args(cols=300)) == tq.TQ_ERR_SHAPE
     assert f(*args(rows=-1)) == tq.TQ_ERR_SHAPE
@@ -202,9 +208,9 @@ def test_quantize_matmul_errors_before_any_work(lib):
     import bit_matvec_gb300 as tq
     X, D = 0x7F4000000000, 0x7F3000000000
     f = lib.tq_quantize_matmul
-    need = lib.tq_matmul_workspace_bytes(64, 512, 16)
+    need = lib.tq_matmul_workspace_bytes(64, 512, 32)
     args = lambda **k: [P(k.get("w", A)), P(k.get("x", X)), P(k.get("xq", B)), P(k.get("y", C)),
-                        k.get("rows", 64), k.get("cols", 512), k.get("ntok", 16),
+                        k.get("rows", 64), k.get("cols", 512), k.get("ntok", 32),
                         P(k.get("ws", D)), k.get("wsb", need), None]
     assert f(*args(cols=300)) == tq.TQ_ERR_SHAPE
     assert f(*args(ntok=-1)) == tq.TQ_ERR_SHAPE

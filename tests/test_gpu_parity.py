@@ -2,8 +2,10 @@
 
 Bit-exact: q8_K bytes (scales, int8 values, partial sums), repacked bytes,
 and every int32 group sum. Within 1e-5 of sum_g |d_w d_x isum| per output:
-the f32 results. Sizes span several tiles with ragged tails; the GEMV path
-is ntok <= 8, the tensor-core path ntok >= 9.
+the f32 results. Sizes span several tiles with ragged tails. tq_matmul runs
+the GEMV up to 16 tokens (int8 activations in shared memory above 8) and the
+tensor cores above; the workspace forms run the GEMV up to 8 tokens and the
+tensor cores above (token tiles of 16, 32 and 64).
 """
 import numpy as np
 import pytest
@@ -88,8 +90,9 @@ def test_repack_bit_exact_and_roundtrip(rows, cols):
 # ---------------------------------------------------------------- group sums and matmul
 
 SHAPES = [(32, 256), (100, 512), (300, 768), (128, 1024)]
-GEMV_TOKENS = [1, 2, 3, 4, 5, 7, 8]          # one weight pass for all tokens
-TC_TOKENS = [9, 15, 16, 17, 63, 64, 65, 130]  # tensor cores, token tile zero-padded
+GEMV_TOKENS = [1, 2, 3, 4, 5, 7, 8, 9, 12, 15, 16]   # one weight pass for all tokens
+TC_TOKENS = [17, 31, 33, 63, 64, 65, 130]           # tensor cores, token tile zero-padded
+TC_WS_TOKENS = [9, 12, 16, 17, 31, 32, 33, 63, 64, 65, 130]   # tiles of 16, 32, 64
 
 
 def _check_product(rows, cols, ntok, ws=False):
@@ -113,14 +116,19 @@ def test_gemv_groupsums_exact_matmul_close(rows, cols, ntok):
 
 @pytest.mark.parametrize("rows,cols,ntok", [(64, 8192, 4), (64, 8192, 8), (96, 16384, 6),
                                              (64, 5120, 5), (100, 5120, 8), (40, 6144, 4),
-                                             (64, 17408, 8), (40, 32768, 5), (33, 65536, 3)])
+                                             (64, 17408, 8), (40, 32768, 5), (33, 65536, 3),
+                                             (64, 5120, 16), (40, 3072, 11), (64, 8192, 12),
+                                             (64, 8192, 16), (64, 17408, 16)])
 def test_gemv_wide_rows(rows, cols, ntok):
     """Long rows: from 4 tokens the tensor-core (mma.sync) variant runs while its
     f16 activations fit in shared memory (8 x 8192 do not: the dp4a loop takes
     over); 16384 columns at 6 tokens exercise the largest staged activations;
     5120 and 6144 columns (40 and 48 groups) take three tiles per warp and
     stage, the others two. Where no variant fits all tokens (8 x 17408,
-    5 x 32768, 3 x 65536) the GEMV runs once per half of the tokens."""
+    5 x 32768, 3 x 65536) the GEMV runs once per half of the tokens. 9 to 16
+    tokens keep int8 activations in shared memory and take two 8-column MMAs
+    per weight fragment (16 x 5120 with two tiles per warp and stage, 12 x 8192
+    with one); 16 x 8192 and 16 x 17408 do not fit and split in halves."""
     _check_product(rows, cols, ntok)
 
 
@@ -131,13 +139,14 @@ def test_tc_groupsums_exact_matmul_close(rows, cols, ntok):
 
 
 @pytest.mark.parametrize("rows,cols", SHAPES)
-@pytest.mark.parametrize("ntok", TC_TOKENS)
+@pytest.mark.parametrize("ntok", TC_WS_TOKENS)
 def test_tc_ws_groupsums_exact_matmul_close(rows, cols, ntok):
     """The workspace form: activations packed once by a pre-pass."""
     _check_product(rows, cols, ntok, ws=True)
 
 
-@pytest.mark.parametrize("ntok", [1, 4, 8, 9, 16, 64, 65], ids=lambda t: f"{'tc' if t > 8 else 'gemv'}{t}")
+@pytest.mark.parametrize("ntok", [1, 4, 8, 9, 16, 17, 64, 65],
+                         ids=lambda t: f"{'tc' if t > 16 else 'gemv'}{t}")
 def test_exact_integer_mode(ntok):
     """d_w = 1 and d_x = 1 (integer activations with absmax 127 in every block):
     the output is the exact integer product, on both paths."""
@@ -155,7 +164,7 @@ def test_exact_integer_mode(ntok):
         assert np.array_equal(y, (x.astype(np.int64) @ w.T).astype(np.float32))
 
 
-@pytest.mark.parametrize("ntok", [1, 8, 64], ids=lambda t: f"{'tc' if t > 8 else 'gemv'}{t}")
+@pytest.mark.parametrize("ntok", [1, 8, 16, 64], ids=lambda t: f"{'tc' if t > 16 else 'gemv'}{t}")
 def test_extremes(ntok):
     """All u = 2 (w = +1) or all u = 0 against q = +-127: the largest group sums,
     and activation sums of -16256, 0 and +16256 (the e4m3 path splits each q
@@ -243,11 +252,11 @@ def test_concurrent_streams():
 
 @pytest.mark.parametrize("rows,cols,ntok", [(300, 1024, 1), (100, 768, 3), (300, 1024, 4),
                                              (64, 8192, 8), (32, 256, 8), (64, 17408, 8),
-                                             (128, 1024, 9),
+                                             (128, 1024, 9), (128, 1024, 16), (64, 17408, 16),
                                              (100, 512, 64), (300, 1024, 65), (160, 2048, 130)])
 def test_quantize_matmul_equals_separate_calls(rows, cols, ntok):
     """The fused call gives the bits of tq_quantize_q8K + tq_matmul_ws: Xq and Y
-    (GEMV with in-CTA quantization for ntok <= 8; above, one kernel that
+    (GEMV with in-CTA quantization for ntok <= 16; above, one kernel that
     quantizes and packs the workspace, including the zero padding of a
     ragged last token tile, before the tensor-core kernel)."""
     import bit_matvec_gb300 as tq

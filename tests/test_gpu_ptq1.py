@@ -49,7 +49,7 @@ def test_repack_ptq1_bit_exact(rows, cols):
     assert np.array_equal(got, oracle.repack(oracle.ptq1_0_to_pq2_0(wpt, rows, cols), rows, cols))
 
 
-@pytest.mark.parametrize("ntok", [1, 4, 64], ids=lambda t: f"{'tc' if t > 8 else 'gemv'}{t}")
+@pytest.mark.parametrize("ntok", [1, 4, 64], ids=lambda t: f"{'tc' if t > 16 else 'gemv'}{t}")
 def test_matmul_through_ptq1(ntok):
     rows, cols = 300, 1024
     wpt, _ = _weights(rows, cols, 12)

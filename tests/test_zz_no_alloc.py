@@ -39,7 +39,7 @@ def test_oversize_rejected_before_any_cuda_work(tq):
     lib = tq.library()
     assert tq.tq_matmul_workspace_bytes(64, 5120, 768) <= tq.STATIC_WS_BYTES
     assert tq.tq_matmul_workspace_bytes(64, 5120, 769) > tq.STATIC_WS_BYTES
-    for rows, cols, ntok in [(64, 5120, 769), (1, 256 * 1024, 9), (1, 256, 1 << 40),
+    for rows, cols, ntok in [(64, 5120, 769), (1, 256 * 1024, 17), (1, 256, 1 << 40),
                              (1, 1 << 40, 1 << 40)]:
         assert lib.tq_matmul_static_ws(None, None, None, rows, cols, ntok, None) == \
             tq.TQ_ERR_WORKSPACE
