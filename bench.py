@@ -390,6 +390,71 @@ def measure_read_ceiling(nbytes, device, warmup):
     return res
 
 
+def measure_ptq1_stream(steps, warmup, world, device, peaks, peak_kind, ref_kernel_ms):
+    """The decode workload's weights as the 1.75-bit ptq1_0 file, streamed and
+    decoded by the GEMV itself (tq_matmul_ptq1_0_stream, one token), timed like
+    the headline's matmul launches: back-to-back launches in graphs, weights
+    rotating over copies larger than twice the L2."""
+    import torch
+    import bit_matvec_gb300 as tq
+    cfg = synth.CONFIGS["decode"]
+    rows, cols = cfg["rows"], cfg["cols"]
+    s = synth.seeds(cfg["index"])
+    wpt = synth.pack_ptq1_0(synth.ternary_codes(rows, cols, s["weights"]),
+                            synth.group_scales(rows, cols, s["scales"]))
+    W = torch.from_numpy(wpt).to(device)
+    del wpt
+    wt1 = torch.empty(tq.tq_ptq1_0_stream_bytes(rows, cols), dtype=torch.uint8, device=device)
+    tq.tq_repack_ptq1_0_stream(W, wt1, rows, cols)
+    del W
+    copies = max(2, -(-2 * L2_BYTES // wt1.numel()) + 1)
+    Ws = [wt1] + [wt1.clone() for _ in range(copies - 1)]
+    X = torch.from_numpy(synth.activations(1, cols, s["acts"])).to(device)
+    Xq = tq.q8K_empty(1, cols, device)
+    tq.tq_quantize_q8K(X, Xq, 1, cols)
+    Y = torch.empty((1, rows), dtype=torch.float32, device=device)
+    stream = torch.cuda.Stream(device=device)
+    stream.wait_stream(torch.cuda.current_stream(device))
+    G = copies * max(1, STEPS_PER_GRAPH // copies)
+    reps = max(1, steps // G)
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, 3)):
+            tq.tq_matmul_ptq1_0_stream(Ws[i % copies], Xq, Y, rows, cols, 1, stream)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(G):
+                tq.tq_matmul_ptq1_0_stream(Ws[i % copies], Xq, Y, rows, cols, 1, stream)
+        for _ in range(3):
+            g.replay()
+        stream.synchronize()
+        barrier(world)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        stream.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b) / (reps * G), world, device)
+    wbytes = wt1.numel()
+    abytes = wbytes + cols // 256 * 292 + rows * 4
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    res = {"workload": "decode GEMV 32768x8192 as the 1.75-bit ptq1_0 file, streamed and decoded "
+                       "in the kernel, ntok=1",
+           "ms_per_launch": ms, "launches": reps * G,
+           "gweights_per_s": world * rows * cols / (ms * 1e-3) / 1e9,
+           "weight_bytes": wbytes, "weight_gbs": wbytes / (ms * 1e-3) / 1e9,
+           "roofline": {"bound": "hbm", "achieved": abytes / (ms * 1e-3) / 1e9, "peak": peak,
+                        "unit": "GB/s", "frac": abytes / (ms * 1e-3) / 1e9 / peak,
+                        "peak_source": peak_kind},
+           "time_vs_2bit_stream": ms / ref_kernel_ms if ref_kernel_ms else None,
+           "timing": f"graphs of {G} back-to-back launches, CUDA events"}
+    del Ws
+    torch.cuda.empty_cache()
+    return res
+
+
 # Steps per captured graph (a multiple of the weight copies): a decode graph
 # holds many matmuls back to back, and consecutive kernels overlap only within
 # one graph launch.
@@ -865,6 +930,10 @@ def main():
             if want_cpu:
                 r["cpu_baseline"] = cpu_baseline_entry(*oracle_replay_rate(ntok, 5.0))
             extra[f"replay_ntok{ntok}"] = r
+    if args.workload == "decode" and not args.no_extra:
+        extra["ptq1_stream"] = measure_ptq1_stream(max(40, args.steps // 10), args.warmup, world,
+                                                   device, peaks, peak_kind,
+                                                   main_res["roofline"]["kernel_ms"])
     if wl.ntok <= GEMV_MAX_TOKENS and not args.no_read_ceiling:
         main_res["roofline"]["read_ceiling"] = measure_read_ceiling(
             main_res["roofline"]["algorithmic_bytes"] // 16 * 16, device, args.warmup)

@@ -93,6 +93,10 @@ def _load():
             "tq_version": ([], ctypes.c_char_p),
             "tq_debug_stall_next_launch": ([I64], I),
             "tq_probe_read_sum": ([P, I64, P, I, P], I),
+            "tq_ptq1_0_stream_bytes": ([I64, I64], I64),
+            "tq_repack_ptq1_0_stream": ([P, P, I64, I64, P], I),
+            "tq_matmul_ptq1_0_stream": ([P, P, P, I64, I64, I64, P], I),
+            "tq_matmul_ptq1_0_stream_groupsums": ([P, P, P, I64, I64, I64, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -183,6 +187,32 @@ def tq_repack_ptq1_0(Wpt: torch.Tensor, Wtq: torch.Tensor, rows: int, cols: int,
     """ptq1_0 (1.75-bit) weights -> the tq layout, decoded once at load."""
     _call("tq_repack_ptq1_0", Wpt.device, _ptr(Wpt), _ptr(Wtq), rows, cols,
           _stream(stream, Wpt.device))
+
+
+def tq_ptq1_0_stream_bytes(rows: int, cols: int) -> int:
+    n = _load().tq_ptq1_0_stream_bytes(rows, cols)
+    if n < 0:
+        raise TQError(TQ_ERR_SHAPE, "tq_ptq1_0_stream_bytes")
+    return int(n)
+
+
+def tq_repack_ptq1_0_stream(Wpt: torch.Tensor, Wt1: torch.Tensor, rows: int, cols: int,
+                            stream=None):
+    """ptq1_0 (1.75-bit) weights -> 32-row stream tiles, not decoded."""
+    _call("tq_repack_ptq1_0_stream", Wpt.device, _ptr(Wpt), _ptr(Wt1), rows, cols,
+          _stream(stream, Wpt.device))
+
+
+def tq_matmul_ptq1_0_stream(Wt1: torch.Tensor, Xq: torch.Tensor, Y: torch.Tensor, rows: int,
+                            cols: int, ntok: int, stream=None):
+    _call("tq_matmul_ptq1_0_stream", Wt1.device, _ptr(Wt1), _ptr(Xq), _ptr(Y), rows, cols, ntok,
+          _stream(stream, Wt1.device))
+
+
+def tq_matmul_ptq1_0_stream_groupsums(Wt1: torch.Tensor, Xq: torch.Tensor, S: torch.Tensor,
+                                      rows: int, cols: int, ntok: int, stream=None):
+    _call("tq_matmul_ptq1_0_stream_groupsums", Wt1.device, _ptr(Wt1), _ptr(Xq), _ptr(S), rows,
+          cols, ntok, _stream(stream, Wt1.device))
 
 
 def tq_matmul(Wtq: torch.Tensor, Xq: torch.Tensor, Y: torch.Tensor, rows: int, cols: int,

@@ -367,6 +367,26 @@ int tq_repack_ptq1_0(const void* Wpt, void* Wtq, int64_t rows, int64_t cols, voi
   return e == cudaSuccess ? TQ_OK : fail_cuda(e);
 }
 
+int64_t tq_ptq1_0_stream_bytes(int64_t rows, int64_t cols) {
+  if (rows < 0 || cols < 0 || cols % kGroup != 0) return -1;
+  return (rows + kTileRows - 1) / kTileRows * (cols / kGroup) * kTq1TileBytes;
+}
+
+int tq_repack_ptq1_0_stream(const void* Wpt, void* Wt1, int64_t rows, int64_t cols,
+                            void* stream) {
+  if (rows < 0 || cols < 0 || cols % kGroup != 0) return TQ_ERR_SHAPE;
+  if (rows == 0 || cols == 0) return TQ_OK;
+  if (!Wpt || !Wt1) return TQ_ERR_NULL;
+  if (!aligned16(Wpt) || !aligned16(Wt1)) return TQ_ERR_ALIGN;
+  if (overlap(Wpt, tq_ptq1_0_bytes(rows, cols), Wt1, tq_ptq1_0_stream_bytes(rows, cols)))
+    return TQ_ERR_ALIAS;
+  note_op(static_cast<cudaStream_t>(stream), kOpOther);
+  cudaError_t e = launch_repack_ptq1_stream(static_cast<const uint8_t*>(Wpt),
+                                            static_cast<uint8_t*>(Wt1), rows, cols,
+                                            static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TQ_OK : fail_cuda(e);
+}
+
 int tq_unrepack(const void* Wtq, void* Wpq2, int64_t rows, int64_t cols, void* stream) {
   if (rows < 0 || cols < 0 || cols % kGroup != 0) return TQ_ERR_SHAPE;
   if (rows == 0 || cols == 0) return TQ_OK;
@@ -388,6 +408,53 @@ int tq_matmul(const void* Wtq, const void* Xq, float* Y, int64_t rows, int64_t c
 int tq_matmul_groupsums(const void* Wtq, const void* Xq, int32_t* S, int64_t rows,
                         int64_t cols, int64_t ntok, void* stream) {
   return matmul_impl(Wtq, Xq, nullptr, S, rows, cols, ntok, nullptr, 0, false, stream);
+}
+
+namespace {
+int matmul_ptq1_stream(const void* Wt1, const void* Xq, float* Y, int32_t* S, int64_t rows,
+                       int64_t cols, int64_t ntok, void* stream) {
+  if (rows < 0 || cols < 0 || ntok < 0 || cols % kQK != 0) return TQ_ERR_SHAPE;
+  if (rows == 0 || ntok == 0) return TQ_OK;
+  void* out = Y ? (void*)Y : (void*)S;
+  if (!out) return TQ_ERR_NULL;
+  const int64_t out_bytes = Y ? ntok * rows * 4 : ntok * rows * (cols / kGroup) * 4;
+  if (!aligned4(out)) return TQ_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cols == 0) {
+    if (Y) {
+      note_op(s, kOpOther);
+      cudaError_t e = cudaMemsetAsync(Y, 0, (size_t)out_bytes, s);
+      if (e != cudaSuccess) return fail_cuda(e);
+    }
+    return TQ_OK;
+  }
+  if (!Wt1 || !Xq) return TQ_ERR_NULL;
+  if (!aligned16(Wt1) || !aligned16(Xq)) return TQ_ERR_ALIGN;
+  const int64_t w_bytes = tq_ptq1_0_stream_bytes(rows, cols);
+  if (overlap(out, out_bytes, Wt1, w_bytes) || overlap(out, out_bytes, Xq, q8K_bytes(ntok, cols)))
+    return TQ_ERR_ALIAS;
+  if (ntok > 0x7fffffff) return TQ_ERR_SHAPE;
+  int* status = nullptr;
+  cudaError_t e = device_status_ptr(&status);
+  if (e != cudaSuccess) return fail_cuda(e);
+  const bool early = early_weights_ok(s, Wt1, w_bytes);
+  note_op(s, kOpOther);
+  e = launch_gemv_ptq1(static_cast<const uint8_t*>(Wt1), static_cast<const uint8_t*>(Xq), Y, S,
+                       rows, cols, (int)ntok, status, early, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  note_kernel(s, kOpMatmul, out, out_bytes);
+  return TQ_OK;
+}
+}  // namespace
+
+int tq_matmul_ptq1_0_stream(const void* Wt1, const void* Xq, float* Y, int64_t rows, int64_t cols,
+                            int64_t ntok, void* stream) {
+  return matmul_ptq1_stream(Wt1, Xq, Y, nullptr, rows, cols, ntok, stream);
+}
+
+int tq_matmul_ptq1_0_stream_groupsums(const void* Wt1, const void* Xq, int32_t* S, int64_t rows,
+                                      int64_t cols, int64_t ntok, void* stream) {
+  return matmul_ptq1_stream(Wt1, Xq, nullptr, S, rows, cols, ntok, stream);
 }
 
 int64_t tq_matmul_workspace_bytes(int64_t rows, int64_t cols, int64_t ntok) {

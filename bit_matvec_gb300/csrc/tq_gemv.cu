@@ -186,33 +186,82 @@ __device__ __forceinline__ void group_dot(const GroupCodes& c, int g, const int8
 // Shared memory: [ring][full bars][red-full bars][red-empty bars][slot counters]
 // [q8 values][group sums][scales][partial sums]
 struct SmemPlan {
-  int64_t ring, bars, counters, sq, sgsum, sdx, red, total;
+  int64_t ring, bars, counters, sq, sgsum, sdx, red, table, total;
 };
 
-template <int T>
+// Weight formats the dp4a GEMV streams: the tq tiles (2 bits per weight) or
+// the ptq1_0 stream tiles (1.75 bits, decoded in the kernel).
+constexpr int kFmtTq = 0;
+constexpr int kFmtPtq1 = 1;
+template <int F>
+__host__ __device__ constexpr int fmt_tile_bytes() { return F == kFmtPtq1 ? kTq1TileBytes : kTileBytes; }
+
+template <int T, int F = kFmtTq>
 __host__ __device__ inline SmemPlan plan_smem(int stages, int64_t cols) {
   SmemPlan p;
   const int64_t g = cols / kGroup, b = cols / kQK;
   p.ring = 0;
-  p.bars = (int64_t)stages * Cfg<T>::kStageBytes;        // full[S], redfull[2], redempty[2]
+  p.bars = (int64_t)stages * Cfg<T>::kStageTiles * fmt_tile_bytes<F>();   // full[S], redfull[2], redempty[2]
   p.counters = p.bars + (stages + 4) * 8;                  // int[S] released, int[S] issued
   p.sq = (p.counters + stages * 8 + 15) / 16 * 16;
   p.sgsum = p.sq + T * cols;
   p.sdx = p.sgsum + T * g * 4;
   p.red = p.sdx + T * b * 4;
-  p.total = p.red + (int64_t)2 * Cfg<T>::kWarps * T * 32 * 4;
+  p.table = p.red + (int64_t)2 * Cfg<T>::kWarps * T * 32 * 4;
+  p.total = p.table + (F == kFmtPtq1 ? 256 * 4 : 0);   // byte -> five 2-bit codes
   return p;
 }
 
-template <int T, bool kGroupSums>
+// The five trits of every byte value as 2-bit codes, trit n at bits 2n.
+__device__ __forceinline__ uint32_t ptq1_codes(uint32_t b) {
+  uint32_t v = 0;
+#pragma unroll
+  for (int n = 0; n < 5; ++n) v |= ptq1_trit(b, n) << (2 * n);
+  return v;
+}
+
+// One row's ptq1_0 block of a stream tile (28 bytes: fp16 scale, then 26
+// code bytes of five weights each) -> the 128 codes as a 2-bit stream, weight
+// k at bits 2 (k % 16) of word k / 16, through the 256-entry table; the last
+// code byte's two unused trits fall past the stream.
+__device__ __forceinline__ void ptq1_decode(const uint8_t* blk, const uint32_t* table,
+                                            uint4& lo, uint4& hi, uint32_t& scale) {
+  uint32_t bw[kPtq1Bytes / 4];
+#pragma unroll
+  for (int i = 0; i < kPtq1Bytes / 4; ++i) bw[i] = reinterpret_cast<const uint32_t*>(blk)[i];
+  uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int c = 0; c < kPtq1Bytes - 2; ++c) {
+    const uint32_t v = table[(bw[(2 + c) >> 2] >> (8 * ((2 + c) & 3))) & 0xFFu];
+    const int bit = 10 * c;
+    w[bit >> 5] |= v << (bit & 31);
+    if ((bit & 31) > 22 && (bit >> 5) + 1 < 8) w[(bit >> 5) + 1] |= v >> (32 - (bit & 31));
+  }
+  lo = make_uint4(w[0], w[1], w[2], w[3]);
+  hi = make_uint4(w[4], w[5], w[6], w[7]);
+  scale = bw[0] & 0xFFFFu;
+}
+
+// Four words of 16 int8 activations x0..x15 -> slot-major order: word s holds
+// x_s, x_{s+4}, x_{s+8}, x_{s+12}, the activations that a 2-bit stream word's
+// slot s (bits 2s of each byte) multiplies.
+__device__ __forceinline__ uint4 act_slot_major(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
+  const uint32_t t0 = __byte_perm(w0, w1, 0x5140), t1 = __byte_perm(w2, w3, 0x5140);
+  const uint32_t t2 = __byte_perm(w0, w1, 0x7362), t3 = __byte_perm(w2, w3, 0x7362);
+  return make_uint4(__byte_perm(t0, t1, 0x5410), __byte_perm(t0, t1, 0x7632),
+                    __byte_perm(t2, t3, 0x5410), __byte_perm(t2, t3, 0x7632));
+}
+
+template <int T, bool kGroupSums, int F = kFmtTq>
 __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kernel(const GemvArgs a) {
   constexpr int kConsumers = Cfg<T>::kWarps;
   constexpr int kStageTiles = Cfg<T>::kStageTiles;
-  constexpr int kStageBytes = Cfg<T>::kStageBytes;
+  constexpr int kTileB = fmt_tile_bytes<F>();
+  constexpr int kStageBytes = kStageTiles * kTileB;
   extern __shared__ __align__(128) uint8_t smem[];
   const int S = a.stages;
   const int cols = a.ngroups * kGroup;
-  const SmemPlan pl = plan_smem<T>(S, cols);
+  const SmemPlan pl = plan_smem<T, F>(S, cols);
   uint8_t* ring = smem + pl.ring;                                 // [S][stage]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + pl.bars);  // [S]
   uint64_t* redfull = full + S;                                   // [2]
@@ -223,6 +272,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
   int* sgsum = reinterpret_cast<int*>(smem + pl.sgsum);           // [T][ngroups]
   float* sdx = reinterpret_cast<float*>(smem + pl.sdx);           // [T][nblk]
   float* red = reinterpret_cast<float*>(smem + pl.red);           // [2][kConsumers][T][32]
+  uint32_t* table = reinterpret_cast<uint32_t*>(smem + pl.table); // [256] (ptq1_0 stream)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // this CTA's tile columns, and the bulk copies (stages) that cover them
@@ -239,12 +289,12 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
   // advance these incrementally (no division in the loop).
   auto issue = [&](int slot, int rb, int st) {
     const int gs = st * kStageTiles;
-    const uint32_t bytes = (uint32_t)(min(kStageTiles, a.ngroups - gs) * kTileBytes);
+    const uint32_t bytes = (uint32_t)(min(kStageTiles, a.ngroups - gs) * kTileB);
     const uint32_t bar = smem_u32(full + slot);
     ++issued[slot];   // one thread at a time per slot: the ring protocol orders them
     mbarrier_arrive_expect_tx(bar, bytes);
     bulk_copy_g2s(smem_u32(ring + (size_t)slot * kStageBytes),
-                  a.Wtq + ((int64_t)rb * a.ngroups + gs) * kTileBytes, bytes, bar, policy);
+                  a.Wtq + ((int64_t)rb * a.ngroups + gs) * kTileB, bytes, bar, policy);
   };
   auto issue_first = [&]() {
     if (stalled) return;
@@ -292,6 +342,17 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
                      if ((lane & 15) == 0) sgsum[2 * tb + (lane >> 4)] = hs;
                      if (lane == 0) sdx[tb] = d;
                    });
+  } else if (F == kFmtPtq1) {
+    // 16 activations per thread, stored slot-major for the 2-bit stream words
+    const int nc = T * a.nblk * (kQK / 16);
+    for (int c = threadIdx.x; c < nc; c += Cfg<T>::kThreads) {
+      const int tb = c >> 4, k = c & 15;
+      const uint32_t* src =
+          reinterpret_cast<const uint32_t*>(a.Xq + (int64_t)tb * kQ8KBytes + kQ8KQsOffset) + 4 * k;
+      reinterpret_cast<uint4*>(sq + tb * kQK)[k] =
+          act_slot_major(__ldg(src), __ldg(src + 1), __ldg(src + 2), __ldg(src + 3));
+    }
+    for (int i = threadIdx.x; i < 256; i += Cfg<T>::kThreads) table[i] = ptq1_codes((uint32_t)i);
   } else {
     const int nw = T * a.nblk * (kQK / 4);
 #pragma unroll 4
@@ -300,6 +361,8 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
       reinterpret_cast<uint32_t*>(sq + tb * kQK)[k] = __ldg(
           reinterpret_cast<const uint32_t*>(a.Xq + (int64_t)tb * kQ8KBytes + kQ8KQsOffset) + k);
     }
+  }
+  if (!a.X) {
     for (int h = threadIdx.x; h < T * a.nblk * 2; h += Cfg<T>::kThreads) {
       const int tb = h >> 1, half = h & 1;
       const uint8_t* blk = a.Xq + (int64_t)tb * kQ8KBytes;
@@ -350,10 +413,14 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, Cfg<T>::kMinCtas) gemv_kerne
       for (int u = 0; u < Cfg<T>::kTilesPerWarp; ++u) {
         const int tl = warp + u * kConsumers;
         if (!failed && tl < nt) {
-          const uint8_t* tile = ring + (size_t)slot * kStageBytes + tl * kTileBytes;
-          c[u].lo = *reinterpret_cast<const uint4*>(tile + lane * 16);
-          c[u].hi = *reinterpret_cast<const uint4*>(tile + 512 + lane * 16);
-          c[u].scale = *reinterpret_cast<const uint16_t*>(tile + kTileCodeBytes + lane * 2);
+          const uint8_t* tile = ring + (size_t)slot * kStageBytes + tl * kTileB;
+          if (F == kFmtPtq1) {
+            ptq1_decode(tile + lane * kPtq1Bytes, table, c[u].lo, c[u].hi, c[u].scale);
+          } else {
+            c[u].lo = *reinterpret_cast<const uint4*>(tile + lane * 16);
+            c[u].hi = *reinterpret_cast<const uint4*>(tile + 512 + lane * 16);
+            c[u].scale = *reinterpret_cast<const uint16_t*>(tile + kTileCodeBytes + lane * 2);
+          }
         }
       }
       __syncwarp();   // the whole warp has read its tile: release the slot
@@ -917,10 +984,10 @@ cudaError_t launch_mma(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
   return launch_pdl(kernel, dim3(grid), dim3(MmaCfg<T, TPW>::kThreads), (size_t)smem, s, a);
 }
 
-template <int T, bool G>
+template <int T, bool G, int F = kFmtTq>
 cudaError_t launch_t(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
   static_assert(T >= 1 && T <= kMaxDp4aTok, "token count");
-  auto kernel = gemv_kernel<T, G>;
+  auto kernel = gemv_kernel<T, G, F>;
   GemvArgs a = a0;
   DeviceLimits lim;
   cudaError_t e = device_limits(&lim);
@@ -928,8 +995,8 @@ cudaError_t launch_t(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
   const int optin = lim.optin_smem, nsm = lim.sms;
   // deepest ring that fits
   int stages = TQ_GEMV_MAX_STAGES;
-  while (stages > 2 && plan_smem<T>(stages, cols).total > optin) --stages;
-  const int64_t smem = plan_smem<T>(stages, cols).total;
+  while (stages > 2 && plan_smem<T, F>(stages, cols).total > optin) --stages;
+  const int64_t smem = plan_smem<T, F>(stages, cols).total;
   if (smem > optin) return cudaErrorNotSupported;
   a.stages = stages;
   e = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), (int)smem);
@@ -1006,9 +1073,58 @@ cudaError_t launch_tok(const GemvArgs& a, int64_t cols, bool gsum, cudaStream_t 
     return cudaErrorNotSupported;
 }
 
+template <bool G>
+cudaError_t launch_ptq1_tok(const GemvArgs& a, int64_t cols, int ntok, cudaStream_t s) {
+  switch (ntok) {
+    case 1: return launch_t<1, G, kFmtPtq1>(a, cols, s);
+    case 2: return launch_t<2, G, kFmtPtq1>(a, cols, s);
+    case 3: return launch_t<3, G, kFmtPtq1>(a, cols, s);
+    case 4: return launch_t<4, G, kFmtPtq1>(a, cols, s);
+    case 5: return launch_t<5, G, kFmtPtq1>(a, cols, s);
+    case 6: return launch_t<6, G, kFmtPtq1>(a, cols, s);
+    case 7: return launch_t<7, G, kFmtPtq1>(a, cols, s);
+    default: return launch_t<8, G, kFmtPtq1>(a, cols, s);
+  }
+}
+
 }  // namespace
 
 int gemv_max_tokens() { return kMaxTok; }
+
+cudaError_t launch_gemv_ptq1(const uint8_t* Wt1, const uint8_t* Xq, float* Y, int32_t* S,
+                             int64_t rows, int64_t cols, int ntok, int* dev_status,
+                             bool early_weights, cudaStream_t s) {
+  if (ntok < 1) return cudaSuccess;
+  if (rows > 0x7fffffff / 2 || cols / kGroup > 0x7fffffff / kTq1TileBytes)
+    return cudaErrorNotSupported;
+  const int nblk = (int)(cols / kQK);
+  const int ngroups = (int)(cols / kGroup);
+  // launches of up to 8 tokens (each streams the weights once)
+  for (int t0 = 0; t0 < ntok; t0 += kMaxDp4aTok) {
+    const int n = min(kMaxDp4aTok, ntok - t0);
+    GemvArgs a;
+    a.Wtq = Wt1;
+    a.Xq = Xq + (int64_t)t0 * nblk * kQ8KBytes;
+    a.Y = Y ? Y + (int64_t)t0 * rows : nullptr;
+    a.S = S ? S + (int64_t)t0 * rows * ngroups : nullptr;
+    a.status = dev_status;
+    a.rows = (int)rows;
+    a.ngroups = ngroups;
+    a.nblk = nblk;
+    a.nrb = (int)((rows + kTileRows - 1) / kTileRows);
+    a.stages = 2;
+    // a later chunk follows this function's own GEMV, which writes no weights
+    a.early_weights = (early_weights || t0 > 0) ? 1 : 0;
+    a.X = nullptr;
+    a.Xq_out = nullptr;
+    a.defer = 0;
+    a.stall = 0;
+    a.stall_ns = 0;
+    const cudaError_t e = S ? launch_ptq1_tok<true>(a, cols, n, s) : launch_ptq1_tok<false>(a, cols, n, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
 
 
 cudaError_t launch_gemv(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t* S,

@@ -19,6 +19,9 @@ constexpr int kQ8KBytes = TQ_Q8K_BYTES;
 constexpr int kTileRows = TQ_TILE_ROWS;  // rows per tile of the tq layout
 constexpr int kTileBytes = TQ_TILE_BYTES;
 constexpr int kTileCodeBytes = 1024;     // code bytes per tile; fp16 scales follow
+// ptq1_0 stream layout: the 28-byte ptq1_0 blocks of 32 rows and one group,
+// row after row (row l of the tile at byte 28 l)
+constexpr int kTq1TileBytes = kTileRows * TQ_PTQ1_0_BYTES;   // 896
 constexpr int kQ8KQsOffset = 4;          // byte offset of qs in a q8_K block
 constexpr int kQ8KBsumsOffset = 260;     // byte offset of bsums in a q8_K block
 
@@ -303,6 +306,22 @@ void record_cuda_error(cudaError_t e);
 // Read-ceiling probe: adds the buffer's 32-bit words (wrapping) to *out.
 cudaError_t launch_read_sum(const void* buf, int64_t bytes, uint32_t* out, bool early,
                             cudaStream_t s);
+
+// ptq1_0 stream layout (see tq_repack_ptq1_0_stream): re-tiling of the file.
+cudaError_t launch_repack_ptq1_stream(const uint8_t* Wpt, uint8_t* Wt1, int64_t rows,
+                                      int64_t cols, cudaStream_t s);
+// GEMV over the ptq1_0 stream layout (1.75 bits per weight streamed and
+// decoded in the kernel), any ntok >= 1 in launches of up to 8 tokens.
+cudaError_t launch_gemv_ptq1(const uint8_t* Wt1, const uint8_t* Xq, float* Y, int32_t* S,
+                             int64_t rows, int64_t cols, int ntok, int* dev_status,
+                             bool early_weights, cudaStream_t s);
+
+// Trit n (0..4) of a ptq1_0 code byte b: floor(3 * (b * 3^n mod 256) / 256),
+// the code u = w + 1 (the ternary post, "the detour that lost").
+__host__ __device__ __forceinline__ uint32_t ptq1_trit(uint32_t b, int n) {
+  const uint32_t p3 = n == 0 ? 1u : n == 1 ? 3u : n == 2 ? 9u : n == 3 ? 27u : 81u;
+  return (((b * p3) & 0xFFu) * 3u) >> 8;
+}
 
 // Test facility (tq_debug_stall_next_launch): the wait limit in ns that the
 // next matmul kernel launched takes for its stalled first CTA, or 0 if none is

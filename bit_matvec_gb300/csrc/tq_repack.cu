@@ -110,8 +110,7 @@ repack_ptq1_kernel(const uint8_t* __restrict__ Wpt, uint8_t* __restrict__ Wtq, i
     for (int k = 0; k < kGroup; ++k) {
       const int c = k / 5, n = k % 5;
       const uint32_t b = (bw[(2 + c) >> 2] >> (8 * ((2 + c) & 3))) & 0xFFu;
-      const uint32_t p3 = n == 0 ? 1u : n == 1 ? 3u : n == 2 ? 9u : n == 3 ? 27u : 81u;
-      const uint32_t u = (((b * p3) & 0xFFu) * 3u) >> 8;
+      const uint32_t u = ptq1_trit(b, n);
       // tq position of weight k: word (k / 64) * 4 + (k % 64) / 16, byte k % 4,
       // bits 2 * ((k % 16) / 4)
       w[(k >> 6) * 4 + ((k & 63) >> 4)] |= u << (8 * (k & 3) + 2 * ((k & 15) >> 2));
@@ -123,6 +122,29 @@ repack_ptq1_kernel(const uint8_t* __restrict__ Wpt, uint8_t* __restrict__ Wtq, i
   *reinterpret_cast<uint4*>(out + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
   *reinterpret_cast<uint4*>(out + 512 + lane * 16) = make_uint4(w[4], w[5], w[6], w[7]);
   reinterpret_cast<uint16_t*>(out + kTileCodeBytes)[lane] = scale;
+}
+
+// ptq1_0 stream layout: one warp per (32-row block, group) tile; lane l
+// copies row l's 28-byte block (seven words) to byte 28 l of the tile. Rows
+// past the matrix get scale 0 and code bytes 0x80 (five trits of 1: w = 0).
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+repack_ptq1_stream_kernel(const uint8_t* __restrict__ Wpt, uint8_t* __restrict__ Wt1, int64_t rows,
+                          int64_t ngroups, int64_t ntiles) {
+  const int lane = threadIdx.x & 31;
+  const int64_t tile = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  if (tile >= ntiles) return;
+  const int64_t rb = tile / ngroups, g = tile - rb * ngroups;
+  const int64_t r = rb * kTileRows + lane;
+  uint32_t* out = reinterpret_cast<uint32_t*>(Wt1 + tile * kTq1TileBytes + lane * kPtq1Bytes);
+  if (r < rows) {
+    const uint32_t* blk = reinterpret_cast<const uint32_t*>(Wpt + (r * ngroups + g) * kPtq1Bytes);
+#pragma unroll
+    for (int i = 0; i < kPtq1Bytes / 4; ++i) out[i] = blk[i];
+  } else {
+    out[0] = 0x80800000u;
+#pragma unroll
+    for (int i = 1; i < kPtq1Bytes / 4; ++i) out[i] = 0x80808080u;
+  }
 }
 
 int64_t tile_count(int64_t rows, int64_t cols) {
@@ -150,6 +172,17 @@ cudaError_t launch_repack_ptq1(const uint8_t* Wpt, uint8_t* Wtq, int64_t rows, i
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
   repack_ptq1_kernel<<<(unsigned)grid, kWarpsPerCta * 32, 0, s>>>(Wpt, Wtq, rows, cols / kGroup,
                                                                   ntiles);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repack_ptq1_stream(const uint8_t* Wpt, uint8_t* Wt1, int64_t rows,
+                                      int64_t cols, cudaStream_t s) {
+  const int64_t ntiles = tile_count(rows, cols);
+  if (ntiles <= 0) return cudaSuccess;
+  const int64_t grid = (ntiles + kWarpsPerCta - 1) / kWarpsPerCta;
+  if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  repack_ptq1_stream_kernel<<<(unsigned)grid, kWarpsPerCta * 32, 0, s>>>(Wpt, Wt1, rows,
+                                                                         cols / kGroup, ntiles);
   return cudaGetLastError();
 }
 

@@ -153,6 +153,47 @@ int64_t tq_ptq1_0_bytes(int64_t rows, int64_t cols);
 int tq_repack_ptq1_0(const void *Wpt, void *Wtq, int64_t rows, int64_t cols, void *stream);
 
 /*
+ * The streamed 1.75-bit form (post, "the detour that lost": the file is 18%
+ * smaller, and on a machine limited by memory that should win; on the CPU the
+ * decode cost more than the bytes saved). Here the GEMV streams the ptq1_0
+ * bytes themselves and decodes them in the kernel: each code byte goes
+ * through a 256-entry shared-memory table (byte -> its five trits as 2-bit
+ * codes), the five-weight chunks are laid end to end into the same 2-bit code
+ * words the pq2_0 path uses, and the activations are staged in the matching
+ * order, so the dot product is the same AND-per-slot dp4a. Measured on GB300
+ * with one token on the 32768 x 8192 decode matrix it takes 30.6 us per
+ * launch against 12.6 us for the 2-bit stream of the same weights: the
+ * decode costs about 2.5 times the 2-bit unpack's instructions, more than the
+ * 18% fewer bytes save. As on the CPU, the file is therefore decoded once at
+ * load (tq_repack_ptq1_0) for the product path; this form is kept so that the
+ * trade can be measured.
+ *
+ * tq_ptq1_0_stream_bytes -- ceil(rows/32) * (cols/128) * 896; -1 if
+ * cols % 128 != 0 or a size is negative.
+ *
+ * tq_repack_ptq1_0_stream -- load-time re-tiling of a ptq1_0 file, no decode:
+ * tile (row block rb, group g) is 896 bytes at (rb * cols/128 + g) * 896, the
+ * 28-byte blocks of rows 32 rb .. 32 rb + 31 and group g, row l at byte 28 l
+ * (rows past the matrix: scale 0 and code bytes 0x80, five trits of 1: w = 0).
+ *   Wpt [rows][cols/128] ptq1_0 blocks, 16-byte aligned.
+ *   Wt1 tq_ptq1_0_stream_bytes(rows, cols) bytes, 16-byte aligned, written.
+ * Errors: as tq_repack_ptq1_0.
+ *
+ * tq_matmul_ptq1_0_stream / tq_matmul_ptq1_0_stream_groupsums -- tq_matmul and
+ * tq_matmul_groupsums over the stream tiles: the same results (the same exact
+ * group sums, the same tolerance on Y), in launches of up to 8 tokens, each
+ * reading the weights once.
+ *   Wt1 the stream tiles, 16-byte aligned; Xq, Y, S as tq_matmul(_groupsums).
+ * Errors: as tq_matmul.
+ */
+int64_t tq_ptq1_0_stream_bytes(int64_t rows, int64_t cols);
+int tq_repack_ptq1_0_stream(const void *Wpt, void *Wt1, int64_t rows, int64_t cols, void *stream);
+int tq_matmul_ptq1_0_stream(const void *Wt1, const void *Xq, float *Y, int64_t rows, int64_t cols,
+                            int64_t ntok, void *stream);
+int tq_matmul_ptq1_0_stream_groupsums(const void *Wt1, const void *Xq, int32_t *S, int64_t rows,
+                                      int64_t cols, int64_t ntok, void *stream);
+
+/*
  * tq_matmul -- Y = the ternary x q8_K product (definition at the top).
  * Each group sum is exact in int32 (post, "the trick with 4 and 16": the
  * largest scaled intermediate is 520,192); the scale products and the sum

@@ -172,6 +172,26 @@ def pack_pq2_0(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     return np.concatenate([sc, packed], axis=2).reshape(-1)
 
 
+def pack_ptq1_0(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """Write ternary codes u[rows][cols] (0..2) and fp16 scales as the 1.75-bit
+    ptq1_0 file: per 128 weights of a row {fp16 scale; 26 code bytes}, weight
+    k in trit k % 5 of code byte k / 5 (the last byte's two spare trits zero),
+    and the byte of trits t0..t4 the smallest b with those trits, ceil(256 q /
+    243) for q = t0 81 + t1 27 + t2 9 + t3 3 + t4 (the format's encoding; the
+    page gives only its decode). Returns a flat uint8 array of rows * cols/128
+    * 28 bytes."""
+    rows, cols = codes.shape
+    assert cols % GROUP == 0 and scales.shape == (rows, cols // GROUP)
+    g = cols // GROUP
+    t = np.zeros((rows, g, 130), np.int64)
+    t[:, :, :GROUP] = codes.reshape(rows, g, GROUP)
+    t = t.reshape(rows, g, 26, 5)
+    q = t[..., 0] * 81 + t[..., 1] * 27 + t[..., 2] * 9 + t[..., 3] * 3 + t[..., 4]
+    packed = ((256 * q + 242) // 243).astype(np.uint8)
+    sc = np.ascontiguousarray(scales.astype(np.float16)).view(np.uint8).reshape(rows, g, 2)
+    return np.concatenate([sc, packed], axis=2).reshape(-1)
+
+
 def pq2_0_weights(rows: int, cols: int, config_index: int, row0: int = 0) -> np.ndarray:
     """pq2_0 bytes of rows row0 .. row0+rows-1 of a workload's weight matrix."""
     s = seeds(config_index)

@@ -61,3 +61,15 @@ def test_conversion_matches_the_pq2_0_packer():
         assert wpt.size == rows * cols // 128 * 28
         assert np.array_equal(oracle.ptq1_0_to_pq2_0(wpt, rows, cols),
                               synth.pack_pq2_0(codes, scales))
+
+
+def test_synthetic_ptq1_packer_matches_oracle_encoder():
+    """The input generator's ptq1_0 packer (used where only generators may run)
+    writes the bytes of the oracle's encoder, which the tests above pin."""
+    rows, cols = 9, 640
+    s = synth.seeds(5)
+    codes = synth.ternary_codes(rows, cols, s["weights"])
+    scales = synth.group_scales(rows, cols, s["scales"])
+    sb = np.ascontiguousarray(scales.astype(np.float16)).view(np.uint16)
+    assert np.array_equal(synth.pack_ptq1_0(codes, scales),
+                          oracle.encode_ptq1_0(codes.astype(np.int8) - 1, sb))
