@@ -80,9 +80,10 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // A smaller tile for fewer tokens: a smaller B per group (less to stage and
 // to read from L2), fewer accumulator columns for the epilogue to read, and
 // room in tensor memory for more group stages.
-template <int N>
+template <int N, int CG = 1>
 struct TcCfg {
   static_assert(N == 16 || N == 32 || N == 64, "token tile");
+  static_assert(CG == 1 || CG == 2, "CTAs per MMA");
   static constexpr int kN = N;                         // tokens per CTA
   static constexpr int kNB = 2 * N;                    // UMMA N: low and high parts
   // A + accumulator ring in tensor memory, one group per stage
@@ -109,9 +110,11 @@ struct TcCfg {
   static constexpr int kSumOff = N;                    // floats
   static constexpr int kDxFloats = N + kGPB * N;
   static constexpr int kDxBytes = kDxFloats * 4;
-  // one staged slot: the block's B tiles, its weight tiles (per 32-row tile
-  // both groups, adjacent), its scales and sums
-  static constexpr int kInW = kGPB * kBTile;
+  // one staged slot: the block's B tiles (with a CTA pair, this CTA's half of
+  // each: rows 0..N-1, the low parts, in rank 0; rows N..2N-1 in rank 1), its
+  // weight tiles (per 32-row tile both groups, adjacent), its scales and sums
+  static constexpr int kBPart = kBTile / CG;
+  static constexpr int kInW = kGPB * kBPart;
   static constexpr int kInDx = kInW + kTilesPerCta * kWRun;
   static constexpr int kInBytes = kInDx + kDxBytes;
   static_assert(kInBytes % 16 == 0 && kWRun % 16 == 0 && kInW % 16 == 0 && kDxBytes % 16 == 0,
@@ -125,12 +128,16 @@ struct TcCfg {
   // Enough shared memory that only one CTA fits on an SM: each CTA allocates
   // all 512 tensor-memory columns.
   static constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
-  static constexpr uint32_t kIdesc = idesc_e4m3(kM, kNB);
+  static constexpr uint32_t kIdesc = idesc_e4m3(kM * CG, kNB);
 };
 
 // Local names for the token tile's constants inside a function templated on N.
 #define TQ_TC_CFG(N)                                                        \
-  using Cfg_ = TcCfg<N>;                                                    \
+  TQ_TC_CFG2(N, 1)
+#define TQ_TC_CFG2(N, CG)                                                   \
+  using Cfg_ = TcCfg<N, CG>;                                                \
+  constexpr int kBPart = Cfg_::kBPart;                                      \
+  (void)kBPart;                                                             \
   constexpr int kN = Cfg_::kN;                                              \
   constexpr int kNB = Cfg_::kNB;                                            \
   constexpr int kStages = Cfg_::kStages;                                    \
@@ -296,8 +303,8 @@ struct WsArgs {
   int ngroups;
   int nblk;
   int nrb;
-  int stall;          // test facility: CTA (0, 0) requests no input, so its waits
-  uint64_t stall_ns;  // expire after stall_ns (tq_debug_stall_next_launch)
+  int stall;          // test facility: the first CTA (pair) requests no input, so its
+  uint64_t stall_ns;  // waits expire after stall_ns (tq_debug_stall_next_launch)
 };
 
 // One group's codes (this thread: one row, the 64 weights of one k half) ->
@@ -318,9 +325,14 @@ __device__ __forceinline__ void convert_store(const uint4 codes, uint32_t taddr)
   tmem_st16(taddr, wa);
 }
 
-template <int N, bool kGroupSums>
-__global__ void __launch_bounds__(TcCfg<N>::kThreads, 1) gemm_tc_ws_kernel(const WsArgs a) {
-  TQ_TC_CFG(N);
+// CG = 2: the CTAs of a cluster of 2 (consecutive 128-row blocks, one token
+// tile) run each MMA as a pair: rank 0 issues 256-row MMAs over both CTAs'
+// tensor memory, and each CTA stages only its half of B. The converters and
+// epilogues of both CTAs arrive on rank 0's mma_ready; rank 0's commits
+// arrive on both CTAs' mma_done and in_empty.
+template <int N, int CG, bool kGroupSums>
+__global__ void __launch_bounds__(TcCfg<N, CG>::kThreads, 1) gemm_tc_ws_kernel(const WsArgs a) {
+  TQ_TC_CFG2(N, CG);
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sIn = smem;                                                         // [in][slot]
   float* sScale = reinterpret_cast<float*>(smem + kInStages * kInBytes);       // [scale][448]
@@ -346,14 +358,17 @@ __global__ void __launch_bounds__(TcCfg<N>::kThreads, 1) gemm_tc_ws_kernel(const
   const int64_t rb0 = (int64_t)blockIdx.x * kTilesPerCta;
   const int64_t nt = blockIdx.y;
   const int64_t tok0 = nt * kN;
-  const bool stalled = a.stall && blockIdx.x == 0 && blockIdx.y == 0;
+  // the test stall takes the first CTA (with pairs, the first pair: once one
+  // CTA of a pair gives up, the other's waits can fall out of step with the
+  // pair's commits and would run to their own limit)
+  const bool stalled = a.stall && blockIdx.x < (unsigned)CG && blockIdx.y == 0;
   const uint64_t lim = stalled ? a.stall_ns : kWaitLimitNs;   // bound of the pipeline's waits
   int issued[kInStages] = {};   // producer: copies requested per input slot
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;   // rank 0 issues the MMAs
 
   if (warp == kMmaWarp) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                 ::"r"(smem_u32(tmem_slot)), "r"(kTmemCols) : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tmem_alloc<CG>(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish<CG>();
   }
   if (tid == 0) {
     // Consumer warps arrive once per warp (lane 0, after __syncwarp).
@@ -364,7 +379,7 @@ __global__ void __launch_bounds__(TcCfg<N>::kThreads, 1) gemm_tc_ws_kernel(const
       mbarrier_init(smem_u32(in_empty + i), kConvWarps + 1);
     }
     for (int s = 0; s < kStages; ++s) {
-      mbarrier_init(smem_u32(mma_ready + s), kConvWarps + kEpiWarps);
+      mbarrier_init(smem_u32(mma_ready + s), CG * (kConvWarps + kEpiWarps));
       mbarrier_init(smem_u32(mma_done + s), 1);
     }
     mbarrier_init(smem_u32(drain_bar), 1);
@@ -373,6 +388,7 @@ __global__ void __launch_bounds__(TcCfg<N>::kThreads, 1) gemm_tc_ws_kernel(const
   }
   tc_fence_before();
   __syncthreads();
+  if (CG == 2) cluster_sync();   // the peer's barriers are initialized before any arrival
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool failed = false;
@@ -401,8 +417,16 @@ __global__ void __launch_bounds__(TcCfg<N>::kThreads, 1) gemm_tc_ws_kernel(const
         const int g0 = j * kGPB;
         // the activations first (from L2), then the weights (from HBM)
         mbarrier_arrive_expect_tx(full, (uint32_t)(kInW + nvalid * kWRun + kDxBytes));
-        bulk_copy_g2s(smem_u32(st + kInB), a.Bt + (nt * G + g0) * (int64_t)kBTile, kInW, full,
-                      policy);
+        if (CG == 1) {
+          bulk_copy_g2s(smem_u32(st + kInB), a.Bt + (nt * G + g0) * (int64_t)kBTile, kInW, full,
+                        policy);
+        } else {
+#pragma unroll
+          for (int gi = 0; gi < kGPB; ++gi)
+            bulk_copy_g2s(smem_u32(st + kInB + gi * kBPart),
+                          a.Bt + (nt * G + g0 + gi) * (int64_t)kBTile + rank * kBPart, kBPart, full,
+                          policy);
+        }
         for (int q = 0; q < nvalid; ++q)
           bulk_copy_g2s(smem_u32(st + kInW + q * kWRun), a.Wtq + ((rb0 + q) * G + g0) * kTileBytes,
                         kWRun, full, policy);
@@ -472,7 +496,10 @@ __global__ void __launch_bounds__(TcCfg<N>::kThreads, 1) gemm_tc_ws_kernel(const
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbarrier_arrive(smem_u32(mma_ready + sa));
+        if (lane == 0) {
+          if (CG == 1) mbarrier_arrive(smem_u32(mma_ready + sa));
+          else mbarrier_arrive_rank(smem_u32(mma_ready + sa), 0u);   // rank 0 issues
+        }
         if (++sa == kStages) { sa = 0; pa ^= 1u; }
         ++g;
       }
@@ -492,7 +519,10 @@ __global__ void __launch_bounds__(TcCfg<N>::kThreads, 1) gemm_tc_ws_kernel(const
     int sa = 0, ss = 0;
     uint32_t pa = 0;
     if (lane == 0) {   // all accumulator stages start free (groups 0..kStages-1)
-      for (int s = 0; s < kStages; ++s) mbarrier_arrive(smem_u32(mma_ready + s));
+      for (int s = 0; s < kStages; ++s) {
+        if (CG == 1) mbarrier_arrive(smem_u32(mma_ready + s));
+        else mbarrier_arrive_rank(smem_u32(mma_ready + s), 0u);
+      }
     }
     for (int b = 0; b < nb; ++b) {
       const float* sst = sScale + ss * kScaleFloats;
@@ -544,7 +574,10 @@ __global__ void __launch_bounds__(TcCfg<N>::kThreads, 1) gemm_tc_ws_kernel(const
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbarrier_arrive(smem_u32(mma_ready + sa));   // for group g + kStages
+        if (lane == 0) {   // for group g + kStages
+          if (CG == 1) mbarrier_arrive(smem_u32(mma_ready + sa));
+          else mbarrier_arrive_rank(smem_u32(mma_ready + sa), 0u);
+        }
         if (++sa == kStages) { sa = 0; pa ^= 1u; }
       }
       if (++ss == kScaleStages) ss = 0;
@@ -558,8 +591,8 @@ __global__ void __launch_bounds__(TcCfg<N>::kThreads, 1) gemm_tc_ws_kernel(const
         if (t + 1 < a.ntok) a.Y[(t + 1) * a.rows + row] = v.y;
       }
     }
-  } else if (lane == 0) {
-    // ---------------- MMA issuer
+  } else if (lane == 0 && rank == 0) {
+    // ---------------- MMA issuer (rank 0 of a pair)
     int i = 0, sa = 0;
     uint32_t pa = 0;
     for (int b = 0; b < nb; ++b) {
@@ -569,8 +602,9 @@ __global__ void __launch_bounds__(TcCfg<N>::kThreads, 1) gemm_tc_ws_kernel(const
 #pragma unroll
       for (int gi = 0; gi < kGPB; ++gi) {
         // A(g) written and the accumulator of group g - 3 read
-        if (!failed && !mbarrier_test_wait(smem_u32(mma_ready + sa), pa) &&
-            !mbarrier_wait_bounded(smem_u32(mma_ready + sa), pa, lim)) {
+        const bool ok = failed || mbarrier_test_wait(smem_u32(mma_ready + sa), pa) ||
+                        mbarrier_wait_bounded(smem_u32(mma_ready + sa), pa, lim);
+        if (!ok) {
           failed = true;
           *s_failed = 1;
         }
@@ -579,17 +613,22 @@ __global__ void __launch_bounds__(TcCfg<N>::kThreads, 1) gemm_tc_ws_kernel(const
           const uint32_t d = tmem + kAccCol + (uint32_t)sa * kAccCols;
           const uint32_t at = tmem + kACol + (uint32_t)sa * kACols;
 #pragma unroll
-          for (int kk = 0; kk < kMmaPerGroup; ++kk)
-            mma_e4m3_tmem_a(d, at + (uint32_t)(kK / 4) * kk,
-                            bd0 + (uint64_t)((gi * kBTile + kk * 2 * kLBO) >> 4), kIdesc,
-                            kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kMmaPerGroup; ++kk) {
+            const uint64_t bd = bd0 + (uint64_t)((gi * kBPart + kk * 2 * kLBO) >> 4);
+            if (CG == 1)
+              mma_e4m3_tmem_a(d, at + (uint32_t)(kK / 4) * kk, bd, kIdesc, kk > 0 ? 1u : 0u);
+            else
+              mma_e4m3_tmem_a_pair(d, at + (uint32_t)(kK / 4) * kk, bd, kIdesc, kk > 0 ? 1u : 0u);
+          }
         }
         // the commit fires when these MMAs are done (at once if none were issued)
-        mma_commit(smem_u32(mma_done + sa));
+        if (CG == 1) mma_commit(smem_u32(mma_done + sa));
+        else mma_commit_pair(smem_u32(mma_done + sa));
         if (++sa == kStages) { sa = 0; pa ^= 1u; }
       }
       // the slot's B is read once these MMAs are complete
-      mma_commit(smem_u32(in_empty + i));
+      if (CG == 1) mma_commit(smem_u32(in_empty + i));
+      else mma_commit_pair(smem_u32(in_empty + i));
       if (++i == kInStages) i = 0;
     }
   }
@@ -601,23 +640,29 @@ __global__ void __launch_bounds__(TcCfg<N>::kThreads, 1) gemm_tc_ws_kernel(const
   // saw its previous copy land, so at most that one is pending; it completes
   // phase issued - 1 of the slot's barrier), and let every MMA issued finish
   // (a commit tracks all of the issuing thread's earlier MMAs).
-  if (__syncthreads_or(failed)) {
-    if (warp == kProdWarp && lane == 0) {
-      for (int i = 0; i < kInStages; ++i)
-        if (issued[i] > 0)
-          mbarrier_wait_bounded(smem_u32(in_full + i), (uint32_t)((issued[i] - 1) & 1),
-                                kWaitLimitNs);
-    } else if (warp == kMmaWarp && lane == 0) {
-      mma_commit(smem_u32(drain_bar));
-      mbarrier_wait_bounded(smem_u32(drain_bar), 0u, kWaitLimitNs);
+  // With a pair, rank 0's MMAs write both CTAs' tensor memory: both wait for
+  // its final commit (always; a failure in either CTA is not seen by the other).
+  const bool any_failed = __syncthreads_or(failed);
+  if (any_failed && warp == kProdWarp && lane == 0) {
+    for (int i = 0; i < kInStages; ++i)
+      if (issued[i] > 0)
+        mbarrier_wait_bounded(smem_u32(in_full + i), (uint32_t)((issued[i] - 1) & 1),
+                              kWaitLimitNs);
+  }
+  if ((any_failed || CG == 2) && warp == kMmaWarp && lane == 0) {
+    if (rank == 0) {
+      if (CG == 1) mma_commit(smem_u32(drain_bar));
+      else mma_commit_pair(smem_u32(drain_bar));
     }
+    if (CG == 1) mbarrier_wait_bounded(smem_u32(drain_bar), 0u, kWaitLimitNs);
+    else mbarrier_wait_bounded_cluster(smem_u32(drain_bar), 0u, kWaitLimitNs);
   }
   tc_fence_before();
   __syncthreads();
+  if (CG == 2) cluster_sync();   // no CTA leaves while the other may still signal it
   if (warp == kMmaWarp) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(kTmemCols) : "memory");
+    tmem_dealloc<CG>(tmem, kTmemCols);
   }
 }
 
@@ -639,11 +684,23 @@ int64_t tc_workspace_bytes(int64_t cols, int64_t ntok) {
 
 namespace {
 
+// CTAs per MMA: 2 runs the kernel on clusters of two CTAs whose MMAs span
+// both (twice the rows per MMA instruction, half of B staged by each CTA).
+// Measured on GB300 (17408 x 5120): 25.5 / 20.7 / 18.7 us at 64 / 32 / 16
+// tokens against 23.6 / 19.3 / 17.5 us for single CTAs, with identical
+// results: the issuing thread then waits on the MMAs themselves (about 150
+// cycles per 256-row MMA), so the halved instruction count does not pay for
+// the cross-CTA hand-offs. Off by default; building with TQ_TC_PAIR=1 selects it.
+#ifndef TQ_TC_PAIR
+#define TQ_TC_PAIR 0
+#endif
+constexpr int kCtasPerMma = TQ_TC_PAIR ? 2 : 1;
+
 // The tensor-core kernel over a workspace already packed.
-template <int N>
+template <int N, int CG = kCtasPerMma>
 cudaError_t launch_main(const uint8_t* Wtq, float* Y, int32_t* S, int64_t rows, int64_t cols,
                         int64_t ntok, uint8_t* ws, int* dev_status, cudaStream_t s) {
-  using C = TcCfg<N>;
+  using C = TcCfg<N, CG>;
   const Layout l = ws_layout<N>(cols, ntok);
   WsArgs a;
   a.Wtq = Wtq;
@@ -660,13 +717,29 @@ cudaError_t launch_main(const uint8_t* Wtq, float* Y, int32_t* S, int64_t rows, 
   const int64_t stall_ns = take_debug_stall();
   a.stall = stall_ns > 0 ? 1 : 0;
   a.stall_ns = stall_ns > 0 ? (uint64_t)stall_ns : 0;
-  const int64_t gx = (rows + kM - 1) / kM;
+  // a whole number of CTA pairs: a last CTA past the rows runs with no weights
+  const int64_t gx = ((rows + kM - 1) / kM + CG - 1) / CG * CG;
   if (gx > 0x7fffffff) return cudaErrorInvalidConfiguration;
   const dim3 grid((unsigned)gx, (unsigned)l.ntile);
-  auto kernel = S ? gemm_tc_ws_kernel<N, true> : gemm_tc_ws_kernel<N, false>;
+  auto kernel = S ? gemm_tc_ws_kernel<N, CG, true> : gemm_tc_ws_kernel<N, CG, false>;
   const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kernel, grid, dim3(C::kThreads), (size_t)C::kSmemBytes, s, a);
+  if (CG == 1) return launch_pdl(kernel, grid, dim3(C::kThreads), (size_t)C::kSmemBytes, s, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = (size_t)C::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CG;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
 template <int N>

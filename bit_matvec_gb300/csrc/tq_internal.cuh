@@ -106,6 +106,32 @@ __device__ __forceinline__ bool mbarrier_test_wait(uint32_t bar, uint32_t parity
   return ok != 0;
 }
 
+// try_wait with acquire at cluster scope: for barriers that threads of the
+// other CTA of a cluster arrive on.
+__device__ __forceinline__ bool mbarrier_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// mbarrier_wait_bounded at cluster scope.
+__device__ __forceinline__ bool mbarrier_wait_bounded_cluster(uint32_t bar, uint32_t parity,
+                                                              uint64_t limit_ns) {
+  if (mbarrier_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0; it < (1u << 28); ++it) {
+    if (mbarrier_try_wait_cluster(bar, parity)) return true;
+    if ((it & 15u) == 15u && global_timer_ns() - t0 > limit_ns) return false;
+  }
+  return false;
+}
+
 // Wait for phase `parity` of an mbarrier, giving up after `limit_ns` of global
 // time (checked every 16 polls, with a cap of 2^28 polls). Returns false on
 // giving up; the caller records the failure and stops using the barrier.

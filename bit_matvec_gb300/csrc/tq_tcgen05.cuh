@@ -75,6 +75,87 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                ::"r"(bar) : "memory");
 }
 
+// ---------------------------------------------------------------- CTA pairs
+//
+// With .cta_group::2 the two CTAs of a cluster of 2 (ranks 0 and 1) act as one
+// MMA unit: one MMA of M = 256 takes rows 0..127 of A and D from the tensor
+// memory of rank 0 and rows 128..255 from that of rank 1 (the same column
+// addresses in both), and N/2 columns of B from the shared memory of each CTA
+// (the same shared-memory offsets in both); rank 0 issues it. Tensor memory is
+// allocated, released and freed by one warp in each CTA of the pair, with the
+// same column count.
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// All threads of both CTAs of the cluster: a release-acquire barrier.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
+template <int CG>
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+  if (CG == 2)
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(slot_smem), "r"(ncols) : "memory");
+  else
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(slot_smem), "r"(ncols) : "memory");
+}
+template <int CG>
+__device__ __forceinline__ void tmem_relinquish() {
+  if (CG == 2)
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  else
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+template <int CG>
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  if (CG == 2)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem], kind::f8f6f4, on the CTA pair (M = 256).
+__device__ __forceinline__ void mma_e4m3_tmem_a_pair(uint32_t d_tmem, uint32_t a_tmem,
+                                                     uint64_t b_desc, uint32_t idesc,
+                                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on the mbarrier at the same shared-memory offset in both CTAs of the
+// pair when the pair MMAs this thread issued so far are complete.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(bar), "h"((uint16_t)3) : "memory");
+}
+
+// Arrive on the mbarrier at shared offset `bar` of the cluster CTA `rank`
+// (this CTA's own when rank is its own rank), with the default semantics. The
+// data it hands over is in tensor memory (A written, an accumulator read),
+// ordered by the tcgen05 fences on either side of the barrier; a release at
+// cluster scope here measured about 1,500 cycles per arrival on GB300.
+__device__ __forceinline__ void mbarrier_arrive_rank(uint32_t bar, uint32_t rank) {
+  asm volatile(
+      "{\n\t.reg .b32 ra;\n\t"
+      "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
+      "mbarrier.arrive.shared::cluster.b64 _, [ra];\n\t}"
+      ::"r"(bar), "r"(rank) : "memory");
+}
+
 // 32 consecutive 32-bit columns of this thread's TMEM lane -> registers.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(

@@ -395,10 +395,11 @@ int tq_probe_read_sum(const void *buf, int64_t bytes, uint32_t *out, int early, 
 /*
  * tq_debug_stall_next_launch -- test facility for the timeout path (the pages
  * have no counterpart). The next matmul kernel this library launches, from
- * any host thread and on any stream, runs with its first thread block
- * requesting none of its input copies, as if they never arrived: that block's
- * waits on them expire after wait_limit_ns (instead of the usual 2 s), it
- * sets the device status word and returns; the other blocks finish normally.
+ * any host thread and on any stream, runs with its first thread block (the
+ * first pair of blocks for the tensor-core kernel, which runs on CTA pairs)
+ * requesting none of its input copies, as if they never arrived: those
+ * blocks' waits expire after wait_limit_ns (instead of the usual 2 s), they
+ * set the device status word and return; the other blocks finish normally.
  * Its outputs are then undefined, and tq_device_status() reports
  * TQ_ERR_TIMEOUT (and clears the word). The block still waits for any copy
  * it did request before it exits, so no copy outlives it. Nothing faults and
