@@ -247,21 +247,24 @@ int tq_matmul_groupsums(const void *Wtq, const void *Xq, int32_t *S, int64_t row
 
 /*
  * tq_matmul_workspace_bytes -- scratch needed by tq_matmul_ws for this shape:
- * 0 when ntok <= 16 (the GEMV needs none); otherwise
- * ceil(ntok/64) * (cols/128) * 16384 + ceil(ntok/64) * (cols/256) * 768 bytes.
+ * 0 when ntok <= 8 (those calls run the GEMV, which needs none); otherwise,
+ * with the token tile T = 16 for ntok <= 16, 32 for ntok <= 32, else 64,
+ * ceil(ntok/T) * (cols/128) * 256*T + ceil(ntok/T) * (cols/256) * 12*T bytes.
  * -1 for a bad shape.
  */
 int64_t tq_matmul_workspace_bytes(int64_t rows, int64_t cols, int64_t ntok);
 
 /*
  * tq_matmul_ws -- tq_matmul with a caller-provided workspace, the faster form
- * for ntok >= 17 (about 1.9x on a 17408 x 5120 matrix at 9 to 130 tokens
+ * for ntok >= 9 (about 1.9x on a 17408 x 5120 matrix at 9 to 130 tokens
  * on GB300): a pre-pass converts the q8_K activations once into the
  * tensor cores' operand layout in the workspace (each int8 split exactly
  * into two e4m3 parts, instead of every 128-row tile of the weights
  * converting them again), then the tensor-core kernel reads them with one
  * bulk copy per q8_K block. Same results
- * and tolerance as tq_matmul; for ntok <= 16 it is tq_matmul.
+ * and tolerance as tq_matmul; for ntok <= 8 it is tq_matmul (the GEMV), and
+ * from 9 tokens on it runs the tensor-core kernel on token tiles of 16, 32 or
+ * 64 where tq_matmul would still run the GEMV up to 16.
  *   workspace  device buffer of at least tq_matmul_workspace_bytes(rows, cols,
  *              ntok) bytes, 16-byte aligned, owned by the caller; its contents
  *              are overwritten and meaningless after the call; it must not
@@ -282,19 +285,19 @@ int tq_matmul_groupsums_ws(const void *Wtq, const void *Xq, int32_t *S, int64_t 
 
 /*
  * tq_quantize_matmul -- tq_quantize_q8K then tq_matmul_ws in one call: Xq =
- * the q8_K blocks of X, Y = the product of Wtq and Xq. For ntok <= 16 it is one
+ * the q8_K blocks of X, Y = the product of Wtq and Xq. For ntok <= 8 it is one
  * fused launch: every CTA of the GEMV quantizes X into its shared memory
  * itself (with the quantizer's arithmetic, so Xq and Y carry the bits of the
  * two separate calls), and writes Xq (CTA 0 at its start; in the graph chains
  * tq_matmul describes, every CTA a share after its wait). That removes a launch and the
- * quantizer's place on the critical path of each matmul. For ntok >= 17 one
+ * quantizer's place on the critical path of each matmul. For ntok >= 9 one
  * kernel quantizes X (the same arithmetic), writes Xq and packs the
  * workspace, which the tensor-core kernel then reads: two launches instead
  * of three, the same bits.
  *   X  [ntok][cols] f32, 16-byte aligned (as tq_quantize_q8K).
  *   Xq [ntok][cols/256] q8_K, 16-byte aligned: written.
  *   Wtq, Y, workspace, workspace_bytes: as tq_matmul_ws (the workspace is
- *   only used for ntok >= 17).
+ *   only used for ntok >= 9).
  * Overlap: like tq_matmul after tq_quantize_q8K, the launch may start
  * reading Wtq before the kernel enqueued just before it ends when the
  * previous call this library received for the stream was the quantizer or a
@@ -342,7 +345,7 @@ int tq_matmul_host(const void *Wtq, const float *X_host, float *X, void *Xq, flo
  *   Same arguments, results and errors as tq_matmul_ws, minus the workspace.
  *   Limit: tq_matmul_workspace_bytes(rows, cols, ntok) <= TQ_STATIC_WS_BYTES,
  *   else TQ_ERR_WORKSPACE before anything runs (for example cols = 5120
- *   allows ntok <= 768; ntok <= 16 needs no workspace and has no limit).
+ *   allows ntok <= 768; ntok <= 8 needs no workspace and has no limit).
  *   Set-up: the first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current), which may also load the
  *   library's code for the array onto that device; make that first call
@@ -403,7 +406,8 @@ int tq_probe_read_sum(const void *buf, int64_t bytes, uint32_t *out, int early, 
  * Its outputs are then undefined, and tq_device_status() reports
  * TQ_ERR_TIMEOUT (and clears the word). The block still waits for any copy
  * it did request before it exits, so no copy outlives it. Nothing faults and
- * nothing waits without bound. Kernels that take it: the GEMV (ntok <= 16) and
+ * nothing waits without bound. Kernels that take it: the GEMV (ntok <= 16, or <= 8
+ * in the workspace forms) and
  * the tensor-core kernel of the workspace forms. wait_limit_ns = 0 cancels a
  * pending stall.
  * Errors: TQ_ERR_SHAPE if wait_limit_ns < 0.
