@@ -21,10 +21,21 @@
 // k whose A carries the factor 4, so every product is u * lo * 2^-9 or
 // u * 16 hi * 2^-9 exactly. Every partial sum is an integer multiple of 2^-9
 // below 2^15 in magnitude, so the accumulation is exact and the low plus high
-// columns end at sum_k u q * 2^-9. The epilogue turns u back into w = u - 1
-// with the group's activation sum from the q8_K bsums (dot(w, q) = dot(u, q) -
-// sum(q), post "the trick with 4 and 16"): isum = 2^9 * acc - sum(q), one
-// exact f32 FMA, then adds d_x * d_w * isum.
+// columns end at sum_k u q * 2^-9. Turning u back into w = u - 1 takes the
+// group's activation sum from the q8_K bsums (dot(w, q) = dot(u, q) - sum(q),
+// post "the trick with 4 and 16"), in one of two exact ways:
+//   - a fifth MMA per group (64-token tiles on single CTAs): B holds the
+//     sum's four base-16 digits d0..d3 (d0..d2 in [0, 15], d3 in [-4, 3], all
+//     exact in e4m3) at k = 0..3 of each token's low row, A the constants
+//     -2^-9 * 16^i, so the accumulator ends at isum * 2^-9 and the epilogue
+//     only scales it;
+//   - in the epilogue (16- and 32-token tiles, CTA pairs): isum =
+//     2^9 * acc - sum(q), one exact f32 FMA per output.
+// Both give the same bits. Measured on GB300 (17408 x 5120): at 64 tokens
+// the MMA is the cheaper place, 21.1 against 22.5 us, because each epilogue
+// warp then handles 32 tokens per group and the epilogue warps share their
+// sub-partitions with the MMA-issuing thread; at 16 and 32 tokens the extra
+// MMA costs more (17.5 against 16.1 us, 18.6 against 17.9 us).
 //
 // Per CTA (128 weight rows x 64 tokens) the work goes one q8_K block (two
 // 128-weight groups) at a time:
@@ -36,13 +47,15 @@
 //     into tensor memory (tcgen05.st), 64 weights per thread and group;
 //   - one thread issues per group 4 tcgen05.mma (K = 32 each) with A in
 //     tensor memory and B read from the staged slot into one accumulator of
-//     128 columns per group, and one commit;
-//   - 8 epilogue warps tcgen05.ld each accumulator and add
-//     d_x * d_w * (2^9 (acc_lo + acc_hi) - sum(q)) in packed f32x2 arithmetic.
+//     128 columns per group, plus the digit MMA, and one commit;
+//   - epilogue warps, four per 32 tokens of the tile (four of 16 tokens at
+//     N = 16), tcgen05.ld each accumulator and add d_x * d_w * isum in
+//     packed f32x2 arithmetic.
 // The A operands and the accumulators form one ring of three group stages
-// (3 x 128 accumulator and 3 x 32 A columns of tensor memory). The MMAs of
-// group g wait on a single barrier: the converters have written A(g) and the
-// epilogue has read the accumulator of g - 3. One commit per group tells both
+// (3 x 128 accumulator and 3 x 32 A columns of tensor memory; the digit
+// tiles form the same ring in shared memory). The MMAs of group g wait on a
+// single barrier: the converters have written A(g) and the digits of g, and
+// the epilogue has read the accumulator of g - 3. One commit per group tells both
 // the epilogue (accumulator g is complete) and the converters (A stage g is
 // free again). Measured on GB300 with clock stamps, the issuing thread sets
 // the pace: each commit and each wait costs it more than an MMA does, so the
@@ -59,7 +72,23 @@ constexpr int kK = 32;             // UMMA K of kind::f8f6f4
 constexpr int kGPB = kQK / kGroup;     // groups per q8_K block (2)
 constexpr int kMmaPerGroup = kGroup / kK;   // 4
 constexpr int kConvWarps = 8;    // converters: warp w -> rows 32*(w%4).., k half w/4
-constexpr int kEpiTok = 16;      // tokens per epilogue warp
+// Tokens per epilogue warp, by token tile, and whether the activation sums
+// enter through the digit MMA (1) or the epilogue (0) (compile-time tuning).
+#ifndef TQ_TC_EPI_TOK_64
+#define TQ_TC_EPI_TOK_64 32
+#endif
+#ifndef TQ_TC_SUM_MMA_64
+#define TQ_TC_SUM_MMA_64 1
+#endif
+#ifndef TQ_TC_SUM_MMA_32
+#define TQ_TC_SUM_MMA_32 0
+#endif
+#ifndef TQ_TC_SUM_MMA_16
+#define TQ_TC_SUM_MMA_16 0
+#endif
+#ifndef TQ_TC_EPI_TOK_32
+#define TQ_TC_EPI_TOK_32 32
+#endif
 constexpr int kTilesPerCta = kM / kTileRows;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kACols = kGroup / 4;              // 32 per group: four e4m3 per column
@@ -72,6 +101,13 @@ constexpr uint32_t kAccCol = 0;                      // accumulator stage s: s *
 constexpr uint32_t kLBO = 128;
 constexpr uint32_t kSBO = 8 * 128;
 constexpr float kProdScale = 512.0f;                   // products carry 2^-9
+// The digit MMA: B per group stage is 2N rows x 32 k (K-major, no swizzle:
+// LBO = 128 for the next 16 k, SBO = 256 for the next 8 rows), the digits of
+// token n at k = 0..3 of row n, zeros elsewhere; A is one word per row of
+// tensor memory, e4m3 -2^-9, -2^-5, -2^-1, -2^3 at k = 0..3.
+constexpr uint32_t kSBOs = 2 * 128;
+constexpr uint32_t kASumWord = 0xD0B09081u;
+constexpr uint32_t kASumCols = 16;                     // one 16-column store per lane quarter
 constexpr int kWRun = kGPB * kTileBytes;               // one 32-row tile, both groups
 constexpr int kInB = 0;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -86,8 +122,11 @@ struct TcCfg {
   static_assert(CG == 1 || CG == 2, "CTAs per MMA");
   static constexpr int kN = N;                         // tokens per CTA
   static constexpr int kNB = 2 * N;                    // UMMA N: low and high parts
-  // A + accumulator ring in tensor memory, one group per stage
-  static constexpr int kStages = (int)(kTmemCols / (kNB + kACols));
+  static constexpr bool kSumMma =
+      CG == 1 && (N == 64 ? TQ_TC_SUM_MMA_64 : N == 32 ? TQ_TC_SUM_MMA_32 : TQ_TC_SUM_MMA_16) != 0;
+  // A + accumulator ring in tensor memory, one group per stage (after it the
+  // digit MMA's constant A)
+  static constexpr int kStages = (int)((kTmemCols - (kSumMma ? kASumCols : 0u)) / (kNB + kACols));
   // d_w, d_x and the group sums per block, written by the converters and
   // read by the epilogue. A converter writing block b has seen the MMAs of
   // group 2b - kStages finish, which were issued after the epilogue released
@@ -97,16 +136,21 @@ struct TcCfg {
   static constexpr int kInStages = N == 64 ? 3 : N == 32 ? 4 : 6;   // staged-input ring
   // epilogue: warp w -> rows 32*(w%4).., tokens kEpiTok*(w/4).. (a warp reaches
   // only the tensor-memory lanes of its warp index mod 4)
+  static constexpr int kEpiTok = N == 64 ? TQ_TC_EPI_TOK_64 : N == 32 ? TQ_TC_EPI_TOK_32 : 16;
+  static_assert(kEpiTok % 16 == 0 && N % kEpiTok == 0, "epilogue width");
   static constexpr int kEpiWarps = 4 * (N / kEpiTok);
   static constexpr int kMmaWarp = kConvWarps + kEpiWarps;
   static constexpr int kProdWarp = kMmaWarp + 1;
   static constexpr int kThreads = (kProdWarp + 1) * 32;
   static constexpr uint32_t kAccCols = kNB;
   static constexpr uint32_t kACol = kStages * kAccCols;   // A stage s: kACol + s * 32
-  static_assert(kACol + kStages * kACols <= kTmemCols, "tensor memory overflow");
+  static constexpr uint32_t kASumCol = kACol + kStages * kACols;
+  static_assert(kASumCol + (kSumMma ? kASumCols : 0u) <= kTmemCols, "tensor memory overflow");
+  static constexpr int kBSumBytes = kSumMma ? kNB * kK : 0;   // digit tile per group stage
   static constexpr int kBTile = kNB * kGroup;
-  // per (token tile, block): d_x of N tokens (f32), then per group minus each
-  // token's activation sum (an integer of magnitude at most 16256, exact in f32)
+  // per (token tile, block): d_x of N tokens (f32), then per group each
+  // token's activation sum: its four e4m3 digits as one word for the digit
+  // MMA, else minus the sum as f32 (magnitude at most 16384, exact)
   static constexpr int kSumOff = N;                    // floats
   static constexpr int kDxFloats = N + kGPB * N;
   static constexpr int kDxBytes = kDxFloats * 4;
@@ -119,12 +163,12 @@ struct TcCfg {
   static constexpr int kInBytes = kInDx + kDxBytes;
   static_assert(kInBytes % 16 == 0 && kWRun % 16 == 0 && kInW % 16 == 0 && kDxBytes % 16 == 0,
                 "bulk copies need 16-byte multiples");
-  // scale ring stage: d_w per group and row, then the block's record (d_x and
-  // minus the sums of each group)
-  static constexpr int kScaleFloats = kGPB * kM + kDxFloats;
+  // scale ring stage: d_w per group and row (times 2^9 with the digit MMA),
+  // then d_x of the block (and minus the sums of each group without it)
+  static constexpr int kScaleFloats = kGPB * kM + (kSumMma ? N : kDxFloats);
   static constexpr int kNumBars = 2 * kInStages + 2 * kStages + 1;   // + the failure drain
-  static constexpr int kSmemUsed = kInStages * kInBytes + kScaleStages * kScaleFloats * 4 +
-                                   kNumBars * 8 + 16;
+  static constexpr int kSmemUsed = kInStages * kInBytes + kStages * kBSumBytes +
+                                   kScaleStages * kScaleFloats * 4 + kNumBars * 8 + 16;
   // Enough shared memory that only one CTA fits on an SM: each CTA allocates
   // all 512 tensor-memory columns.
   static constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
@@ -144,6 +188,10 @@ struct TcCfg {
   constexpr int kScaleStages = Cfg_::kScaleStages;                          \
   constexpr int kInStages = Cfg_::kInStages;                                \
   constexpr int kEpiWarps = Cfg_::kEpiWarps;                                \
+  constexpr int kEpiTok = Cfg_::kEpiTok;                                    \
+  constexpr bool kSumMma = Cfg_::kSumMma;                                   \
+  constexpr uint32_t kASumCol = Cfg_::kASumCol;                             \
+  constexpr int kBSumBytes = Cfg_::kBSumBytes;                              \
   constexpr int kMmaWarp = Cfg_::kMmaWarp;                                  \
   constexpr int kProdWarp = Cfg_::kProdWarp;                                \
   constexpr int kThreads = Cfg_::kThreads;                                  \
@@ -159,7 +207,7 @@ struct TcCfg {
   constexpr int kScaleFloats = Cfg_::kScaleFloats;                          \
   constexpr uint32_t kIdesc = Cfg_::kIdesc;                                 \
   (void)kN; (void)kNB; (void)kStages; (void)kScaleStages; (void)kInStages;  \
-  (void)kEpiWarps; (void)kMmaWarp; (void)kProdWarp; (void)kThreads;          \
+  (void)kEpiWarps; (void)kEpiTok; (void)kSumMma; (void)kASumCol; (void)kBSumBytes; (void)kMmaWarp; (void)kProdWarp; (void)kThreads;          \
   (void)kAccCols; (void)kACol; (void)kBTile; (void)kSumOff; (void)kDxFloats; \
   (void)kDxBytes; (void)kInW; (void)kInDx; (void)kInBytes; (void)kScaleFloats; \
   (void)kIdesc
@@ -181,16 +229,29 @@ __host__ __device__ inline Layout ws_layout(int64_t cols, int64_t ntok) {
 
 // ---------------------------------------------------------------- pre-pass
 
+// A group's activation sum as the four e4m3 digits the digit MMA reads:
+// sq = d0 + 16 d1 + 256 d2 + 4096 d3, d0..d2 in [0, 15], d3 in [-4, 3].
+__device__ __forceinline__ uint32_t sum_digits(int sq) {
+  return e4m3x2((float)(sq & 15), (float)((sq >> 4) & 15)) |
+         (e4m3x2((float)((sq >> 8) & 15), (float)(sq >> 12)) << 16);
+}
+
+// The record word of a token's group sum (see TcCfg::kDxFloats).
+template <bool kSumMma>
+__device__ __forceinline__ uint32_t sum_word(int sq) {
+  return kSumMma ? sum_digits(sq) : __float_as_uint((float)(-sq));
+}
+
 // One CTA of 4N threads per (group g, token tile): thread t takes token t % N
 // and k quarter t / N (32 activations) and writes two 16-byte core-matrix rows
 // of the low part and two of the high part; the k-quarter-0 threads also
-// write minus the token's group sum and (for even g) its block scale.
-template <int N>
+// write the token's group sum word and (for even g) its block scale.
+template <int N, int CG>
 __global__ void __launch_bounds__(4 * N) act_pack_kernel(const uint8_t* __restrict__ Xq,
                                                          uint8_t* __restrict__ Bt,
                                                          float* __restrict__ Dx, int64_t ntok,
                                                          int ngroups, int nblk) {
-  TQ_TC_CFG(N);
+  TQ_TC_CFG2(N, CG);
   pdl_launch_dependents();
   pdl_wait_primary();   // the q8_K activations come from the previous kernel
   const int g = blockIdx.x;
@@ -234,7 +295,7 @@ __global__ void __launch_bounds__(4 * N) act_pack_kernel(const uint8_t* __restri
   }
   if (kq == 0) {
     float* rec = Dx + (nt * nblk + (g >> 1)) * kDxFloats;
-    rec[kSumOff + (g & 1) * kN + n] = (float)(-sq);
+    reinterpret_cast<uint32_t*>(rec)[kSumOff + (g & 1) * kN + n] = sum_word<kSumMma>(sq);
     if ((g & 1) == 0) rec[n] = d;
   }
 }
@@ -242,17 +303,17 @@ __global__ void __launch_bounds__(4 * N) act_pack_kernel(const uint8_t* __restri
 // Fused form of the quantizer and the pre-pass (tq_quantize_matmul): one warp
 // per (token slot, q8_K block) quantizes the f32 activations exactly as the
 // quantizer kernel does (q8K_warp), writes the q8_K block, and writes the
-// token's e4m3 rows of both groups' B tiles, minus the group sums and the
+// token's e4m3 rows of both groups' B tiles, the group sum words and the
 // block scale. Token slots past ntok (the last tile's padding) get zeros.
 // Lane l holds values 8l .. 8l + 7: group l / 16, k = 8 (l % 16) .. + 7 of it,
 // bit 2 of k clear for the first four and set for the last four.
 constexpr int kPackWarps = 8;
 
-template <int N>
+template <int N, int CG>
 __global__ void __launch_bounds__(kPackWarps * 32) quantize_pack_kernel(
     const float* __restrict__ X, uint8_t* __restrict__ Xq, uint8_t* __restrict__ Bt,
     float* __restrict__ Dx, int64_t ntok, int ngroups, int nblk, int64_t nslots) {
-  TQ_TC_CFG(N);
+  TQ_TC_CFG2(N, CG);
   pdl_launch_dependents();
   // the workspace and Xq may still be read by the previous kernel in the stream
   pdl_wait_primary();
@@ -285,7 +346,7 @@ __global__ void __launch_bounds__(kPackWarps * 32) quantize_pack_kernel(
   *reinterpret_cast<uint2*>(tile + (n >> 3) * kSBO + (n & 7) * 16 + off) = make_uint2(l0, l1);
   *reinterpret_cast<uint2*>(tile + ((kN + n) >> 3) * kSBO + (n & 7) * 16 + off) = make_uint2(h0, h1);
   float* rec = Dx + (nt * nblk + b) * kDxFloats;
-  if ((lane & 15) == 0) rec[kSumOff + gi * kN + n] = (float)(-sq);
+  if ((lane & 15) == 0) reinterpret_cast<uint32_t*>(rec)[kSumOff + gi * kN + n] = sum_word<kSumMma>(sq);
   if (lane == 0) rec[n] = d;
 }
 
@@ -335,21 +396,27 @@ __global__ void __launch_bounds__(TcCfg<N, CG>::kThreads, 1) gemm_tc_ws_kernel(c
   TQ_TC_CFG2(N, CG);
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sIn = smem;                                                         // [in][slot]
-  float* sScale = reinterpret_cast<float*>(smem + kInStages * kInBytes);       // [scale][448]
+  uint8_t* sBSum = smem + kInStages * kInBytes;                                // [stage][digits]
+  float* sScale = reinterpret_cast<float*>(sBSum + kStages * kBSumBytes);      // [scale]
   uint64_t* in_full = reinterpret_cast<uint64_t*>(sScale + kScaleStages * kScaleFloats);  // [in]
   uint64_t* in_empty = in_full + kInStages;                                    // [in]
   // mma_ready[s]: the MMAs of group g (stage s = g % 3) may go: the converters
-  // have written A(g), and the epilogue has read the accumulator of g - 3
-  // (the epilogue pre-arrives for groups 0..2).
+  // have written A(g) (and its digits), and the epilogue has read the
+  // accumulator of g - 3 (the epilogue pre-arrives for groups 0..2).
   uint64_t* mma_ready = in_empty + kInStages;                                  // [stage]
   // mma_done[s]: the MMAs of group g are complete: its accumulator is ready
-  // for the epilogue, and A stage s is free for the converters' group g + 3.
+  // for the epilogue, and A (and digit) stage s is free for the converters'
+  // group g + 3.
   uint64_t* mma_done = mma_ready + kStages;                                    // [stage]
   uint64_t* drain_bar = mma_done + kStages;   // after a failure: the MMAs issued are done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
-  // Set by a role that gave up a wait (before its next arrival): the producer
-  // then requests no more input, so a slot is never refilled while a copy into
-  // it may still be in flight.
+  // Set by a converter warp that gave up waiting for a slot's copy, before its
+  // arrival on the slot's in_empty: the producer then requests no more input.
+  // A slot is freed only once every converter has arrived on it (each after
+  // seeing the copy land or after setting this flag) and the MMAs that read
+  // it are complete, so a slot is never refilled while a copy into it may
+  // still be in flight. (The MMA thread sets nothing here: a store on its
+  // failure branch made the kernel up to 8 percent slower.)
   volatile int* s_failed = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -386,12 +453,30 @@ __global__ void __launch_bounds__(TcCfg<N, CG>::kThreads, 1) gemm_tc_ws_kernel(c
     *s_failed = 0;
     mbarrier_init_fence();
   }
+  if (kSumMma) {
+    // the digit tiles are zero outside k = 0..3 of rows 0..N-1
+    for (int i = tid; i < kStages * kBSumBytes / 16; i += kThreads)
+      reinterpret_cast<uint4*>(sBSum)[i] = make_uint4(0u, 0u, 0u, 0u);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
   tc_fence_before();
   __syncthreads();
   if (CG == 2) cluster_sync();   // the peer's barriers are initialized before any arrival
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool failed = false;
+  if (kSumMma) {   // the digit MMA's constant A, one warp per lane quarter
+    if (warp < 4) {
+      uint32_t r[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) r[j] = j == 0 ? kASumWord : 0u;
+      tmem_st16(tmem + ((uint32_t)(warp * 32) << 16) + kASumCol, r);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
 
   if (warp == kProdWarp) {
     // ---------------- producer: stage block j into slot j % kInStages
@@ -483,14 +568,21 @@ __global__ void __launch_bounds__(TcCfg<N, CG>::kThreads, 1) gemm_tc_ws_kernel(c
         tc_fence_after();
         if (!failed) {
           convert_store(cw[gi], a_base + (uint32_t)sa * kACols);
+          if (kSumMma && ct >= kSumOff + gi * kN && ct < kSumOff + (gi + 1) * kN) {
+            const int n = ct - kSumOff - gi * kN;   // this group's digits of token n
+            *reinterpret_cast<uint32_t*>(sBSum + sa * kBSumBytes + (n >> 3) * kSBOs + (n & 7) * 16) =
+                rec;
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          }
           if (gi == 0) {
             float* sst = sScale + ss * kScaleFloats;
             if (khalf == 0) {
 #pragma unroll
               for (int gj = 0; gj < kGPB; ++gj)
-                sst[gj * kM + q4 * 32 + lane] = __half2float(__ushort_as_half((unsigned short)sc[gj]));
+                sst[gj * kM + q4 * 32 + lane] = __half2float(__ushort_as_half((unsigned short)sc[gj])) *
+                                                (kSumMma ? kProdScale : 1.0f);
             }
-            if (ct < kDxFloats) sst[kGPB * kM + ct] = __uint_as_float(rec);
+            if (ct < (kSumMma ? kN : kDxFloats)) sst[kGPB * kM + ct] = __uint_as_float(rec);
           }
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         }
@@ -547,14 +639,16 @@ __global__ void __launch_bounds__(TcCfg<N, CG>::kThreads, 1) gemm_tc_ws_kernel(c
 #pragma unroll
             for (int j4 = 0; j4 < 4; ++j4) {
               const float4 d = dx4[h * 4 + j4];
-              const float4 m = nsq4[h * 4 + j4];          // minus the tokens' sums
+              const float4 m = kSumMma ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                       : nsq4[h * 4 + j4];          // minus the tokens' sums
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
                 const int j = 4 * j4 + 2 * e;             // token pair n0 + 16h + j, +1
-                const uint64_t z = f2_add(f2_pack(lo[j], lo[j + 1]),
-                                          f2_pack(hi[j], hi[j + 1]));   // sum u q * 2^-9
+                // sum u q * 2^-9, or with the digit MMA isum * 2^-9 (exact)
+                const uint64_t z = f2_add(f2_pack(lo[j], lo[j + 1]), f2_pack(hi[j], hi[j + 1]));
                 const uint64_t nsq = e == 0 ? f2_packf(m.x, m.y) : f2_packf(m.z, m.w);
-                const uint64_t is = f2_fma(z, k512, nsq);                      // isum, exact
+                // isum (exact); with the digit MMA d_w carries the 2^9 instead
+                const uint64_t is = kSumMma ? (kGroupSums ? f2_mul(z, k512) : z) : f2_fma(z, k512, nsq);
                 if (kGroupSums) {
                   if (row < a.rows) {
                     const float2 ii = f2_unpack(is);
@@ -599,15 +693,13 @@ __global__ void __launch_bounds__(TcCfg<N, CG>::kThreads, 1) gemm_tc_ws_kernel(c
       // Descriptor of this slot's B, once: the start address field (bits 0-13,
       // address >> 4) then advances by plain adds, as no address passes 2^18.
       const uint64_t bd0 = smem_desc(smem_u32(sIn + i * kInBytes + kInB), kLBO, kSBO);
+      const uint64_t sd0 = smem_desc(smem_u32(sBSum), kLBO, kSBOs);
 #pragma unroll
       for (int gi = 0; gi < kGPB; ++gi) {
         // A(g) written and the accumulator of group g - 3 read
         const bool ok = failed || mbarrier_test_wait(smem_u32(mma_ready + sa), pa) ||
                         mbarrier_wait_bounded(smem_u32(mma_ready + sa), pa, lim);
-        if (!ok) {
-          failed = true;
-          *s_failed = 1;
-        }
+        if (!ok) failed = true;
         tc_fence_after();
         if (!failed) {
           const uint32_t d = tmem + kAccCol + (uint32_t)sa * kAccCols;
@@ -620,6 +712,8 @@ __global__ void __launch_bounds__(TcCfg<N, CG>::kThreads, 1) gemm_tc_ws_kernel(c
             else
               mma_e4m3_tmem_a_pair(d, at + (uint32_t)(kK / 4) * kk, bd, kIdesc, kk > 0 ? 1u : 0u);
           }
+          if (kSumMma)   // minus the activation sums: the accumulator ends at isum * 2^-9
+            mma_e4m3_tmem_a(d, tmem + kASumCol, sd0 + (uint64_t)((sa * kBSumBytes) >> 4), kIdesc, 1u);
         }
         // the commit fires when these MMAs are done (at once if none were issued)
         if (CG == 1) mma_commit(smem_u32(mma_done + sa));
@@ -685,12 +779,13 @@ int64_t tc_workspace_bytes(int64_t cols, int64_t ntok) {
 namespace {
 
 // CTAs per MMA: 2 runs the kernel on clusters of two CTAs whose MMAs span
-// both (twice the rows per MMA instruction, half of B staged by each CTA).
-// Measured on GB300 (17408 x 5120): 25.5 / 20.7 / 18.7 us at 64 / 32 / 16
-// tokens against 23.6 / 19.3 / 17.5 us for single CTAs, with identical
-// results: the issuing thread then waits on the MMAs themselves (about 150
-// cycles per 256-row MMA), so the halved instruction count does not pay for
-// the cross-CTA hand-offs. Off by default; building with TQ_TC_PAIR=1 selects it.
+// both (twice the rows per MMA instruction, half of B staged by each CTA;
+// the activation sums then enter in the epilogue). Measured on GB300
+// (17408 x 5120): 24.8 / 19.0 / 17.4 us at 64 / 32 / 16 tokens against
+// 21.1 / 17.7 / 16.1 us for single CTAs, with identical results: the issuing
+// thread then waits on the MMAs themselves (about 150 cycles per 256-row
+// MMA), so the halved instruction count does not pay for the cross-CTA
+// hand-offs. Off by default; building with TQ_TC_PAIR=1 selects it.
 #ifndef TQ_TC_PAIR
 #define TQ_TC_PAIR 0
 #endif
@@ -748,7 +843,7 @@ cudaError_t launch_ws(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t* 
   const Layout l = ws_layout<N>(cols, ntok);
   const int G = (int)(cols / kGroup), nblk = (int)(cols / kQK);
   if (l.ntile > 65535) return cudaErrorInvalidConfiguration;
-  cudaError_t e = launch_pdl(act_pack_kernel<N>, dim3((unsigned)G, (unsigned)l.ntile),
+  cudaError_t e = launch_pdl(act_pack_kernel<N, kCtasPerMma>, dim3((unsigned)G, (unsigned)l.ntile),
                              dim3(4 * N), 0, s, Xq, ws, reinterpret_cast<float*>(ws + l.b_bytes),
                              ntok, G, nblk);
   if (e != cudaSuccess) return e;
@@ -765,7 +860,7 @@ cudaError_t launch_quantize_ws(const float* X, uint8_t* Xq, const uint8_t* Wtq, 
   const int64_t warps = l.ntile * N * nblk;
   const int64_t grid = (warps + kPackWarps - 1) / kPackWarps;
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  cudaError_t e = launch_pdl(quantize_pack_kernel<N>, dim3((unsigned)grid), dim3(kPackWarps * 32),
+  cudaError_t e = launch_pdl(quantize_pack_kernel<N, kCtasPerMma>, dim3((unsigned)grid), dim3(kPackWarps * 32),
                              0, s, X, Xq, ws, reinterpret_cast<float*>(ws + l.b_bytes), ntok,
                              (int)(cols / kGroup), nblk, l.ntile * N);
   if (e != cudaSuccess) return e;
