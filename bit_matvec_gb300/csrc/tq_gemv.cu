@@ -976,8 +976,9 @@ cudaError_t launch_mma(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
   per_sm = max(1, min(per_sm, TQ_GEMV_CTAS_PER_SM));
   int grid = (int)std::min<int64_t>(a.nrb, (int64_t)nsm * per_sm);
 #if TQ_GEMV_EVEN_GRID
-  for (int g = grid; g >= grid - grid / 4 && g >= 1; --g)
-    if (a.nrb % g == 0) { grid = g; break; }
+  if (a.defer)   // as in launch_t
+    for (int g = grid; g >= grid - grid / 4 && g >= 1; --g)
+      if (a.nrb % g == 0) { grid = g; break; }
 #endif
   a.defer = defer_wait(a, G, grid, MmaCfg<T, TPW>::kStageTiles, false);
   take_stall(a);
@@ -1007,10 +1008,19 @@ cudaError_t launch_t(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
   per_sm = max(1, min(per_sm, TQ_GEMV_CTAS_PER_SM));
   int grid = (int)std::min<int64_t>(a.nrb, (int64_t)nsm * per_sm);
 #if TQ_GEMV_EVEN_GRID
-  // Prefer a grid that splits the tile columns evenly (every CTA the same
-  // work), if one exists within the top quarter of the resident capacity.
-  for (int g = grid; g >= grid - grid / 4 && g >= 1; --g)
-    if (a.nrb % g == 0) { grid = g; break; }
+  // A launch that may read its inputs before the kernel ahead of it ends
+  // (a.defer: the host showed they are final) starts its CTAs staggered, as
+  // that kernel's CTAs leave: there a grid that splits the tile columns
+  // evenly (every CTA the same work), if one exists within the top quarter of
+  // the resident capacity, measured faster. A launch that waits for that
+  // kernel first starts all its CTAs together, and the SM with the most work
+  // sets the pace: there the grid fills every resident slot (uneven columns
+  // per CTA, but less on the busiest SM). Measured on GB300 at one token:
+  // 32768 x 8192 14.07 -> 13.68 us waiting first (12.49 -> 12.90 us with
+  // early reads), 17408 x 5120 7.07 -> 6.70 (6.11 -> 6.96).
+  if (a.defer)
+    for (int g = grid; g >= grid - grid / 4 && g >= 1; --g)
+      if (a.nrb % g == 0) { grid = g; break; }
 #endif
   a.defer = defer_wait(a, G, grid, Cfg<T>::kStageTiles, true);
   take_stall(a);
