@@ -308,7 +308,39 @@ class ReplayWorkload:
                                  for m in self.mats)
 
 
-def measure_replay(ntok, steps, warmup, world, device, peaks, peak_kind):
+def replay_read_ceiling(wl, steps, warmup, stream):
+    """The same step's weight reads by the read-ceiling probe instead of the
+    matmuls: one tq_probe_read_sum launch per matrix and block, in the step's
+    order, each allowed to read before the one ahead of it ends (as the
+    replay's GEMVs do), from one CUDA graph. The most any kernel that reads
+    each matrix once per launch can expect."""
+    import torch
+    import bit_matvec_gb300 as tq
+    out = torch.zeros(1, dtype=torch.int32, device=wl.device)
+
+    def probe_step():
+        for b in range(wl.blocks):
+            for m in wl.mats:
+                tq.tq_probe_read_sum(m["W"][b], out, True, stream)
+
+    probe_step()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        probe_step()
+    for _ in range(max(warmup, 3)):
+        g.replay()
+    stream.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        g.replay()
+    end.record(stream)
+    stream.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+def measure_replay(ntok, steps, warmup, world, device, peaks, peak_kind, read_ceiling=False):
     """Device time of whole replay steps from one CUDA graph per step."""
     import torch
     wl = ReplayWorkload(ntok, device)
@@ -331,6 +363,7 @@ def measure_replay(ntok, steps, warmup, world, device, peaks, peak_kind):
         end.record(stream)
         stream.synchronize()
         ms = max_over_ranks(start.elapsed_time(end) / steps, world, device)
+        rc_ms = replay_read_ceiling(wl, steps, warmup, stream) if read_ceiling else None
     res = {"workload": f"decode-step replay, {wl.blocks} blocks x 5 matrices, ntok={ntok}",
            "ntok": ntok, "ms_per_step": ms, "steps": steps, "launches_per_step": wl.launches(),
            "weights_per_step": wl.weights(), "weight_bytes_per_step": wl.weight_bytes(),
@@ -343,6 +376,14 @@ def measure_replay(ntok, steps, warmup, world, device, peaks, peak_kind):
                            "frac": achieved / peak, "peak_source": peak_kind,
                            "frac_of_nominal": achieved / HBM_NOMINAL_GBS,
                            "note": "whole step (quantize + matmul launches) over algorithmic bytes"}
+        if rc_ms is not None:
+            wb = wl.weight_bytes()
+            res["read_ceiling"] = {
+                "ms_per_step": rc_ms, "bytes": wb, "gbs": wb / (rc_ms * 1e-3) / 1e9,
+                "frac": wb / (rc_ms * 1e-3) / 1e9 / peak,
+                "replay_vs_ceiling": rc_ms / ms,
+                "how": "tq_probe_read_sum over the same weight buffers, one launch per matrix "
+                       "and block in the step's order, reading early, one CUDA graph"}
     else:
         res["gmac_per_s"] = world * wl.weights() * ntok / (ms * 1e-3) / 1e9
         achieved = 2.0 * wl.weights() * ntok / (ms * 1e-3) / 1e12
@@ -937,7 +978,7 @@ def main():
     if not args.no_replay:
         for ntok, rsteps in ((1, 30), (512, 3)):
             r = measure_replay(ntok, rsteps, args.warmup // 100 + 1, world, device, peaks,
-                               peak_kind)
+                               peak_kind, read_ceiling=ntok == 1 and not args.no_read_ceiling)
             if want_cpu:
                 r["cpu_baseline"] = cpu_baseline_entry(*oracle_replay_rate(ntok, 5.0))
             extra[f"replay_ntok{ntok}"] = r
