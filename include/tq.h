@@ -162,7 +162,7 @@ int tq_repack_ptq1_0(const void *Wpt, void *Wtq, int64_t rows, int64_t cols, voi
  * words the pq2_0 path uses, and the activations are staged in the matching
  * order, so the dot product is the same AND-per-slot dp4a. Measured on GB300
  * with one token on the 32768 x 8192 decode matrix it takes 30.6 us per
- * launch against 12.6 us for the 2-bit stream of the same weights: the
+ * launch against 12.8 us for the 2-bit stream of the same weights: the
  * decode costs about 2.5 times the 2-bit unpack's instructions, more than the
  * 18% fewer bytes save. As on the CPU, the file is therefore decoded once at
  * load (tq_repack_ptq1_0) for the product path; this form is kept so that the
