@@ -49,14 +49,17 @@ def _bits(t):
 
 @pytest.mark.parametrize("rows,cols,ntok", [(ROWS, 1024, 1), (ROWS, 1024, 3), (ROWS, 1024, 4),
                                              (ROWS, 1024, 8), (5120, 17408, 1), (5120, 17408, 3),
-                                             (5120, 17408, 4)])
+                                             (5120, 17408, 4), (32768, 1024, 1), (32768, 1024, 4)])
 def test_graph_chain_of_independent_calls(rows, cols, ntok):
     """Four fused calls and two tq_matmul calls, each on its own weights, all
     reading activations no call of the chain writes (the fused calls share
     one q8_K output buffer): the early-read form runs from the second call on.
     With 1024 columns every CTA has several tile columns and waits after its
     first; 5120 x 17408 gives one long tile column per CTA, and the one- and
-    three-token kernels wait after its first ring stage."""
+    three-token kernels wait after its first ring stage. With 32768 rows (1024
+    tile columns) the calls made one at a time, which wait first, fill every
+    resident slot with uneven tile columns per CTA, while the chain splits
+    them evenly over fewer CTAs: the bits must not change."""
     import bit_matvec_gb300 as tq
     n = 4
     wpq = [synth.pq2_0_weights(rows, cols, 40 + i) for i in range(n + 2)]
