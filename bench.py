@@ -813,9 +813,11 @@ def run_reference(args, rank, world):
 
 def code_text(src: str) -> str:
     """C/CUDA source without its comments (no string literal in the kernel
-    sources holds a comment marker): what the compiler sees of it."""
+    sources holds a comment marker) and without the lines left empty: what
+    the compiler sees of it, unchanged by adding or removing comment lines."""
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return re.sub(r"//[^\n]*", "", src)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(ln.rstrip() for ln in src.splitlines() if ln.strip())
 
 
 def kernel_source_sha(files):

@@ -1015,9 +1015,10 @@ cudaError_t launch_t(const GemvArgs& a0, int64_t cols, cudaStream_t s) {
   // the resident capacity, measured faster. A launch that waits for that
   // kernel first starts all its CTAs together, and the SM with the most work
   // sets the pace: there the grid fills every resident slot (uneven columns
-  // per CTA, but less on the busiest SM). Measured on GB300 at one token:
-  // 32768 x 8192 14.07 -> 13.68 us waiting first (12.49 -> 12.90 us with
-  // early reads), 17408 x 5120 7.07 -> 6.70 (6.11 -> 6.96).
+  // per CTA, but less on the busiest SM). Measured on GB300 at one token, the
+  // full grid against the even split: waiting first 14.07 -> 13.68 us on
+  // 32768 x 8192 and 7.07 -> 6.70 on 17408 x 5120; reading early 12.49 ->
+  // 12.90 and 6.11 -> 6.96 (so launches that read early keep the even split).
   if (a.defer)
     for (int g = grid; g >= grid - grid / 4 && g >= 1; --g)
       if (a.nrb % g == 0) { grid = g; break; }

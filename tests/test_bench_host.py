@@ -126,3 +126,5 @@ def test_source_hash_ignores_comments():
     assert bench.code_text(a) == bench.code_text(b)
     assert bench.code_text(a) != bench.code_text(c)
     assert "return x;" in bench.code_text(a) and "one" not in bench.code_text(a)
+    # a comment line added or removed changes nothing either
+    assert bench.code_text("int f();\n// added\nint g();\n") == bench.code_text("int f();\nint g();\n")
