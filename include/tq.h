@@ -256,8 +256,9 @@ int64_t tq_matmul_workspace_bytes(int64_t rows, int64_t cols, int64_t ntok);
 
 /*
  * tq_matmul_ws -- tq_matmul with a caller-provided workspace, the faster form
- * for ntok >= 9 (about 1.9x on a 17408 x 5120 matrix at 9 to 130 tokens
- * on GB300): a pre-pass converts the q8_K activations once into the
+ * for ntok >= 9 (measured on GB300 on a 17408 x 5120 matrix: 1.25-1.4x at 9
+ * to 16 tokens, where tq_matmul runs the GEMV; 1.8-2.2x from 17 to 130
+ * tokens): a pre-pass converts the q8_K activations once into the
  * tensor cores' operand layout in the workspace (each int8 split exactly
  * into two e4m3 parts, instead of every 128-row tile of the weights
  * converting them again), then the tensor-core kernel reads them with one
