@@ -65,10 +65,29 @@ def mma_flops_per_flop(ntok: int) -> float:
     return (2.5 if tile == 64 else 2.0) * padded / ntok
 
 # Token counts the workspace forms (every call the benchmark makes) run as a
-# GEMV: one weight pass, one fused launch; above, two launches (quantize and
-# pack, then the tensor-core kernel). The forms without a workspace run the
-# GEMV up to 16 tokens.
+# GEMV, one weight pass: one fused launch, or from 4 tokens, where the
+# workspace size is not 0 (3072 to 19968 columns), two (one kernel quantizes
+# and stages the activations in the workspace, then the GEMV); above, two
+# launches too (quantize and pack, then the tensor-core kernel). The forms
+# without a workspace run the GEMV up to 16 tokens.
 GEMV_MAX_TOKENS = 8
+
+
+def staged(rows: int, cols: int, ntok: int) -> bool:
+    import bit_matvec_gb300 as tq
+    return ntok <= GEMV_MAX_TOKENS and tq.tq_matmul_workspace_bytes(rows, cols, ntok) > 0
+
+
+def launches_per_matmul(rows: int, cols: int, ntok: int) -> int:
+    """Kernels one tq_quantize_matmul call launches (for the shapes benchmarked: a
+    GEMV whose activations fit its shared memory, or the tensor cores)."""
+    return 2 if ntok > GEMV_MAX_TOKENS or staged(rows, cols, ntok) else 1
+
+
+def gemv_kernel_name(rows: int, cols: int, ntok: int) -> str:
+    if not staged(rows, cols, ntok):
+        return "gemv_kernel (quantize fused in)"
+    return "gemv_stage_kernel + gemv_mma_kernel (activations quantized and staged once)"
 
 WORKLOADS = {
     "decode": "decode GEMV 32768x8192 pq2_0 x q8_K, ntok=1",
@@ -232,14 +251,15 @@ class Workload:
         self.device = device
 
     def step(self, i, stream=None):
-        """quantize + matmul: one fused launch for ntok <= GEMV_MAX_TOKENS."""
+        """quantize + matmul (one fused launch where nothing is staged)."""
         import bit_matvec_gb300 as tq
         tq.tq_quantize_matmul(self.W[i % self.copies], self.X, self.Xq, self.Y, self.rows,
                               self.cols, self.ntok, self.ws, stream)
 
     def matmul_only(self, i, stream=None):
-        """The dominant kernel alone: the fused GEMV for ntok <= GEMV_MAX_TOKENS (it is the
-        whole step), the workspace tensor-core matmul otherwise."""
+        """The dominant kernel alone: for ntok <= GEMV_MAX_TOKENS the whole step (the
+        fused GEMV, or the staging kernel and the GEMV), the workspace tensor-core
+        matmul otherwise."""
         import bit_matvec_gb300 as tq
         if self.ntok <= GEMV_MAX_TOKENS:
             self.step(i, stream)
@@ -248,9 +268,9 @@ class Workload:
                             self.ntok, self.ws, stream)
 
     def launches(self):
-        # tq_quantize_matmul: one fused GEMV launch up to 8 tokens; above, the
-        # quantize-and-pack kernel and the tensor-core kernel
-        return 1 if self.ntok <= GEMV_MAX_TOKENS else 2
+        # tq_quantize_matmul: one fused GEMV launch, or a staging (or
+        # quantize-and-pack) kernel, then the GEMV (or tensor cores)
+        return launches_per_matmul(self.rows, self.cols, self.ntok)
 
     def weights(self):
         return self.rows * self.cols
@@ -295,7 +315,8 @@ class ReplayWorkload:
                                       self.ntok, self.ws, stream)
 
     def launches(self):
-        return (1 if self.ntok <= GEMV_MAX_TOKENS else 2) * self.blocks * len(self.mats)
+        return self.blocks * sum(launches_per_matmul(m["rows"], m["cols"], self.ntok)
+                                 for m in self.mats)
 
     def weights(self):
         return self.blocks * sum(m["rows"] * m["cols"] for m in self.mats)
@@ -876,7 +897,8 @@ def measure(name, args, rank, world, device, peaks, peak_kind, steps):
         res["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                            "frac": achieved / peak, "traffic": traffic,
                            "frac_of_nominal": achieved / HBM_NOMINAL_GBS,
-                           "kernel": "gemv_kernel (quantize fused in)", "kernel_ms": kern_ms,
+                           "kernel": gemv_kernel_name(wl.rows, wl.cols, wl.ntok),
+                           "kernel_ms": kern_ms,
                            "kernel_timing": kern_how,
                            "frac_meaning": "frac: independent launches back to back in a graph "
                                            "(each reads nothing the one before writes, so it "

@@ -263,7 +263,8 @@ def tq_matmul_static_ws(Wtq: torch.Tensor, Xq: torch.Tensor, Y: torch.Tensor, ro
 
 def tq_quantize_matmul(Wtq: torch.Tensor, X: torch.Tensor, Xq: torch.Tensor, Y: torch.Tensor,
                        rows: int, cols: int, ntok: int, workspace: torch.Tensor, stream=None):
-    """Xq = q8_K(X) and Y = Wtq x Xq in one call (one fused launch for ntok <= 8)."""
+    """Xq = q8_K(X) and Y = Wtq x Xq in one call (one fused launch up to 3 tokens; from 4 to
+    8, where the workspace size is not 0, a staging kernel and the GEMV)."""
     _call("tq_quantize_matmul", Wtq.device, _ptr(Wtq), _ptr(X), _ptr(Xq), _ptr(Y), rows, cols,
           ntok, _ptr(workspace), workspace.numel(), _stream(stream, Wtq.device))
 

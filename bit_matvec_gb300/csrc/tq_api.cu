@@ -38,7 +38,7 @@ bool overlap(const void* a, int64_t na, const void* b, int64_t nb) {
 // other work on the stream (a caller's kernel between two calls could write
 // the weights), so its kernels always wait first there.
 enum LastOp { kOpOther = 0, kOpQuantize = 1, kOpMatmul = 2, kOpGemv = 3 };
-constexpr int kMaxOuts = 3;
+constexpr int kMaxOuts = 5;
 struct StreamLast {
   int op = kOpOther;
   unsigned long long capture_id = 0;   // inside a capture: its id and the
@@ -94,6 +94,36 @@ void note_kernel(cudaStream_t s, int op, const void* out0, int64_t bytes0,
   g_last_op[s] = l;
 }
 
+// Like note_kernel, for a kernel that lets its successor start at its own
+// start: the kernel before it (record prev, when proven) may then still run
+// beside that successor, so prev's outputs join this kernel's.
+void note_early_trigger_kernel(cudaStream_t s, int op, const StreamLast& prev, bool proven,
+                               const void* out0, int64_t bytes0, const void* out1 = nullptr,
+                               int64_t bytes1 = 0) {
+  StreamLast l;
+  l.op = op;
+  if (!proven || !capture_tail(s, &l.capture_id, &l.node)) {
+    l.capture_id = 0;
+    l.node = nullptr;
+  }
+  l.out[0] = out0;
+  l.out_bytes[0] = bytes0;
+  l.out[1] = out1;
+  l.out_bytes[1] = bytes1;
+  int k = 2;
+  for (int i = 0; i < kMaxOuts && proven; ++i)
+    if (prev.out_bytes[i] > 0) {
+      if (k == kMaxOuts) {   // no room: the successor must not be trusted
+        l.node = nullptr;
+        break;
+      }
+      l.out[k] = prev.out[i];
+      l.out_bytes[k++] = prev.out_bytes[i];
+    }
+  std::lock_guard<std::mutex> lk(g_stream_mu);
+  g_last_op[s] = l;
+}
+
 bool misses_outputs(const StreamLast& l, const void* p, int64_t n) {
   for (int i = 0; i < kMaxOuts; ++i)
     if (overlap(p, n, l.out[i], l.out_bytes[i])) return false;
@@ -117,9 +147,10 @@ bool proven_predecessor(cudaStream_t s, StreamLast* l) {
 
 // The GEMV about to be enqueued on s may request its weights W before
 // waiting for the kernel before it: that kernel is this library's and writes
-// no part of W, and, like every kernel of this library that is recorded
-// here, it lets its successor start only after its own wait (or at its end),
-// so no older kernel can still be running.
+// no part of W, and every kernel of this library that is recorded here lets
+// its successor start only after its own wait (or at its end), so no older
+// kernel can still be running, or else (the GEMV's staging kernel) its
+// record also holds the outputs of the one kernel before it that can.
 bool early_weights_ok(cudaStream_t s, const void* W, int64_t w_bytes) {
   StreamLast l;
   return proven_predecessor(s, &l) && misses_outputs(l, W, w_bytes);
@@ -164,11 +195,25 @@ int64_t q8K_bytes(int64_t ntok, int64_t cols) { return ntok * (cols / kQK) * kQ8
 
 // With a workspace, tokens beyond this many go to the tensor cores (a token
 // tile of 16, 32 or 64); without one the GEMV takes up to gemv_max_tokens().
+// From 4 tokens up to it (and from 3072 columns) the workspace holds the
+// mma.sync GEMV's activations, staged once instead of in every CTA.
 constexpr int kWsGemvMaxTok = 8;
 
 int64_t workspace_bytes(int64_t rows, int64_t cols, int64_t ntok) {
-  if (rows <= 0 || cols <= 0 || ntok <= kWsGemvMaxTok) return 0;
+  if (rows <= 0 || cols <= 0) return 0;
+  if (ntok <= kWsGemvMaxTok) return gemv_stage_bytes(cols, (int)ntok);
   return tc_workspace_bytes(cols, ntok);
+}
+
+// The staging kernel about to be enqueued on s: *proven when the kernel
+// before it is provably this library's (record *prev), and then the staging
+// kernel lets the GEMV start at once; the result says whether it may also
+// read its input in (bytes n) before waiting (that kernel is a GEMV, which
+// lets its successor start only after its own wait, and writes none of it).
+bool stage_input_final(cudaStream_t s, const void* in, int64_t n, StreamLast* prev,
+                       bool* proven) {
+  *proven = proven_predecessor(s, prev);
+  return *proven && prev->op == kOpGemv && misses_outputs(*prev, in, n);
 }
 
 int matmul_impl(const void* Wtq, const void* Xq, float* Y, int32_t* S, int64_t rows,
@@ -210,8 +255,27 @@ int matmul_impl(const void* Wtq, const void* Xq, float* Y, int32_t* S, int64_t r
   cudaError_t e = device_status_ptr(&status);
   if (e != cudaSuccess) return fail_cuda(e);
   const int64_t w_bytes = tq_repacked_bytes(rows, cols);
-  const bool early = early_weights_ok(s, Wtq, w_bytes);
   const bool gemv = ntok <= (use_ws ? kWsGemvMaxTok : gemv_max_tokens());
+  if (gemv && need > 0 && gemv_stage_fits(cols, (int)ntok, false)) {
+    // 4..8 tokens with a workspace: the activations staged once (see
+    // tq_quantize_matmul), from the q8_K blocks
+    uint8_t* region = static_cast<uint8_t*>(ws);
+    StreamLast prev;
+    bool proven = false;
+    const bool x_final = stage_input_final(s, Xq, q8K_bytes(ntok, cols), &prev, &proven);
+    note_op(s, kOpOther);
+    e = launch_gemv_stage(nullptr, X, nullptr, region, cols, (int)ntok, x_final, proven, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    note_early_trigger_kernel(s, kOpQuantize, prev, proven, region, need);
+    const bool early_w = early_weights_ok(s, Wtq, w_bytes);
+    note_op(s, kOpOther);
+    e = launch_gemv(W, X, Y, S, rows, cols, (int)ntok, status, early_w, false, s, nullptr, nullptr,
+                    region);
+    if (e != cudaSuccess) return fail_cuda(e);
+    note_kernel(s, kOpGemv, out, out_bytes);
+    return TQ_OK;
+  }
+  const bool early = early_weights_ok(s, Wtq, w_bytes);
   const bool inputs_final =
       gemv && gemv_inputs_final(s, Xq, q8K_bytes(ntok, cols), Wtq, w_bytes);
   note_op(s, kOpOther);
@@ -224,7 +288,9 @@ int matmul_impl(const void* Wtq, const void* Xq, float* Y, int32_t* S, int64_t r
     if (e != cudaErrorNotSupported) return fail_cuda(e);
     // activations too large for the GEMV's shared memory: tensor-core path
   }
-  if (need > 0)
+  // up to kWsGemvMaxTok tokens a workspace is sized for the staged GEMV, not
+  // for the tensor cores
+  if (need > 0 && ntok > kWsGemvMaxTok)
     e = launch_gemm_tc_ws(W, X, Y, S, rows, cols, ntok, static_cast<uint8_t*>(ws), status, s);
   else
     e = launch_gemm_tc(W, X, Y, S, rows, cols, ntok, status, s);
@@ -504,6 +570,26 @@ int tq_quantize_matmul(const void* Wtq, const float* X, void* Xq, float* Y, int6
     int* status = nullptr;
     cudaError_t e = device_status_ptr(&status);
     if (e != cudaSuccess) return fail_cuda(e);
+    if (need > 0 && gemv_stage_fits(cols, (int)ntok, true)) {
+      // 4..8 tokens: one kernel quantizes X, writes Xq and stages the GEMV's
+      // activations in the workspace; the GEMV loads them
+      uint8_t* region = static_cast<uint8_t*>(workspace);
+      StreamLast prev;
+      bool proven = false;
+      const bool x_final = stage_input_final(s, X, x_bytes, &prev, &proven);
+      note_op(s, kOpOther);
+      e = launch_gemv_stage(X, nullptr, static_cast<uint8_t*>(Xq), region, cols, (int)ntok, x_final,
+                            proven, s);
+      if (e != cudaSuccess) return fail_cuda(e);
+      note_early_trigger_kernel(s, kOpQuantize, prev, proven, Xq, xq_bytes, region, need);
+      const bool early_w = early_weights_ok(s, Wtq, w_bytes);
+      note_op(s, kOpOther);
+      e = launch_gemv(static_cast<const uint8_t*>(Wtq), nullptr, Y, nullptr, rows, cols, (int)ntok,
+                      status, early_w, false, s, nullptr, nullptr, region);
+      if (e != cudaSuccess) return fail_cuda(e);
+      note_kernel(s, kOpGemv, Y, y_bytes);
+      return TQ_OK;
+    }
     const bool early = early_weights_ok(s, Wtq, w_bytes);
     const bool inputs_final = gemv_inputs_final(s, X, x_bytes, Wtq, w_bytes);
     note_op(s, kOpOther);
@@ -519,7 +605,7 @@ int tq_quantize_matmul(const void* Wtq, const float* X, void* Xq, float* Y, int6
     }
     // activations too large for the GEMV's shared memory: the separate calls
   }
-  if (need > 0) {
+  if (need > 0 && ntok > kWsGemvMaxTok) {
     // one kernel quantizes and packs the workspace, then the tensor-core kernel
     int* status = nullptr;
     cudaError_t e = device_status_ptr(&status);

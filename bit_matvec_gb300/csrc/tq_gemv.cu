@@ -100,6 +100,9 @@ struct GemvArgs {
   int stall;          // test facility: CTA 0 requests no weight stage, so its
                       // waits expire after stall_ns (tq_debug_stall_next_launch)
   uint64_t stall_ns;
+  const uint8_t* Xs = nullptr;  // mma.sync GEMV: the activations already staged by the
+                      // staging kernel (the shared-memory image of the f16
+                      // rows, group sums and scales), or null to stage here
 };
 
 // Fused form: quantizes the T x cols f32 activations block by block (warp per
@@ -545,7 +548,7 @@ __host__ __device__ inline MmaPlan plan_mma(int stages, int64_t cols) {
   p.sb_stride = MmaCfg<T, TPW>::kI8 ? cols + 4 : cols * 2 + 8;
   p.ring = 0;
   p.bars = (int64_t)stages * MmaCfg<T, TPW>::kStageBytes;
-  p.counters = p.bars + (stages + 4) * 8;                  // int[S] released, int[S] issued
+  p.counters = p.bars + (stages + 5) * 8;                  // int[S] released, int[S] issued
   p.sb = (p.counters + stages * 8 + 15) / 16 * 16;
   p.sgsum = (p.sb + T * p.sb_stride + 15) / 16 * 16;
   p.sdx = p.sgsum + T * g * 4;
@@ -706,6 +709,7 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + pl.bars);  // [S]
   uint64_t* redfull = full + S;                                   // [2]
   uint64_t* redempty = redfull + 2;                               // [2]
+  uint64_t* actfull = redempty + 2;                               // staged activations
   int* released = reinterpret_cast<int*>(smem + pl.counters);    // [S]
   int* issued = released + S;                                    // [S] copies per slot
   uint8_t* sb = smem + pl.sb;                                     // [T][cols] f16 (+8 B)
@@ -750,14 +754,32 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
       mbarrier_init(smem_u32(redfull + i), kConsumers);
       mbarrier_init(smem_u32(redempty + i), kReducers);
     }
+    mbarrier_init(smem_u32(actfull), 1);
     mbarrier_init_fence();
     if (a.early_weights) issue_first();
   }
   if (!a.defer) {   // as in the one-token kernel
     pdl_wait_primary();
-    pdl_launch_dependents();
+    if (!a.Xs) pdl_launch_dependents();
   }
   if (threadIdx.x == 0 && !a.early_weights) issue_first();
+
+  // Activations staged by the staging kernel (which this kernel has waited
+  // for): one bulk copy of their shared-memory image. The next kernel may
+  // start only once the copy has landed, since it may overwrite the staged
+  // region (the next call's staging).
+  bool failed = false;
+  const int64_t act_bytes = pl.red - pl.sb;
+  if (a.Xs) {
+    __syncthreads();   // thread 0 has initialized the barriers
+    if (threadIdx.x == 0) {
+      mbarrier_arrive_expect_tx(smem_u32(actfull), (uint32_t)act_bytes);
+      bulk_copy_g2s(smem_u32(sb), a.Xs, (uint32_t)act_bytes, smem_u32(actfull),
+                    l2_evict_last_policy());
+    }
+    if (!mbarrier_wait_bounded(smem_u32(actfull), 0u, lim)) failed = true;
+    pdl_launch_dependents();
+  }
 
   // Stage the activations: f16 q * 2^(9 - 2s) (up to 8 tokens) or the int8 q
   // (more) per token row, the sum of each 128-value half-block (8 partial
@@ -779,7 +801,9 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
     dst[0] = make_uint2(h2_mul_rn(h[0], m0), h2_mul_rn(h[1], m0));
     dst[1] = make_uint2(h2_mul_rn(h[2], m1), h2_mul_rn(h[3], m1));
   };
-  if (a.X) {
+  if (a.Xs) {
+    // staged already
+  } else if (a.X) {
     stage_quantize(a, T * a.nblk, warp, kConsumers, lane,
                    [&](int tb, uint32_t w0, uint32_t w1, int s8, float d) {
                      put_f16(tb, w0, w1);
@@ -845,7 +869,6 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
     waited = true;
   };
 
-  bool failed = false;
   int j = 0, slot = 0;
   uint32_t phase = 0;
   for (int rb = rb0, i = 0; rb < rb1; ++rb, ++i) {
@@ -925,7 +948,79 @@ __global__ void __launch_bounds__(MmaCfg<T, TPW>::kThreads, 1) gemv_mma_kernel(c
     for (int sl = 0; sl < S; ++sl)
       if (issued[sl] > 0)
         mbarrier_wait_bounded(smem_u32(full + sl), (uint32_t)((issued[sl] - 1) & 1), kWaitLimitNs);
+    if (a.Xs) mbarrier_wait_bounded(smem_u32(actfull), 0u, kWaitLimitNs);   // the staged copy
   }
+}
+
+// The staging kernel of the mma.sync GEMV's workspace forms: the activations
+// in the shared-memory image the GEMV would otherwise build in every CTA (f16
+// rows of q * 2^(9 - 2s), the half-block sums, the block scales), built once
+// in the caller's workspace; each GEMV CTA then loads it with one bulk copy.
+// One warp per q8_K block (token t, block b), from the f32 activations
+// (quantized exactly as the quantizer kernel does, the q8_K block written to
+// Xq_out) or from the q8_K blocks Xq_in. Launched as a programmatic dependent:
+// with x_final (the host showed the kernel before it writes nothing this one
+// reads) it reads and quantizes before waiting for that kernel; it writes
+// only after the wait. It lets its successor (the GEMV, which waits for it
+// before reading the image) start at once when early_trigger (the host knows
+// the kernel before it and passes its outputs on to the GEMV's early-read
+// check), else only after its own wait.
+constexpr int kStageWarps = 8;
+
+template <int T>
+__global__ void __launch_bounds__(kStageWarps * 32) gemv_stage_kernel(
+    const float* __restrict__ X, const uint8_t* __restrict__ Xq_in, uint8_t* __restrict__ Xq_out,
+    uint8_t* __restrict__ region, int nblk, int64_t sb_stride, int64_t off_sgsum, int64_t off_sdx,
+    int x_final, int early_trigger) {
+  const int lane = threadIdx.x & 31;
+  const int tb = blockIdx.x * kStageWarps + (threadIdx.x >> 5);
+  const bool active = tb < T * nblk;   // warp-uniform
+  if (early_trigger) pdl_launch_dependents();
+  if (!x_final) {
+    pdl_wait_primary();
+    if (!early_trigger) pdl_launch_dependents();
+  }
+  uint32_t w0 = 0u, w1 = 0u;
+  int s8 = 0, bs = 0;
+  float d = 0.0f;
+  if (active) {
+    if (X) {
+      const float4* src = reinterpret_cast<const float4*>(X + (int64_t)tb * kQK) + 2 * lane;
+      q8K_warp(__ldg(src), __ldg(src + 1), w0, w1, s8, d);
+    } else {
+      const uint8_t* blk = Xq_in + (int64_t)tb * kQ8KBytes;
+      const uint32_t* qs = reinterpret_cast<const uint32_t*>(blk + kQ8KQsOffset);
+      w0 = __ldg(qs + 2 * lane);
+      w1 = __ldg(qs + 2 * lane + 1);
+      bs = lane < 16 ? (int)__ldg(reinterpret_cast<const int16_t*>(blk + kQ8KBsumsOffset) + lane) : 0;
+      d = __ldg(reinterpret_cast<const float*>(blk));
+    }
+  }
+  if (x_final) {
+    pdl_wait_primary();
+    if (!early_trigger) pdl_launch_dependents();
+  }
+  if (!active) return;
+  if (X && Xq_out) q8K_store(Xq_out + (int64_t)tb * kQ8KBytes, lane, w0, w1, s8, d);
+  const int t = tb / nblk, b = tb - t * nblk;
+  uint32_t h[4];
+  tc::s8x4_to_h2x2(w0, h[0], h[1]);
+  tc::s8x4_to_h2x2(w1, h[2], h[3]);
+  const uint32_t m0 = mma_slot_scale(2 * (lane & 1)), m1 = mma_slot_scale(2 * (lane & 1) + 1);
+  uint2* dst = reinterpret_cast<uint2*>(region + t * sb_stride + ((int64_t)b * kQK + 8 * lane) * 2);
+  dst[0] = make_uint2(h2_mul_rn(h[0], m0), h2_mul_rn(h[1], m0));
+  dst[1] = make_uint2(h2_mul_rn(h[2], m1), h2_mul_rn(h[3], m1));
+  int* sgsum = reinterpret_cast<int*>(region + off_sgsum);
+  if (X) {
+    const int hs = half_block_sum(s8);
+    if ((lane & 15) == 0) sgsum[2 * tb + (lane >> 4)] = hs;
+  } else {
+    bs += __shfl_xor_sync(0xffffffffu, bs, 1);
+    bs += __shfl_xor_sync(0xffffffffu, bs, 2);
+    bs += __shfl_xor_sync(0xffffffffu, bs, 4);
+    if (lane == 0 || lane == 8) sgsum[2 * tb + (lane >> 3)] = bs;
+  }
+  if (lane == 0) reinterpret_cast<float*>(region + off_sdx)[tb] = d;
 }
 
 // Where a launch the host allowed to defer its wait (a.defer) waits: never
@@ -1076,7 +1171,7 @@ cudaError_t launch_tok(const GemvArgs& a, int64_t cols, bool gsum, cudaStream_t 
     // tile per warp and stage, then the dp4a loop
     if (e == cudaErrorNotSupported && tpw != 1)
       e = gsum ? launch_mma<T, true, 1>(a, cols, s) : launch_mma<T, false, 1>(a, cols, s);
-    if (e != cudaErrorNotSupported) return e;
+    if (e != cudaErrorNotSupported || a.Xs) return e;   // staged activations: the mma kernel only
   }
   if constexpr (T <= kMaxDp4aTok)
     return gsum ? launch_t<T, true>(a, cols, s) : launch_t<T, false>(a, cols, s);
@@ -1140,7 +1235,8 @@ cudaError_t launch_gemv_ptq1(const uint8_t* Wt1, const uint8_t* Xq, float* Y, in
 
 cudaError_t launch_gemv(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t* S,
                         int64_t rows, int64_t cols, int ntok, int* dev_status, bool early_weights,
-                        bool inputs_final, cudaStream_t s, const float* X, uint8_t* Xq_out) {
+                        bool inputs_final, cudaStream_t s, const float* X, uint8_t* Xq_out,
+                        const uint8_t* Xs) {
   if (ntok < 1 || ntok > kMaxTok) return cudaErrorNotSupported;
   if (rows > 0x7fffffff / 2 || cols / kGroup > 0x7fffffff / kTileBytes)
     return cudaErrorNotSupported;
@@ -1161,6 +1257,7 @@ cudaError_t launch_gemv(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t
   a.defer = inputs_final ? 1 : 0;
   a.stall = 0;
   a.stall_ns = 0;
+  a.Xs = Xs;
   const bool gsum = S != nullptr;
   cudaError_t e;
   switch (ntok) {
@@ -1181,7 +1278,7 @@ cudaError_t launch_gemv(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t
     case 15: e = launch_tok<15>(a, cols, gsum, s); break;
     default: e = launch_tok<16>(a, cols, gsum, s); break;
   }
-  if (e != cudaErrorNotSupported || ntok == 1) return e;
+  if (e != cudaErrorNotSupported || ntok == 1 || Xs) return e;
   // The activations of all tokens do not fit in shared memory (long rows:
   // 8 tokens of 17408 columns, 16 of 8192): one launch per half of the tokens, each
   // streaming the weights once, instead of the tensor-core path for a tile
@@ -1200,6 +1297,91 @@ cudaError_t launch_gemv(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t
                      S ? S + (int64_t)n0 * rows * a.ngroups : nullptr, rows, cols, ntok - n0,
                      dev_status, true, false, s, X ? X + (int64_t)n0 * cols : nullptr,
                      Xq_out ? Xq_out + (int64_t)n0 * a.nblk * kQ8KBytes : nullptr);
+}
+
+namespace {
+
+// The staged image's layout (relative to its first byte) for ntok tokens of
+// cols columns: the same for every ring depth and tiles per warp.
+template <int T>
+MmaPlan stage_plan(int64_t cols) { return plan_mma<T, 1>(2, cols); }
+
+// The staged form is planned against the opt-in shared memory of one block
+// on sm_103a (227 KB), so whether it applies, and the workspace it needs, are
+// functions of the shape alone.
+constexpr int64_t kStageSmemLimit = 232448;
+
+// Staging pays where preparing the activations in every CTA costs more than
+// the staging kernel's launch: from 3072 columns where the call also
+// quantizes X (tq_quantize_matmul), from 5120 where the GEMV only converts
+// q8_K blocks to f16, work it does before waiting for the launch before it
+// in a chain (measured at 4 to 8 tokens on matrices of 2048 to 17408
+// columns). Below, the workspace stays empty and the fused GEMV runs.
+#ifndef TQ_GEMV_STAGE_MIN_COLS
+#define TQ_GEMV_STAGE_MIN_COLS 3072
+#endif
+constexpr int64_t kStageMinColsConvert = 5120;
+
+template <int T>
+bool stage_fits(int64_t cols) {
+  DeviceLimits lim;
+  if (device_limits(&lim) != cudaSuccess) return false;
+  const int64_t total = stage_plan<T>(cols).total;   // the smallest mma.sync configuration
+  return total <= kStageSmemLimit && total <= lim.optin_smem;
+}
+
+template <int T>
+cudaError_t launch_stage_t(const float* X, const uint8_t* Xq_in, uint8_t* Xq_out, uint8_t* region,
+                           int64_t cols, bool x_final, bool early_trigger, cudaStream_t s) {
+  const MmaPlan p = stage_plan<T>(cols);
+  const int nblk = (int)(cols / kQK);
+  const int grid = (T * nblk + kStageWarps - 1) / kStageWarps;
+  return launch_pdl(gemv_stage_kernel<T>, dim3(grid), dim3(kStageWarps * 32), 0, s, X, Xq_in,
+                    Xq_out, region, nblk, p.sb_stride, p.sgsum - p.sb, p.sdx - p.sb,
+                    x_final ? 1 : 0, early_trigger ? 1 : 0);
+}
+
+}  // namespace
+
+int64_t gemv_stage_bytes(int64_t cols, int ntok) {
+  if (cols <= 0 || cols < TQ_GEMV_STAGE_MIN_COLS || ntok < TQ_GEMV_MMA_MIN_TOK ||
+      ntok > kMaxDp4aTok)
+    return 0;
+  MmaPlan p;
+  switch (ntok) {
+    case 4: p = stage_plan<4>(cols); break;
+    case 5: p = stage_plan<5>(cols); break;
+    case 6: p = stage_plan<6>(cols); break;
+    case 7: p = stage_plan<7>(cols); break;
+    default: p = stage_plan<8>(cols); break;
+  }
+  return p.total <= kStageSmemLimit ? p.red - p.sb : 0;
+}
+
+bool gemv_stage_fits(int64_t cols, int ntok, bool quantizes) {
+  if (gemv_stage_bytes(cols, ntok) == 0) return false;
+  if (!quantizes && cols < kStageMinColsConvert) return false;
+  if (cols / kGroup > 0x7fffffff / kTileBytes) return false;
+  switch (ntok) {
+    case 4: return stage_fits<4>(cols);
+    case 5: return stage_fits<5>(cols);
+    case 6: return stage_fits<6>(cols);
+    case 7: return stage_fits<7>(cols);
+    default: return stage_fits<8>(cols);
+  }
+}
+
+cudaError_t launch_gemv_stage(const float* X, const uint8_t* Xq_in, uint8_t* Xq_out,
+                              uint8_t* region, int64_t cols, int ntok, bool x_final,
+                              bool early_trigger, cudaStream_t s) {
+  switch (ntok) {
+    case 4: return launch_stage_t<4>(X, Xq_in, Xq_out, region, cols, x_final, early_trigger, s);
+    case 5: return launch_stage_t<5>(X, Xq_in, Xq_out, region, cols, x_final, early_trigger, s);
+    case 6: return launch_stage_t<6>(X, Xq_in, Xq_out, region, cols, x_final, early_trigger, s);
+    case 7: return launch_stage_t<7>(X, Xq_in, Xq_out, region, cols, x_final, early_trigger, s);
+    case 8: return launch_stage_t<8>(X, Xq_in, Xq_out, region, cols, x_final, early_trigger, s);
+    default: return cudaErrorNotSupported;
+  }
 }
 
 }  // namespace tq

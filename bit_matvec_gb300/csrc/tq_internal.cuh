@@ -152,6 +152,13 @@ __device__ __forceinline__ void mbarrier_arrive_expect_tx(uint32_t bar, uint32_t
                : "memory");
 }
 
+// L2 policy for data every CTA of a launch reads: keep it.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // L2 policy for data read once per launch: evict it first.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t p;
@@ -284,10 +291,32 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // With X non-null the GEMV quantizes the f32 activations X itself (the fused
 // form; Xq is then an output, written once, and may be null) instead of
 // reading q8_K blocks from Xq.
+// With Xs non-null (4..8 tokens, the mma.sync GEMV) the activations come
+// staged by launch_gemv_stage into Xs, enqueued just before on s; the kernel
+// waits for it, loads the image with one bulk copy, and lets its successor
+// start only once that copy has landed.
 cudaError_t launch_gemv(const uint8_t* Wtq, const uint8_t* Xq, float* Y, int32_t* S,
                         int64_t rows, int64_t cols, int ntok, int* dev_status, bool early_weights,
                         bool inputs_final, cudaStream_t s, const float* X = nullptr,
-                        uint8_t* Xq_out = nullptr);
+                        uint8_t* Xq_out = nullptr, const uint8_t* Xs = nullptr);
+
+// Bytes of the staged activations of the mma.sync GEMV for ntok tokens (0
+// outside 4..8, below 3072 columns, or where that GEMV would need more than
+// the 227 KB of shared memory a block may opt in to on sm_103a), and whether
+// the staged form runs: it fits on the current device, and the call
+// quantizes X (quantizes) or has at least 5120 columns.
+int64_t gemv_stage_bytes(int64_t cols, int ntok);
+bool gemv_stage_fits(int64_t cols, int ntok, bool quantizes);
+// Stages the activations into region (gemv_stage_bytes, 16-byte aligned):
+// from the f32 X (quantized, the q8_K blocks written to Xq_out) or from the
+// q8_K blocks Xq_in. x_final: the kernel before it on s writes nothing it
+// reads (it may then read before waiting; it writes only after the wait).
+// early_trigger: its successor may start before its wait (the host then
+// checks that successor's early reads against the outputs of the kernel
+// before this one too).
+cudaError_t launch_gemv_stage(const float* X, const uint8_t* Xq_in, uint8_t* Xq_out,
+                              uint8_t* region, int64_t cols, int ntok, bool x_final,
+                              bool early_trigger, cudaStream_t s);
 int gemv_max_tokens();
 // Token counts up to which the workspace forms also run the GEMV (beyond, the
 // tensor cores, which need the workspace).

@@ -247,8 +247,14 @@ int tq_matmul_groupsums(const void *Wtq, const void *Xq, int32_t *S, int64_t row
 
 /*
  * tq_matmul_workspace_bytes -- scratch needed by tq_matmul_ws for this shape:
- * 0 when ntok <= 8 (those calls run the GEMV, which needs none); otherwise,
- * with the token tile T = 16 for ntok <= 16, 32 for ntok <= 32, else 64,
+ * 0 when ntok <= 3 (the GEMV needs none). From 4 to 8 tokens the GEMV's
+ * activations staged once, as f16 rows: with R = round16(ntok * (2*cols + 8)),
+ * round16(R + ntok * (cols/128) * 4 + ntok * (cols/256) * 4) bytes (round16:
+ * up to a multiple of 16); 0 below 3072 columns (staging does not pay there)
+ * and where that GEMV would need more than the 227 KB of shared memory a
+ * block may opt in to (cols > 9984 at 8 tokens, cols > 19968 at 4).
+ * Otherwise, with the token tile T = 16 for
+ * ntok <= 16, 32 for ntok <= 32, else 64,
  * ceil(ntok/T) * (cols/128) * 256*T + ceil(ntok/T) * (cols/256) * 12*T bytes.
  * -1 for a bad shape.
  */
@@ -263,9 +269,15 @@ int64_t tq_matmul_workspace_bytes(int64_t rows, int64_t cols, int64_t ntok);
  * into two e4m3 parts, instead of every 128-row tile of the weights
  * converting them again), then the tensor-core kernel reads them with one
  * bulk copy per q8_K block. Same results
- * and tolerance as tq_matmul; for ntok <= 8 it is tq_matmul (the GEMV), and
- * from 9 tokens on it runs the tensor-core kernel on token tiles of 16, 32 or
- * 64 where tq_matmul would still run the GEMV up to 16.
+ * and tolerance as tq_matmul. For ntok <= 8 it runs tq_matmul's GEMV; from 4
+ * tokens and 5120 columns (where the workspace size is not 0) a small kernel
+ * first converts the activations once into the GEMV's f16 layout in the
+ * workspace, which every CTA of the GEMV then loads with one bulk copy
+ * instead of converting them itself (measured in graph chains: 1.0-1.15x
+ * faster from 5120 columns, slower below, where each CTA converts before
+ * waiting for the launch before it). From 9 tokens on it runs the tensor-core
+ * kernel on token tiles of 16, 32 or 64 where tq_matmul would still run the
+ * GEMV up to 16.
  *   workspace  device buffer of at least tq_matmul_workspace_bytes(rows, cols,
  *              ntok) bytes, 16-byte aligned, owned by the caller; its contents
  *              are overwritten and meaningless after the call; it must not
@@ -286,19 +298,25 @@ int tq_matmul_groupsums_ws(const void *Wtq, const void *Xq, int32_t *S, int64_t 
 
 /*
  * tq_quantize_matmul -- tq_quantize_q8K then tq_matmul_ws in one call: Xq =
- * the q8_K blocks of X, Y = the product of Wtq and Xq. For ntok <= 8 it is one
+ * the q8_K blocks of X, Y = the product of Wtq and Xq. For ntok <= 3 (and up
+ * to 8 where the workspace size is 0, as below 3072 columns) it is one
  * fused launch: every CTA of the GEMV quantizes X into its shared memory
  * itself (with the quantizer's arithmetic, so Xq and Y carry the bits of the
  * two separate calls), and writes Xq (CTA 0 at its start; in the graph chains
  * tq_matmul describes, every CTA a share after its wait). That removes a launch and the
- * quantizer's place on the critical path of each matmul. For ntok >= 9 one
+ * quantizer's place on the critical path of each matmul. From 4 to 8 tokens
+ * with a workspace, one small kernel quantizes X (the same arithmetic),
+ * writes Xq and stages the GEMV's activations in the workspace, then the
+ * GEMV runs (measured in graph chains: 1.1-1.7x faster than the fused launch
+ * from 3072 columns; 11.4 against 12.6 us at 4 tokens on 17408 x 5120).
+ * For ntok >= 9 one
  * kernel quantizes X (the same arithmetic), writes Xq and packs the
  * workspace, which the tensor-core kernel then reads: two launches instead
  * of three, the same bits.
  *   X  [ntok][cols] f32, 16-byte aligned (as tq_quantize_q8K).
  *   Xq [ntok][cols/256] q8_K, 16-byte aligned: written.
  *   Wtq, Y, workspace, workspace_bytes: as tq_matmul_ws (the workspace is
- *   only used for ntok >= 9).
+ *   used from 4 tokens on where its size is not 0).
  * Overlap: like tq_matmul after tq_quantize_q8K, the launch may start
  * reading Wtq before the kernel enqueued just before it ends when the
  * previous call this library received for the stream was the quantizer or a
@@ -346,7 +364,8 @@ int tq_matmul_host(const void *Wtq, const float *X_host, float *X, void *Xq, flo
  *   Same arguments, results and errors as tq_matmul_ws, minus the workspace.
  *   Limit: tq_matmul_workspace_bytes(rows, cols, ntok) <= TQ_STATIC_WS_BYTES,
  *   else TQ_ERR_WORKSPACE before anything runs (for example cols = 5120
- *   allows ntok <= 768; ntok <= 8 needs no workspace and has no limit).
+ *   allows ntok <= 768; ntok <= 8 needs at most the GEMV's staged
+ *   activations, under 227 KB, and has no limit).
  *   Set-up: the first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current), which may also load the
  *   library's code for the array onto that device; make that first call

@@ -143,9 +143,25 @@ def test_binding_rejects_cpu_tensors(lib):
 
 
 def test_workspace_bytes(lib):
-    # none for the GEMV route; B tiles + block scales per 64-token tile otherwise
+    # none for 1..3 tokens; for 4..8 the mma.sync GEMV's staged activations:
+    # f16 rows of cols * 2 + 8 bytes (the block's 16-byte multiple), then the
+    # half-block sums and the block scales, rounded up to 16 bytes;
+    # B tiles + block scales per token tile above
     assert lib.tq_matmul_workspace_bytes(32768, 8192, 1) == 0
-    assert lib.tq_matmul_workspace_bytes(17408, 5120, 8) == 0
+    assert lib.tq_matmul_workspace_bytes(32768, 8192, 3) == 0
+
+    def staged(cols, t):
+        rows16 = -(-t * (cols * 2 + 8) // 16) * 16
+        return -(-(rows16 + t * (cols // 128) * 4 + t * (cols // 256) * 4) // 16) * 16
+
+    for cols, t in ((5120, 4), (5120, 8), (8192, 5), (17408, 4), (9984, 8), (3072, 7)):
+        assert lib.tq_matmul_workspace_bytes(17408, cols, t) == staged(cols, t)
+    assert lib.tq_matmul_workspace_bytes(17408, 5120, 8) == 83904
+    # none below 3072 columns (the fused GEMV is faster there), nor where that
+    # GEMV would not fit in a block's 227 KB of shared memory (the larger
+    # activations then go to the tensor cores without a workspace)
+    for cols, t in ((256, 7), (2816, 4), (10240, 8), (17408, 8), (20224, 4), (1 << 30, 4)):
+        assert lib.tq_matmul_workspace_bytes(5120, cols, t) == 0
     # token tiles of 16, 32 and 64: per group 2 x 16 x 128 bytes of B (and per
     # block 3 x 16 floats of scales and sums), 2 x 32 x 128, 2 x 64 x 128
     assert lib.tq_matmul_workspace_bytes(17408, 5120, 9) == 40 * 4096 + 20 * 192

@@ -49,7 +49,8 @@ def _bits(t):
 
 @pytest.mark.parametrize("rows,cols,ntok", [(ROWS, 1024, 1), (ROWS, 1024, 3), (ROWS, 1024, 4),
                                              (ROWS, 1024, 8), (5120, 17408, 1), (5120, 17408, 3),
-                                             (5120, 17408, 4), (32768, 1024, 1), (32768, 1024, 4)])
+                                             (5120, 17408, 4), (32768, 1024, 1), (32768, 1024, 4),
+                                             (ROWS, 5120, 8), (ROWS, 3072, 5)])
 def test_graph_chain_of_independent_calls(rows, cols, ntok):
     """Four fused calls and two tq_matmul calls, each on its own weights, all
     reading activations no call of the chain writes (the fused calls share
@@ -59,7 +60,10 @@ def test_graph_chain_of_independent_calls(rows, cols, ntok):
     three-token kernels wait after its first ring stage. With 32768 rows (1024
     tile columns) the calls made one at a time, which wait first, fill every
     resident slot with uneven tile columns per CTA, while the chain splits
-    them evenly over fewer CTAs: the bits must not change."""
+    them evenly over fewer CTAs: the bits must not change. From 4 tokens and
+    3072 columns each fused call is a staging kernel and the GEMV, which the
+    staging kernel lets start at once (5120 x 17408 at 4 tokens, 20480 x 5120
+    at 8, 20480 x 3072 at 5)."""
     import bit_matvec_gb300 as tq
     n = 4
     wpq = [synth.pq2_0_weights(rows, cols, 40 + i) for i in range(n + 2)]
@@ -116,44 +120,46 @@ def _wide(wpq, rows, cols, reps):
     return np.tile(wpq.reshape(rows, -1), (1, reps)).reshape(-1)
 
 
-@pytest.mark.parametrize("ntok", [1, 4])
-def test_graph_chain_reading_previous_outputs(ntok):
+@pytest.mark.parametrize("ntok,n", [(1, ROWS), (4, ROWS), (4, 16384), (8, 8192)])
+def test_graph_chain_reading_previous_outputs(ntok, n):
     """Each call reads what the call before it wrote (its Y as the next
     activations, or its q8_K bytes): those calls wait before reading, and the
     results equal the calls run one at a time. One call in the chain reads
-    only older outputs and may read early."""
+    only older outputs and may read early. At 4 tokens and 16384 columns, and 8
+    tokens and 8192, the fused calls on the square matrices stage their
+    activations in the workspace (a staging kernel, then the GEMV)."""
     import bit_matvec_gb300 as tq
-    c0, reps = 1024, ROWS // 1024
-    w0 = synth.pq2_0_weights(ROWS, c0, 50)
-    W1 = gpu_repack(w0, ROWS, c0)                               # c0 -> ROWS
-    W2 = gpu_repack(_wide(synth.pq2_0_weights(ROWS, c0, 51), ROWS, c0, reps), ROWS, ROWS)
-    W3 = gpu_repack(_wide(synth.pq2_0_weights(ROWS, c0, 52), ROWS, c0, reps), ROWS, ROWS)
-    W4 = gpu_repack(_wide(synth.pq2_0_weights(ROWS, c0, 53), ROWS, c0, reps), ROWS, ROWS)
+    c0, reps = 1024, n // 1024
+    w0 = synth.pq2_0_weights(n, c0, 50)
+    W1 = gpu_repack(w0, n, c0)                               # c0 -> n
+    W2 = gpu_repack(_wide(synth.pq2_0_weights(n, c0, 51), n, c0, reps), n, n)
+    W3 = gpu_repack(_wide(synth.pq2_0_weights(n, c0, 52), n, c0, reps), n, n)
+    W4 = gpu_repack(_wide(synth.pq2_0_weights(n, c0, 53), n, c0, reps), n, n)
     X0 = torch.from_numpy(np.ascontiguousarray(_acts(ntok, c0, 54))).to(DEV)
-    ws0 = tq.workspace_empty(ROWS, c0, ntok, DEV)
-    ws = tq.workspace_empty(ROWS, ROWS, ntok, DEV)
+    ws0 = tq.workspace_empty(n, c0, ntok, DEV)
+    ws = tq.workspace_empty(n, n, ntok, DEV)
 
     def buffers():
-        return dict(Y1=torch.full((ntok, ROWS), float("nan"), device=DEV),
-                    Y2=torch.full((ntok, ROWS), float("nan"), device=DEV),
-                    Y3=torch.full((ntok, ROWS), float("nan"), device=DEV),
-                    Y4=torch.full((ntok, ROWS), float("nan"), device=DEV),
-                    Y5=torch.full((ntok, ROWS), float("nan"), device=DEV),
+        return dict(Y1=torch.full((ntok, n), float("nan"), device=DEV),
+                    Y2=torch.full((ntok, n), float("nan"), device=DEV),
+                    Y3=torch.full((ntok, n), float("nan"), device=DEV),
+                    Y4=torch.full((ntok, n), float("nan"), device=DEV),
+                    Y5=torch.full((ntok, n), float("nan"), device=DEV),
                     Xq0=torch.full((tq.q8K_nbytes(ntok, c0),), 0xEE, dtype=torch.uint8, device=DEV),
-                    Xq1=torch.full((tq.q8K_nbytes(ntok, ROWS),), 0xEE, dtype=torch.uint8, device=DEV),
-                    Xq2=torch.full((tq.q8K_nbytes(ntok, ROWS),), 0xEE, dtype=torch.uint8, device=DEV))
+                    Xq1=torch.full((tq.q8K_nbytes(ntok, n),), 0xEE, dtype=torch.uint8, device=DEV),
+                    Xq2=torch.full((tq.q8K_nbytes(ntok, n),), 0xEE, dtype=torch.uint8, device=DEV))
 
     def steps(b):
         return [
-            lambda s: tq.tq_quantize_matmul(W1, X0, b["Xq0"], b["Y1"], ROWS, c0, ntok, ws0, stream=s),
+            lambda s: tq.tq_quantize_matmul(W1, X0, b["Xq0"], b["Y1"], n, c0, ntok, ws0, stream=s),
             # activations = the previous call's Y
-            lambda s: tq.tq_quantize_matmul(W2, b["Y1"], b["Xq1"], b["Y2"], ROWS, ROWS, ntok, ws, stream=s),
+            lambda s: tq.tq_quantize_matmul(W2, b["Y1"], b["Xq1"], b["Y2"], n, n, ntok, ws, stream=s),
             # q8_K bytes the previous call wrote
-            lambda s: tq.tq_matmul(W3, b["Xq1"], b["Y3"], ROWS, ROWS, ntok, stream=s),
+            lambda s: tq.tq_matmul(W3, b["Xq1"], b["Y3"], n, n, ntok, stream=s),
             # Y of two calls back (complete once the previous call has waited)
-            lambda s: tq.tq_quantize_matmul(W4, b["Y2"], b["Xq2"], b["Y4"], ROWS, ROWS, ntok, ws, stream=s),
+            lambda s: tq.tq_quantize_matmul(W4, b["Y2"], b["Xq2"], b["Y4"], n, n, ntok, ws, stream=s),
             # the previous call's Y again
-            lambda s: tq.tq_quantize_matmul(W2, b["Y4"], b["Xq1"], b["Y5"], ROWS, ROWS, ntok, ws, stream=s),
+            lambda s: tq.tq_quantize_matmul(W2, b["Y4"], b["Xq1"], b["Y5"], n, n, ntok, ws, stream=s),
         ]
 
     ref = buffers()
@@ -197,3 +203,65 @@ def test_eager_chain_equals_graph():
     for a, b in zip(eager[0], graph[0]):
         assert torch.equal(_bits(a), _bits(b))
     assert torch.equal(eager[1], graph[1])
+
+
+def test_graph_chain_mixed_kinds_sharing_a_workspace():
+    """Staged GEMV calls beside the quantizer and the tensor-core path, all on
+    one workspace: a staging kernel after the quantizer (it must wait before
+    reading the q8_K bytes), the quantize-and-pack kernel after a staged GEMV
+    (it must not rewrite the workspace before that GEMV has loaded it), a
+    staging kernel after the tensor-core kernel, and one after a staged GEMV
+    (its input final, read before waiting). The staging kernel lets its GEMV
+    start at once, so that GEMV may read its weights beside the kernel before
+    the staging kernel. Captured and eager runs give the bits of the calls
+    made one at a time."""
+    import bit_matvec_gb300 as tq
+    rows, cols = 8192, 5120
+    Ws = [gpu_repack(synth.pq2_0_weights(rows, cols, 70 + i), rows, cols) for i in range(3)]
+    X8 = torch.from_numpy(np.ascontiguousarray(_acts(8, cols, 71))).to(DEV)
+    X16 = torch.from_numpy(np.ascontiguousarray(_acts(16, cols, 72))).to(DEV)
+    nb = max(tq.tq_matmul_workspace_bytes(rows, cols, 8), tq.tq_matmul_workspace_bytes(rows, cols, 16))
+    assert tq.tq_matmul_workspace_bytes(rows, cols, 8) > 0
+    ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
+
+    def buffers():
+        return dict(Xq8=tq.q8K_empty(8, cols, DEV), Xq8b=tq.q8K_empty(8, cols, DEV),
+                    Xq16=tq.q8K_empty(16, cols, DEV),
+                    **{f"Y{i}": torch.full((16 if i == 2 else 8, rows), float("nan"), device=DEV)
+                       for i in range(1, 5)})
+
+    def steps(b):
+        return [
+            lambda s: tq.tq_quantize_q8K(X8, b["Xq8"], 8, cols, stream=s),
+            lambda s: tq.tq_matmul_ws(Ws[0], b["Xq8"], b["Y1"], rows, cols, 8, ws, stream=s),
+            lambda s: tq.tq_quantize_matmul(Ws[1], X16, b["Xq16"], b["Y2"], rows, cols, 16, ws,
+                                            stream=s),
+            lambda s: tq.tq_matmul_ws(Ws[2], b["Xq8"], b["Y3"], rows, cols, 8, ws, stream=s),
+            lambda s: tq.tq_quantize_matmul(Ws[0], X8, b["Xq8b"], b["Y4"], rows, cols, 8, ws,
+                                            stream=s),
+        ]
+
+    ref = buffers()
+    for step in steps(ref):
+        step(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+    assert torch.equal(_bits(ref["Y1"]), _bits(ref["Y4"]))
+    assert torch.equal(ref["Xq8"], ref["Xq8b"])
+    eager = buffers()
+    for step in steps(eager):
+        step(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    got = buffers()
+    g = _capture(lambda s: [step(s) for step in steps(got)])
+    for _ in range(2):
+        g.replay()
+        torch.cuda.synchronize()
+        for k in ref:
+            assert torch.equal(_bits(got[k]), _bits(ref[k])), k
+            assert torch.equal(_bits(eager[k]), _bits(ref[k])), k
+    assert tq.tq_device_status() == tq.TQ_OK
+    xq = oracle.quantize_q8K(_acts(8, cols, 71))
+    rows_s = np.r_[0:32, rows - 32:rows]
+    w0 = synth.pq2_0_weights(rows, cols, 70).reshape(rows, -1)
+    y_ref, abs_sum = oracle.matmul(w0[rows_s].reshape(-1), xq, len(rows_s), cols)
+    assert_close(ref["Y1"].cpu().numpy()[:, rows_s], y_ref, abs_sum)

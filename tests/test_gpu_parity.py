@@ -4,8 +4,9 @@ Bit-exact: q8_K bytes (scales, int8 values, partial sums), repacked bytes,
 and every int32 group sum. Within 1e-5 of sum_g |d_w d_x isum| per output:
 the f32 results. Sizes span several tiles with ragged tails. tq_matmul runs
 the GEMV up to 16 tokens (int8 activations in shared memory above 8) and the
-tensor cores above; the workspace forms run the GEMV up to 8 tokens and the
-tensor cores above (token tiles of 16, 32 and 64).
+tensor cores above; the workspace forms run the GEMV up to 8 tokens (from 4
+on with its activations staged once in the workspace) and the tensor cores
+above (token tiles of 16, 32 and 64).
 """
 import numpy as np
 import pytest
@@ -132,6 +133,34 @@ def test_gemv_wide_rows(rows, cols, ntok):
     _check_product(rows, cols, ntok)
 
 
+@pytest.mark.parametrize("rows,cols,ntok", [(100, 5120, 4), (40, 5120, 8), (64, 6144, 5),
+                                             (33, 9984, 8), (40, 19968, 4), (64, 3072, 7),
+                                             (64, 4096, 6), (64, 10240, 8), (40, 20224, 4)])
+def test_ws_gemv_staged_activations(rows, cols, ntok):
+    """4 to 8 tokens through the workspace forms: a staging kernel converts the
+    activations once into the GEMV's f16 rows in the workspace (tq_matmul_ws
+    from 5120 columns, tq_quantize_matmul from 3072; up to 9984 columns at 8
+    tokens, 19968 at 4, beyond which the workspace size is 0 and the calls
+    run as without one). The group sums are exact and Y is within tolerance
+    of the oracle; the fused call writes the quantizer's q8_K bytes."""
+    import bit_matvec_gb300 as tq
+    ws_bytes = tq.tq_matmul_workspace_bytes(rows, cols, ntok)
+    assert (ws_bytes > 0) == (3072 <= cols <= (9984 if ntok == 8 else 19968))
+    _check_product(rows, cols, ntok, ws=True)
+    wpq, x = _weights(rows, cols, 20 + rows % 7), _acts(ntok, cols, 30 + ntok)
+    Wtq = gpu_repack(wpq, rows, cols)
+    X = torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
+    Xq = tq.q8K_empty(ntok, cols, DEV)
+    Y = torch.full((ntok, rows), float("nan"), dtype=torch.float32, device=DEV)
+    ws = tq.workspace_empty(rows, cols, ntok, DEV)
+    ws.fill_(0xAB)
+    tq.tq_quantize_matmul(Wtq, X, Xq, Y, rows, cols, ntok, ws)
+    assert torch.equal(Xq, gpu_quantize(x))
+    y_ref, abs_sum = oracle.matmul(wpq, oracle.quantize_q8K(x), rows, cols)
+    assert_close(Y.cpu().numpy(), y_ref, abs_sum)
+    assert tq.tq_device_status() == tq.TQ_OK
+
+
 @pytest.mark.parametrize("rows,cols", SHAPES)
 @pytest.mark.parametrize("ntok", TC_TOKENS)
 def test_tc_groupsums_exact_matmul_close(rows, cols, ntok):
@@ -252,11 +281,14 @@ def test_concurrent_streams():
 
 @pytest.mark.parametrize("rows,cols,ntok", [(300, 1024, 1), (100, 768, 3), (300, 1024, 4),
                                              (64, 8192, 8), (32, 256, 8), (64, 17408, 8),
+                                             (40, 17408, 4), (40, 20224, 4),
                                              (128, 1024, 9), (128, 1024, 16), (64, 17408, 16),
                                              (100, 512, 64), (300, 1024, 65), (160, 2048, 130)])
 def test_quantize_matmul_equals_separate_calls(rows, cols, ntok):
     """The fused call gives the bits of tq_quantize_q8K + tq_matmul_ws: Xq and Y
-    (GEMV with in-CTA quantization for ntok <= 16; above, one kernel that
+    (GEMV with in-CTA quantization up to 3 tokens; from 4 to 8 a staging
+    kernel that quantizes X and stages the GEMV's activations, where they fit
+    (not at 8 x 17408 nor 4 x 20224); above, one kernel that
     quantizes and packs the workspace, including the zero padding of a
     ragged last token tile, before the tensor-core kernel)."""
     import bit_matvec_gb300 as tq

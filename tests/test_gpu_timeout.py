@@ -32,9 +32,11 @@ def test_stall_argument_checked(tq):
     tq.tq_debug_stall_next_launch(0)   # cancels; no launch involved
 
 
-# (rows, cols, ntok): the one-token dp4a GEMV, the mma.sync GEMV, the
-# tensor-core kernel of the workspace form (two token tiles)
-CASES = [(4096, 8192, 1), (4096, 5120, 4), (1024, 1024, 100)]
+# (rows, cols, ntok): the one-token dp4a GEMV, the mma.sync GEMV (staging its
+# activations itself at 1024 columns; loading them from the workspace, where
+# a staging kernel wrote them, at 5120), the tensor-core kernel of the
+# workspace form (two token tiles)
+CASES = [(4096, 8192, 1), (4096, 1024, 4), (4096, 5120, 4), (1024, 1024, 100)]
 
 
 @pytest.mark.gpu
