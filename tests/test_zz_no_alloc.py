@@ -61,13 +61,15 @@ def test_static_workspace_matches_caller_workspace(tq):
         pytest.skip("no CUDA device")
     from gpu_util import DEV, assert_close, gpu_quantize, gpu_repack
 
-    # Two calls in a row on the shared array. The first fills whole token
-    # tiles (192 = 3 x 64 tokens, no padding), so its data sits where the
-    # second call's padded token slots fall: the second (130 tokens, a ragged
-    # third tile) must not read any of it. Each result must equal the caller
-    # workspace form bit for bit (same kernels, same inputs) and the oracle
-    # within the matmul tolerance.
-    cases = [(128, 1024, 192, 2), (300, 1024, 130, 3)]
+    # Calls in a row on the shared array. The first fills whole token tiles
+    # (192 = 3 x 64 tokens, no padding), so its data sits where the second
+    # call's padded token slots fall: the second (130 tokens, a ragged third
+    # tile) must not read any of it. The third (6 tokens, 5120 columns) stages
+    # the GEMV's activations in the array over what the others left there.
+    # Each result must equal the caller workspace form bit for bit (same
+    # kernels, same inputs) and the oracle within the matmul tolerance.
+    cases = [(128, 1024, 192, 2), (300, 1024, 130, 3), (100, 5120, 6, 4)]
+    assert tq.tq_matmul_workspace_bytes(100, 5120, 6) > 0
     ins, outs = [], []
     for rows, cols, ntok, seed in cases:
         wpq, x = _case(rows, cols, ntok, seed)
