@@ -307,7 +307,7 @@ int tq_matmul_groupsums_ws(const void *Wtq, const void *Xq, int32_t *S, int64_t 
  * quantizer's place on the critical path of each matmul. From 4 to 8 tokens
  * with a workspace, one small kernel quantizes X (the same arithmetic),
  * writes Xq and stages the GEMV's activations in the workspace, then the
- * GEMV runs (measured in graph chains: 1.1-1.7x faster than the fused launch
+ * GEMV runs (measured in graph chains: 1.02-1.7x faster than the fused launch
  * from 3072 columns; 11.4 against 12.6 us at 4 tokens on 17408 x 5120).
  * For ntok >= 9 one
  * kernel quantizes X (the same arithmetic), writes Xq and packs the
