@@ -128,3 +128,20 @@ def test_source_hash_ignores_comments():
     assert "return x;" in bench.code_text(a) and "one" not in bench.code_text(a)
     # a comment line added or removed changes nothing either
     assert bench.code_text("int f();\n// added\nint g();\n") == bench.code_text("int f();\nint g();\n")
+
+
+def test_launch_count_follows_the_staging_rule():
+    """gpu_launches counts what tq_quantize_matmul enqueues: one fused GEMV, or
+    from 4 tokens where the workspace size is not 0 (3072 columns and more) a
+    staging kernel and the GEMV, and two launches on the tensor-core path."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from bit_matvec_gb300 import build
+    build.build()
+    assert bench.launches_per_matmul(32768, 8192, 1) == 1
+    assert bench.launches_per_matmul(17408, 5120, 3) == 1
+    assert bench.launches_per_matmul(17408, 5120, 4) == 2
+    assert bench.launches_per_matmul(17408, 2048, 4) == 1
+    assert bench.launches_per_matmul(17408, 5120, 64) == 2
+    assert bench.gemv_kernel_name(17408, 5120, 4).startswith("gemv_stage_kernel")
+    assert bench.gemv_kernel_name(32768, 8192, 1).startswith("gemv_kernel")
